@@ -1,0 +1,390 @@
+"""Benchmark of the Mamba-2 chunked SSD forward pass on GB300.
+
+One step = one mamba2_ssd_fwd over one batch of the long-sequence workload
+(batch 4, L 8192, 64 heads x headdim 64, state 128, 1 group, chunk 256, bf16,
+carried fp32 initial state), i.e. every stage of the path: chunk cumsum, state
+pass, chunk output.  Inputs are seeded synthetic tensors already resident in
+HBM; a 256 MiB buffer is written between timed steps so each step starts with
+a cold L2.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(the path has no exchange step), the step time is the max over ranks and the
+value is the tokens of all ranks over that time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Mamba-2 SSD fwd tokens/s and TFLOP/s at 1 GB300; % of tensor/HBM roofline"
+DEFAULT_WORKLOAD = "long_seq_carried_state"
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-pairs", type=int, default=256,
+                   help="(batch, head) pairs the oracle runs for the CPU baseline sample")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------- work
+def work_counts(w):
+    """Algorithmic FLOPs and bytes of one forward pass.
+
+    FLOPs count the causal half of every T x T product and C B^T once per
+    group: N [G (T+1) S + nh (T+1) H + 4 nh S H].  Compulsory bytes: x read,
+    y written, B, C, dt read, final state written, initial state read."""
+    N = w.batch * w.seqlen
+    e = 2 if w.dtype == "bf16" else 4
+    T, S, H, nh, G = w.chunk_size, w.dstate, w.headdim, w.nheads, w.ngroups
+    flop = N * (G * (T + 1) * S + nh * (T + 1) * H + 4 * nh * S * H)
+    flop_dense = N * (2 * G * T * S + 2 * nh * T * H + 4 * nh * S * H)
+    state = 4 * w.batch * nh * S * H
+    bytes_min = N * (2 * nh * H * e + 2 * G * S * e + 4 * nh) + state * (2 if w.init_state else 1)
+    return flop, flop_dense, bytes_min
+
+
+def kernel_bytes(w):
+    """Algorithmic bytes of one launch of each stage kernel (what it must read
+    and write once): cumsum reads dt (and A) and writes G; the state pass reads
+    x, dt, B, G (and the initial state) and writes every chunk state and the
+    final state; the output kernel reads x, dt, G, B, C, D and the chunk states
+    and writes y."""
+    N = w.batch * w.seqlen
+    e = 2 if w.dtype == "bf16" else 4
+    S, H, nh, G = w.dstate, w.headdim, w.nheads, w.ngroups
+    xb = N * nh * H * e
+    bcb = N * G * S * e
+    dtb = gb = 4 * N * nh
+    state = 4 * w.batch * nh * S * H
+    csb = w.batch * nh * w.nchunks * S * H * e
+    return {
+        "chunk_cumsum": dtb + gb + 4 * nh,
+        "state_pass": xb + dtb + bcb + gb + csb + state * (2 if w.init_state else 1),
+        "chunk_out": xb + dtb + gb + 2 * bcb + csb + xb + 4 * nh,
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            out_dir = os.path.join(ROOT, "gpurun_out")
+            os.makedirs(out_dir, exist_ok=True)
+            self.path = os.path.join(out_dir, f"bench_clocks_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ CPU baseline
+def _pick_pairs(batch, nheads, n):
+    step = max(1, (batch * nheads) // max(1, n))
+    pairs = [(i // nheads, i % nheads) for i in range(0, batch * nheads, step)][:n]
+    return pairs
+
+
+def oracle_sample_problem(w, inp, npairs):
+    """The sampled (batch, head) sequences gathered into one fp64 problem of
+    batch 1 whose heads are the sampled pairs, each its own group (a head only
+    reads its own group's B and C, so this is the same arithmetic)."""
+    import numpy as np
+    import torch
+    pairs = _pick_pairs(w.batch, w.nheads, npairs)
+    r = w.nheads // w.ngroups
+    bi = torch.tensor([b for b, _ in pairs])
+    hi = torch.tensor([h for _, h in pairs])
+    gi = hi // r
+    f64 = lambda t: np.ascontiguousarray(t.to(torch.float64).numpy())
+    prob = {
+        "x": f64(inp["x"][bi, :, hi].permute(1, 0, 2).unsqueeze(0)),
+        "dt": f64(inp["dt"][bi, :, hi].permute(1, 0).unsqueeze(0)),
+        "A": f64(inp["A"][hi]),
+        "B": f64(inp["B"][bi, :, gi].permute(1, 0, 2).unsqueeze(0)),
+        "C": f64(inp["C"][bi, :, gi].permute(1, 0, 2).unsqueeze(0)),
+        "D": f64(inp["D"][hi]),
+        "init": None if inp["initial_state"] is None else f64(inp["initial_state"][bi, hi].unsqueeze(0)),
+    }
+    return pairs, prob
+
+
+def run_oracle_sample(w, inp, npairs, prepared=None):
+    """The fp64 oracle recurrence, as it stands, on the host cores, over a
+    bounded sample: `npairs` (batch, head) sequences of the workload at full
+    length (inputs widened to fp64 before the clock starts).  Reported as
+    whole-workload tokens/s: the sample's share of the heads times batch*L
+    tokens, over the wall time of the oracle call."""
+    import oracle
+    pairs, prob = prepared if prepared is not None else oracle_sample_problem(w, inp, npairs)
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.ssd_recurrence(prob["x"], prob["dt"], prob["A"], prob["B"], prob["C"], D=prob["D"],
+                          init=prob["init"], nthreads=cores)
+    dt = time.perf_counter() - t0
+    frac = len(pairs) / (w.batch * w.nheads)
+    return {"value": frac * w.tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{len(pairs)} of {w.batch * w.nheads} (batch, head) sequences at full length "
+                      f"L={w.seqlen}; fp64 token-by-token recurrence, pthreads over sequences; "
+                      f"tokens/s scaled by the fraction of sequences covered"}
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_gpu(args, w, rank, world):
+    import torch
+    import torch.distributed as dist
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300 import build_lib
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    build_lib.build()
+    bd.load_library()
+    inp = make_inputs(w, seed=w.seed + rank)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    stream = torch.cuda.current_stream()
+    shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
+    ws = torch.empty(max(bd.mamba2_ssd_fwd_workspace_size(shape), 1), device="cuda", dtype=torch.uint8)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty(w.batch, w.nheads, w.dstate, w.headdim, device="cuda", dtype=torch.float32)
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+
+    def step():
+        bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size, D=d["D"],
+                          initial_state=d["initial_state"], y=y, final_state=fin, workspace=ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    bd.mamba2_check_device_status()
+
+    # ---- timed region: K steps, cold L2 before each
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    barrier()
+    clock_info = clocks.stop()
+    bd.mamba2_check_device_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- per-kernel durations: the same launches through the per-stage entry points
+    kev = {k: [] for k in ("chunk_cumsum", "state_pass", "chunk_out")}
+    G = ws[: 4 * w.batch * w.nheads * w.seqlen].view(torch.float32).view(w.batch, w.nheads, w.seqlen)
+    cs = torch.empty(w.batch, w.nheads, w.nchunks, w.dstate, w.headdim, device="cuda", dtype=d["x"].dtype)
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        bd.mamba2_chunk_cumsum(d["dt"], d["A"], w.chunk_size, G=G)
+        e[1].record(stream)
+        bd.mamba2_state_pass(d["x"], d["dt"], d["B"], G, w.chunk_size, initial_state=d["initial_state"],
+                             chunk_states=cs, final_state=fin)
+        e[2].record(stream)
+        bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], G, cs, w.chunk_size, D=d["D"], y=y)
+        e[3].record(stream)
+        if i >= args.warmup:
+            kev["chunk_cumsum"].append((e[0], e[1]))
+            kev["state_pass"].append((e[1], e[2]))
+            kev["chunk_out"].append((e[2], e[3]))
+    torch.cuda.synchronize()
+    kernel_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in kev.items()}
+
+    # ---- end to end through the public API with host buffers
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    fin_host = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = y_host.numel() * y_host.element_size() + fin_host.numel() * fin_host.element_size()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k, v in host.items():
+            if v is not None:
+                d[k].copy_(v, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+        fin_host.copy_(fin, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    return {"total_ms": total_ms, "step_ms": step_ms, "kernel_ms": kernel_ms, "clocks": clock_info,
+            "e2e_ms": e2e_total, "h2d": h2d, "d2h": d2h, "inp": inp}
+
+
+def main():
+    args = parse_args()
+    from mamba_chunked_ssd_gb300.synthetic import WORKLOADS
+    w = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return main_reference(args, w, rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = run_gpu(args, w, rank, world)
+    if rank != 0:
+        return
+    flop, flop_dense, bytes_min = work_counts(w)
+    peaks = load_peaks()
+    ms = r["total_ms"] / args.steps
+    tokens = w.tokens * world
+    value = tokens / (ms * 1e-3)
+    kb = kernel_bytes(w)
+    top = max(r["kernel_ms"], key=r["kernel_ms"].get)
+    achieved = kb[top] / (r["kernel_ms"][top] * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
+                   "chunk_size": w.chunk_size, "initial_state": w.init_state,
+                   "l2": "flushed: 256 MiB buffer written before every timed step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tflops": flop / (ms * 1e-3) / 1e12 * world,
+        "tflops_dense_convention": flop_dense / (ms * 1e-3) / 1e12 * world,
+        "step_roofline": {"bytes_min": bytes_min, "flop_alg": flop,
+                          "hbm_frac": bytes_min / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                          "tensor_frac": flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                          "peaks": peaks["source"]},
+        "roofline": {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None},
+        "kernel_ms": r["kernel_ms"],
+        "gpu_launches": 3 * args.steps,
+        "e2e": {"value": tokens / (r["e2e_ms"] / args.steps * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = run_oracle_sample(w, r["inp"], args.cpu_pairs)
+        out["cpu_baseline"].pop("seconds", None)
+    print(json.dumps(out), flush=True)
+
+
+def main_reference(args, w, rank):
+    """The reference arm: the fp64 CPU oracle, as it stands, on host cores.
+    Each step is a bounded sample of the workload (see run_oracle_sample)."""
+    if rank != 0:
+        return
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+    inp = make_inputs(w)
+    prepared = oracle_sample_problem(w, inp, args.cpu_pairs)
+    small = oracle_sample_problem(w, inp, max(1, args.cpu_pairs // 8))
+    for _ in range(args.warmup):
+        run_oracle_sample(w, inp, 0, prepared=small)
+    runs = [run_oracle_sample(w, inp, args.cpu_pairs, prepared=prepared) for _ in range(args.steps)]
+    secs = sum(r["seconds"] for r in runs)
+    frac_tokens = sum(r["value"] * r["seconds"] for r in runs)
+    value = frac_tokens / secs
+    ms = secs / args.steps * 1e3
+    cb = {k: v for k, v in runs[0].items() if k != "seconds"}
+    cb["value"] = value
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                      "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
+                      "chunk_size": w.chunk_size, "initial_state": w.init_state},
+           "cpu_baseline": cb,
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

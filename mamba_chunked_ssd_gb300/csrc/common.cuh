@@ -1,0 +1,92 @@
+// common.cuh — small helpers shared by the CUDA translation units of the
+// library (element conversion, problem geometry, internal launch interface).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mamba2_ssd.h"
+
+namespace m2 {
+
+// log2(e) rounded to fp32: stage 1 scales the natural-log cumsum by it so the
+// later stages can use exp2 [blog §Kernel 1].
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Problem geometry resolved once on the host and passed by value to kernels.
+struct Geom {
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk;
+    int64_t nchunks;      // ceil(seqlen / chunk)
+    int64_t heads_per_group;
+};
+
+inline Geom make_geom(const mamba2_shape& s) {
+    Geom g;
+    g.batch = s.batch;
+    g.seqlen = s.seqlen;
+    g.nheads = s.nheads;
+    g.headdim = s.headdim;
+    g.dstate = s.dstate;
+    g.ngroups = s.ngroups;
+    g.chunk = s.chunk_size;
+    g.nchunks = (s.seqlen + s.chunk_size - 1) / s.chunk_size;
+    g.heads_per_group = s.nheads / s.ngroups;
+    return g;
+}
+
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Status word values written by kernels (mirrors mamba2_status codes).
+constexpr unsigned int kStatusTimeout = MAMBA2_ERR_TIMEOUT;
+
+// ---------------------------------------------------------------- launchers
+// Each returns the cudaError_t of its launch(es).  Arguments were validated
+// by the C-ABI layer; pointers are device pointers.
+struct StatePassArgs {
+    const void* x;
+    const float* dt;
+    const void* B;
+    const float* G;
+    const float* init;  // may be null
+    void* chunk_states;
+    float* final_state;  // may be null
+};
+
+struct ChunkOutArgs {
+    const void* x;
+    const float* dt;
+    const void* B;
+    const void* C;
+    const float* D;  // may be null
+    const float* G;
+    const void* chunk_states;
+    void* y;
+};
+
+cudaError_t launch_chunk_cumsum(const Geom& g, const float* dt, const float* A, float* G,
+                                cudaStream_t st);
+cudaError_t launch_state_pass_simt(const Geom& g, bool bf16, const StatePassArgs& a, cudaStream_t st);
+cudaError_t launch_chunk_out_simt(const Geom& g, bool bf16, const ChunkOutArgs& a, cudaStream_t st);
+
+// Dispatchers: pick the tensor-core kernel when the shape has one, else the
+// CUDA-core kernel (dispatch.cu).
+cudaError_t launch_state_pass(const Geom& g, bool bf16, const StatePassArgs& a, cudaStream_t st);
+cudaError_t launch_chunk_out(const Geom& g, bool bf16, const ChunkOutArgs& a, cudaStream_t st);
+
+// Device address of the current device's status word (api.cu).
+unsigned int* device_status_word();
+
+}  // namespace m2

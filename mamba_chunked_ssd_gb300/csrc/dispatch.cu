@@ -1,0 +1,14 @@
+// dispatch.cu — chooses the kernel that runs each stage for a given shape.
+#include "common.cuh"
+
+namespace m2 {
+
+cudaError_t launch_state_pass(const Geom& g, bool bf16, const StatePassArgs& a, cudaStream_t st) {
+    return launch_state_pass_simt(g, bf16, a, st);
+}
+
+cudaError_t launch_chunk_out(const Geom& g, bool bf16, const ChunkOutArgs& a, cudaStream_t st) {
+    return launch_chunk_out_simt(g, bf16, a, st);
+}
+
+}  // namespace m2

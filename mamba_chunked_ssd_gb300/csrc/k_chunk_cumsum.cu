@@ -1,0 +1,85 @@
+// k_chunk_cumsum.cu — stage 1, the intra-chunk log2-space cumsum of a_t.
+//
+// [blog §Kernel 1] "Computing cumulative sums": per (batch, chunk) the
+// effective decay a[h] * dt[t, h] is summed along the chunk's tokens for every
+// head and scaled by log2(e).  [blog §Mamba-2 performance optimization, GMEM
+// layout]: the result is stored head-major, G[b, h, t], so that the later
+// stages read one head's decays as one contiguous run.
+//
+// GB300 mapping: one CTA per (chunk, block of 32 heads, batch).  dt rows of 32
+// heads (128 B) are read coalesced into shared memory, each warp scans whole
+// heads (per-lane serial prefix + warp-shuffle scan of the lane totals), and
+// the tile is written back transposed, coalesced along t.  Pure streaming.
+#include "common.cuh"
+
+namespace m2 {
+namespace {
+
+constexpr int kHeadsPerCta = 32;
+constexpr int kThreads = 256;
+constexpr int kMaxChunk = 256;
+
+__global__ void __launch_bounds__(kThreads)
+k_chunk_cumsum(const float* __restrict__ dt, const float* __restrict__ A, float* __restrict__ G,
+               Geom g) {
+    __shared__ float tile[kMaxChunk][kHeadsPerCta + 1];
+    const int64_t c = blockIdx.x;
+    const int64_t h0 = (int64_t)blockIdx.y * kHeadsPerCta;
+    const int64_t b = blockIdx.z;
+    const int64_t t0 = c * g.chunk;
+    const int tc = (int)imin64(g.chunk, g.seqlen - t0);  // valid tokens (ragged tail)
+    const int nh_here = (int)imin64(kHeadsPerCta, g.nheads - h0);
+
+    // a_t = A[h] * dt[b, t, h], coalesced over heads.
+    for (int i = threadIdx.x; i < tc * kHeadsPerCta; i += kThreads) {
+        const int t = i / kHeadsPerCta, hh = i % kHeadsPerCta;
+        float v = 0.f;
+        if (hh < nh_here) v = A[h0 + hh] * dt[(b * g.seqlen + t0 + t) * g.nheads + h0 + hh];
+        tile[t][hh] = v;
+    }
+    __syncthreads();
+
+    // Inclusive scan along t, one warp per head.
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int per_lane = (tc + 31) / 32;
+    for (int hh = warp; hh < nh_here; hh += kThreads / 32) {
+        const int lo = lane * per_lane;
+        const int hi = min(lo + per_lane, tc);
+        float run = 0.f;
+        for (int t = lo; t < hi; ++t) {
+            run += tile[t][hh];
+            tile[t][hh] = run;
+        }
+        // exclusive prefix of the lane totals, formed from lower lanes only
+        // (never as inclusive - own), so G_t cannot depend on tokens after t
+        float incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += n;
+        }
+        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) excl = 0.f;
+        for (int t = lo; t < hi; ++t) tile[t][hh] = (tile[t][hh] + excl) * kLog2e;
+    }
+    __syncthreads();
+
+    // G[b, h, t0 + t], coalesced along t.
+    for (int hh = warp; hh < nh_here; hh += kThreads / 32) {
+        float* out = G + ((b * g.nheads) + h0 + hh) * g.seqlen + t0;
+        for (int t = lane; t < tc; t += 32) out[t] = tile[t][hh];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_cumsum(const Geom& g, const float* dt, const float* A, float* G,
+                                cudaStream_t st) {
+    if (g.batch == 0 || g.seqlen == 0) return cudaSuccess;
+    dim3 grid((unsigned)g.nchunks, (unsigned)((g.nheads + kHeadsPerCta - 1) / kHeadsPerCta),
+              (unsigned)g.batch);
+    k_chunk_cumsum<<<grid, kThreads, 0, st>>>(dt, A, G, g);
+    return cudaGetLastError();
+}
+
+}  // namespace m2

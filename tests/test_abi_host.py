@@ -1,0 +1,115 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/mamba2_ssd.h declares, and rejects bad arguments on the host before
+any CUDA call (fake pointer values are never dereferenced on these paths)."""
+import ctypes
+
+import pytest
+
+from mamba_chunked_ssd_gb300 import binding as bd
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mamba_chunked_ssd_gb300 import build_lib
+    build_lib.build()
+    return bd.load_library()
+
+
+def test_exports_every_declared_function(lib):
+    names = bd.header_functions()
+    assert len(names) == 8
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in the header but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.mamba2_version() == 10000
+    for code in range(5):
+        s = lib.mamba2_status_string(code).decode()
+        assert s.startswith(bd.STATUS[code])
+
+
+def _shape(**kw):
+    d = dict(batch=1, seqlen=64, nheads=2, headdim=16, dstate=16, ngroups=1, chunk_size=64, dtype_code=0)
+    d.update(kw)
+    return bd.make_shape(d["batch"], d["seqlen"], d["nheads"], d["headdim"], d["dstate"],
+                         d["ngroups"], d["chunk_size"], d["dtype_code"])
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def _cumsum(lib, shape, dt=FAKE, A=FAKE * 2, G=FAKE * 64):
+    return lib.mamba2_chunk_cumsum(ctypes.byref(shape) if shape is not None else None,
+                                   _p(dt), _p(A), _p(G), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype_code=7), INVALID),
+    (dict(nheads=3, ngroups=2), INVALID),
+    (dict(chunk_size=0), INVALID),
+    (dict(headdim=0), INVALID),
+    (dict(batch=-1), INVALID),
+    (dict(seqlen=-5), INVALID),
+    (dict(headdim=512), UNSUPPORTED),
+    (dict(dstate=300), UNSUPPORTED),
+    (dict(chunk_size=512), UNSUPPORTED),
+    (dict(batch=70000), UNSUPPORTED),
+])
+def test_shape_validation(lib, kw, code):
+    assert _cumsum(lib, _shape(**kw)) == code
+
+
+def test_null_shape(lib):
+    assert _cumsum(lib, None) == INVALID
+    assert lib.mamba2_ssd_fwd_workspace_size(None) == 0
+
+
+def test_reserved_must_be_zero(lib):
+    s = _shape()
+    s.reserved = 1
+    assert _cumsum(lib, s) == INVALID
+
+
+def test_null_and_misaligned_pointers(lib):
+    s = _shape()
+    assert _cumsum(lib, s, dt=0) == INVALID
+    assert _cumsum(lib, s, G=FAKE * 64 + 4) == INVALID
+    assert _cumsum(lib, s, A=FAKE * 2 + 8) == INVALID
+
+
+def test_output_aliasing_input_is_rejected(lib):
+    s = _shape()
+    # G [1, 2, 64] fp32 = 512 bytes written over dt's bytes
+    assert _cumsum(lib, s, dt=FAKE, G=FAKE + 256) == INVALID
+
+
+def test_chunk_out_rejects_y_aliasing_x(lib):
+    s = _shape(dtype_code=1)
+    args = [ctypes.byref(s)] + [_p(FAKE * (i + 1) * 16) for i in range(7)] + [_p(FAKE * 16), None]
+    assert lib.mamba2_chunk_out(*args) == INVALID
+
+
+def test_workspace_size(lib):
+    s = _shape(batch=2, seqlen=100, nheads=4, headdim=16, dstate=8, chunk_size=32, dtype_code=1)
+    nc = 4
+    g_bytes = 2 * 4 * 100 * 4
+    cs_bytes = 2 * 4 * nc * 8 * 16 * 2
+    up = lambda v: (v + 255) // 256 * 256
+    assert lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s)) == up(g_bytes) + up(cs_bytes)
+
+
+def test_ssd_fwd_rejects_small_or_misaligned_workspace(lib):
+    s = _shape()
+    need = lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s))
+    ptrs = [_p(FAKE * (i + 1) * 64) for i in range(9)]
+    small = lib.mamba2_ssd_fwd(ctypes.byref(s), *ptrs, _p(FAKE * 4096), need - 1, None)
+    assert small == INVALID
+    misaligned = lib.mamba2_ssd_fwd(ctypes.byref(s), *ptrs, _p(FAKE * 4096 + 16), need, None)
+    assert misaligned == INVALID

@@ -1,0 +1,138 @@
+"""Per-stage GPU parity: each C-ABI stage against the fp64 oracle, fed the
+same inputs (the oracle's own intermediates where a stage needs them).
+
+Stage 1 (chunk_cumsum): |G - G_ref| <= 1e-5 max(1, |G_ref|), plus a bit-exact
+layout check.  Stages 2 and 3: max|err| / max|ref| <= 2e-2 (bf16) / 1e-4
+(fp32), plus the exact special cases (dt = 0, B = C = 0, chunk 0's state).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import TOL, np64, rel_err, to_dev
+from mamba_chunked_ssd_gb300 import binding as bd
+from mamba_chunked_ssd_gb300.synthetic import Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+# name, b, L, nh, H, S, G, T, dtype, init
+SHAPES = [
+    ("fp32_tiny", 1, 256, 2, 16, 16, 1, 64, "fp32", False),
+    ("fp32_ragged", 2, 203, 3, 16, 32, 1, 64, "fp32", True),
+    ("fp32_small_chunk", 1, 100, 4, 32, 16, 2, 16, "fp32", True),
+    ("bf16_t128", 2, 384, 4, 64, 64, 2, 128, "bf16", True),
+    ("bf16_t256", 1, 512, 3, 64, 128, 1, 256, "bf16", True),
+    ("bf16_t256_ragged", 2, 700, 2, 64, 128, 1, 256, "bf16", False),
+    ("bf16_h128_s256", 1, 256, 4, 128, 256, 2, 128, "bf16", True),
+    ("bf16_t128_ragged", 1, 333, 4, 128, 64, 4, 128, "bf16", True),
+]
+
+
+def _w(name, b, L, nh, H, S, G, T, dtype, init, seed=0):
+    return Workload(name, b, L, nh, H, S, G, T, dtype=dtype, init_state=init, seed=seed)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from mamba_chunked_ssd_gb300 import build_lib
+    build_lib.build()
+    bd.load_library()
+
+
+@pytest.mark.parametrize("spec", SHAPES, ids=[s[0] for s in SHAPES])
+def test_chunk_cumsum_matches_oracle(spec):
+    w = _w(*spec)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    G = bd.mamba2_chunk_cumsum(d["dt"], d["A"], w.chunk_size)
+    bd.mamba2_check_device_status()
+    Gref = oracle.chunk_cumsum(inp["dt"], inp["A"], w.chunk_size)
+    err = np.abs(np64(G) - Gref) / np.maximum(1.0, np.abs(Gref))
+    assert err.max() <= 1e-5, err.max()
+
+
+def test_chunk_cumsum_bit_exact_layout():
+    """With A a power of two and dt on a 2^-12 grid every partial sum is exact
+    in fp32, so G = fl(sum * log2e) exactly: any indexing or layout slip shows."""
+    b, L, nh, T = 2, 300, 37, 64
+    g = torch.Generator().manual_seed(5)
+    dt = (torch.randint(1, 64, (b, L, nh), generator=g).float() / 4096.0)
+    A = torch.tensor([-(2.0 ** (k % 3)) for k in range(nh)], dtype=torch.float32)
+    G = bd.mamba2_chunk_cumsum(dt.cuda(), A.cuda(), T).cpu()
+    a = (A[None, None, :] * dt).double().numpy()  # exact
+    ref = np.zeros((b, nh, L), dtype=np.float32)
+    for c0 in range(0, L, T):
+        run = np.cumsum(a[:, c0:c0 + T], axis=1)  # exact sums of grid values
+        ref[:, :, c0:c0 + T] = (run.astype(np.float32) * np.float32(1.4426950408889634)).transpose(0, 2, 1)
+    assert np.array_equal(G.numpy(), ref)
+
+
+def _oracle_stage_inputs(inp, w):
+    """Oracle G rounded to fp32 (what the GPU stages consume) and the oracle's
+    chunk states computed from that same G."""
+    G32 = oracle.chunk_cumsum(inp["dt"], inp["A"], w.chunk_size).astype(np.float32)
+    cs, fin = oracle.state_pass(inp["x"], inp["dt"], inp["B"], G32, w.chunk_size,
+                                init=inp["initial_state"])
+    return G32, cs, fin
+
+
+@pytest.mark.parametrize("spec", SHAPES, ids=[s[0] for s in SHAPES])
+def test_state_pass_matches_oracle(spec):
+    w = _w(*spec)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    G32, cs_ref, fin_ref = _oracle_stage_inputs(inp, w)
+    cs, fin = bd.mamba2_state_pass(d["x"], d["dt"], d["B"], torch.from_numpy(G32).cuda(),
+                                   w.chunk_size, initial_state=d["initial_state"])
+    bd.mamba2_check_device_status()
+    tol = TOL[w.dtype]
+    assert rel_err(np64(cs), cs_ref) <= tol
+    assert rel_err(np64(fin), fin_ref) <= tol
+
+
+@pytest.mark.parametrize("spec", SHAPES, ids=[s[0] for s in SHAPES])
+def test_chunk_out_matches_oracle(spec):
+    w = _w(*spec)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    G32, cs_ref, _ = _oracle_stage_inputs(inp, w)
+    cs_dev = torch.from_numpy(cs_ref).to(d["x"].dtype).cuda()  # rounded like stored states
+    y = bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], torch.from_numpy(G32).cuda(), cs_dev,
+                            w.chunk_size, D=d["D"])
+    bd.mamba2_check_device_status()
+    y_ref = oracle.chunk_out(inp["x"], inp["dt"], inp["B"], inp["C"], G32, cs_dev.cpu(), w.chunk_size,
+                             D=inp["D"])
+    assert rel_err(np64(y), y_ref) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("spec", [s for s in SHAPES if s[-1]], ids=[s[0] for s in SHAPES if s[-1]])
+def test_state_pass_exact_cases(spec):
+    """dt = 0 leaves the state untouched (exp2(0) = 1, added terms exactly 0),
+    and chunk 0's stored state is the initial state rounded to dtype."""
+    w = _w(*spec)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    zero_dt = torch.zeros_like(d["dt"])
+    G = bd.mamba2_chunk_cumsum(zero_dt, d["A"], w.chunk_size)
+    cs, fin = bd.mamba2_state_pass(d["x"], zero_dt, d["B"], G, w.chunk_size,
+                                   initial_state=d["initial_state"])
+    assert torch.equal(fin, d["initial_state"])
+    G = bd.mamba2_chunk_cumsum(d["dt"], d["A"], w.chunk_size)
+    cs, _ = bd.mamba2_state_pass(d["x"], d["dt"], d["B"], G, w.chunk_size,
+                                 initial_state=d["initial_state"])
+    assert torch.equal(cs[:, :, 0], d["initial_state"].to(cs.dtype))
+
+
+@pytest.mark.parametrize("spec", SHAPES, ids=[s[0] for s in SHAPES])
+def test_chunk_out_skip_only_is_exact(spec):
+    """B = C = 0 leaves only the skip term: y = fl(D x), rounded once to dtype."""
+    w = _w(*spec)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    zB = torch.zeros_like(d["B"])
+    G = bd.mamba2_chunk_cumsum(d["dt"], d["A"], w.chunk_size)
+    cs = torch.randn(w.batch, w.nheads, w.nchunks, w.dstate, w.headdim, device="cuda").to(d["x"].dtype)
+    y = bd.mamba2_chunk_out(d["x"], d["dt"], zB, zB, G, cs, w.chunk_size, D=d["D"])
+    ref = (d["D"][None, None, :, None] * d["x"].float()).to(d["x"].dtype)
+    assert torch.equal(y, ref)
