@@ -81,6 +81,12 @@ cudaError_t launch_chunk_cumsum(const Geom& g, const float* dt, const float* A, 
 cudaError_t launch_state_pass_simt(const Geom& g, bool bf16, const StatePassArgs& a, cudaStream_t st);
 cudaError_t launch_chunk_out_simt(const Geom& g, bool bf16, const ChunkOutArgs& a, cudaStream_t st);
 
+// Tensor-core kernels (bf16) and the shapes they cover.
+bool chunk_out_tc_fits(const Geom& g);
+cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream_t st);
+bool state_pass_tc_fits(const Geom& g);
+cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStream_t st);
+
 // Dispatchers: pick the tensor-core kernel when the shape has one, else the
 // CUDA-core kernel (dispatch.cu).
 cudaError_t launch_state_pass(const Geom& g, bool bf16, const StatePassArgs& a, cudaStream_t st);

@@ -1,0 +1,343 @@
+// k_state_pass_tc.cu — stage 2 on the 5th-generation tensor cores (bf16).
+//
+// [blog §Kernel 2]: for c = 0 .. nc-1 store h_c, then
+//     h_{c+1} = exp2(G_last) h_c + (w . B_c)^T X_c,   w_t = dt_t exp2(G_last - G_t).
+// GB300 design.  One CTA owns (batch, head, 128-row tile of the S x H state)
+// and walks the chunks in order:
+//   warp 0      TMA producer: 64-token sub-blocks of B (the tile's 128 state
+//               columns) and of X, through a ring of shared-memory stages;
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
+//               U_c = B_c^T (w . X_c) accumulated over the chunk's sub-blocks
+//               into one of two TMEM buffers (A = B_c^T and B = w . X_c are
+//               both read "MN-major" straight from the TMA layout);
+//   warps 2..5  fold the weights w_t into the X rows in shared memory (so the
+//               weighted operand is formed once, on chip), and run the scan:
+//               the state h lives in TMEM next to U; per chunk each thread
+//               (one state row) stores h_c, then sets h <- exp2(G_last) h + U_c.
+// The weighted-operand fold applies the blog's "pre-multiplied operand" to X
+// instead of B (same product; X is the smaller per-head tile).  States past
+// dstate (when dstate = 64) are zero-filled by TMA and never stored.
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "tmap_host.cuh"
+
+namespace m2 {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kWorkWarps = 4;
+constexpr int kKb = 64;  // tokens per sub-block
+constexpr int kMaxStages = 8;
+constexpr int kSmemLimit = 232448;
+
+struct SpTcParams {
+    Geom g;
+    int nsb;            // sub-blocks per chunk = chunk / 64
+    int nst;            // ring stages
+    uint32_t stage_bytes, off_x_in_stage, off_bar, smem_bytes, tmem_cols;
+    const float* dt;
+    const float* G;
+    const float* init;
+    __nv_bfloat16* chunk_states;
+    float* final_state;
+    unsigned int* status;
+};
+
+enum : int {
+    kBarUDone = 0,     // [2]
+    kBarUFree = 2,     // [2]
+    kBarFull = 4,      // [kMaxStages]
+    kBarXform = 4 + kMaxStages,
+    kBarSlotFree = 4 + 2 * kMaxStages,
+    kNumBars = 4 + 3 * kMaxStages
+};
+
+struct SharedCtl {
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) {
+    ctl->abort = 1;
+    if (status) atomicExch(status, kStatusTimeout);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+                const SpTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Geom& g = p.g;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int mt = blockIdx.x;              // 128-row tile of the state
+    const int h = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    const int64_t bh = b * g.nheads + h;
+    const int grp = (int)(h / g.heads_per_group);
+    const int S = (int)g.dstate, H = (int)g.headdim;
+    const int nsub = (int)g.nchunks * p.nsb;  // total sub-blocks
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + p.off_bar + kNumBars * 8);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&bars[kBarUDone + i], 1);
+            tc::mbar_init(&bars[kBarUFree + i], kWorkWarps);
+        }
+        for (int i = 0; i < kMaxStages; ++i) {
+            tc::mbar_init(&bars[kBarFull + i], 1);
+            tc::mbar_init(&bars[kBarXform + i], kWorkWarps);
+            tc::mbar_init(&bars[kBarSlotFree + i], 1);
+        }
+        ctl->abort = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&ctl->tmem_base, p.tmem_cols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const uint32_t tm_u0 = tmem;           // U buffers: [0, H), [H, 2H)
+    const uint32_t tm_h = tmem + 2 * H;    // running state: [2H, 3H)
+    volatile int* abort_flag = &ctl->abort;
+    const uint32_t x_box_bytes = kKb * 128;
+
+    if (warp == 0) {
+        // =========================== TMA producer ===========================
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tm_x);
+            tc::tma_prefetch_desc(&tm_b);
+            bool ok = true;
+            for (int u = 0; u < nsub; ++u) {
+                const int st = u % p.nst;
+                if (u >= p.nst && !tc::mbar_wait(&bars[kBarSlotFree + st], ((u / p.nst) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int c = u / p.nsb, sb = u % p.nsb;
+                const int tok = (int)(c * g.chunk + sb * kKb);
+                uint8_t* sB = smem + st * p.stage_bytes;
+                uint8_t* sX = sB + p.off_x_in_stage;
+                tc::mbar_arrive_expect_tx(&bars[kBarFull + st], (2 + H / 64) * x_box_bytes);
+                for (int kb = 0; kb < 2; ++kb)
+                    tc::tma_load_4d(sB + kb * x_box_bytes, &tm_b, &bars[kBarFull + st], mt * 128 + kb * 64, grp, tok,
+                                    (int)b);
+                for (int cb = 0; cb < H / 64; ++cb)
+                    tc::tma_load_4d(sX + cb * x_box_bytes, &tm_x, &bars[kBarFull + st], cb * 64, h, tok, (int)b);
+            }
+            if (!ok) set_abort(ctl, p.status);
+        }
+    } else if (warp == 1) {
+        // ============================ MMA issuer ============================
+        if (lane == 0) {
+            bool ok = true;
+            // A = B_c^T (rows of the box are tokens = K, columns are states = M),
+            // B = w . X_c (rows tokens = K, columns head dim = N): both MN-major.
+            const uint32_t idesc = tc::idesc_bf16(128, H, true, true);
+            for (int u = 0; u < nsub; ++u) {
+                const int st = u % p.nst, c = u / p.nsb, sb = u % p.nsb, ub = c & 1;
+                if (sb == 0 && c >= 2 && !tc::mbar_wait(&bars[kBarUFree + ub], ((c >> 1) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (!tc::mbar_wait(&bars[kBarXform + st], (u / p.nst) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t aB = tc::smem_u32(smem + st * p.stage_bytes);
+                const uint32_t aX = aB + p.off_x_in_stage;
+                for (int k16 = 0; k16 < kKb / 16; ++k16) {
+                    const uint64_t da = tc::sdesc_sw128(aB + k16 * 2048, x_box_bytes, 1024);
+                    const uint64_t db = tc::sdesc_sw128(aX + k16 * 2048, x_box_bytes, 1024);
+                    tc::mma_bf16_ss(tm_u0 + ub * H, da, db, idesc, (sb > 0 || k16 > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(&bars[kBarSlotFree + st]);
+                if (sb == p.nsb - 1) tc::mma_commit(&bars[kBarUDone + ub]);
+            }
+            if (!ok) set_abort(ctl, p.status);
+        }
+    } else {
+        // ================= weight fold + scan (warps 2..5) =================
+        const int et = (warp - 2) * 32 + lane;   // 0..127
+        const int q = warp & 3;
+        const int s_local = q * 32 + lane;
+        const int s = mt * 128 + s_local;
+        const bool valid = s < S;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        const float* Gbh = p.G + bh * g.seqlen;
+
+        // h <- initial state (or zeros), kept in TMEM columns [2H, 3H)
+        for (int m = 0; m < H / 32; ++m) {
+            uint32_t r[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                r[e] = __float_as_uint((valid && p.init) ? p.init[(bh * S + s) * H + 32 * m + e] : 0.f);
+            tc::tmem_st32(tm_h + lane_base + 32 * m, r);
+        }
+        tc::tmem_wait_st();
+
+        // Fold w_t into the X rows of sub-block u (two threads per token row).
+        auto fold = [&](int u) -> bool {
+            const int st = u % p.nst, c = u / p.nsb, sb = u % p.nsb;
+            const int64_t t0 = c * g.chunk;
+            const int tc = (int)imin64(g.chunk, g.seqlen - t0);
+            const int row = et & 63, half = et >> 6;
+            const int tl = sb * kKb + row;
+            float w = 0.f;
+            if (tl < tc) {
+                const float g_last = Gbh[t0 + tc - 1];
+                w = p.dt[(b * g.seqlen + t0 + tl) * g.nheads + h] * exp2f(g_last - Gbh[t0 + tl]);
+            }
+            if (!tc::mbar_wait(&bars[kBarFull + st], (u / p.nst) & 1, abort_flag)) return false;
+            uint8_t* sX = smem + st * p.stage_bytes + p.off_x_in_stage;
+            const int per = 4 * (H / 64);  // 16-byte chunks per thread
+            for (int f = half * per; f < (half + 1) * per; ++f) {
+                const int box = f >> 3, pc = ((f & 7) + row) & 7;  // rotate to spread banks
+                uint4* ptr = reinterpret_cast<uint4*>(sX + box * x_box_bytes + row * 128 + pc * 16);
+                uint4 v = *ptr;
+                v.x = tc::pack_bf16x2(tc::bf16_lo(v.x) * w, tc::bf16_hi(v.x) * w);
+                v.y = tc::pack_bf16x2(tc::bf16_lo(v.y) * w, tc::bf16_hi(v.y) * w);
+                v.z = tc::pack_bf16x2(tc::bf16_lo(v.z) * w, tc::bf16_hi(v.z) * w);
+                v.w = tc::pack_bf16x2(tc::bf16_lo(v.w) * w, tc::bf16_hi(v.w) * w);
+                *ptr = v;
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[kBarXform + st]);
+            return true;
+        };
+
+        // Store h_c, then h <- exp2(G_last) h + U_c.
+        auto scan = [&](int c) -> bool {
+            const int ub = c & 1;
+            const int64_t t0 = c * g.chunk;
+            const int tc = (int)imin64(g.chunk, g.seqlen - t0);
+            const float alpha = exp2f(Gbh[t0 + tc - 1]);
+            if (!tc::mbar_wait(&bars[kBarUDone + ub], (c >> 1) & 1, abort_flag)) return false;
+            tc::tc_fence_after();
+            __nv_bfloat16* dst = p.chunk_states + ((bh * g.nchunks + c) * S + s) * H;
+            for (int m = 0; m < H / 32; ++m) {
+                uint32_t hv[32], uv[32];
+                tc::tmem_ld32(tm_h + lane_base + 32 * m, hv);
+                tc::tmem_ld32(tm_u0 + ub * H + lane_base + 32 * m, uv);
+                if (valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * m);
+#pragma unroll
+                    for (int s4 = 0; s4 < 4; ++s4) {
+                        const int e = 8 * s4;
+                        d4[s4] = make_uint4(
+                            tc::pack_bf16x2(__uint_as_float(hv[e]), __uint_as_float(hv[e + 1])),
+                            tc::pack_bf16x2(__uint_as_float(hv[e + 2]), __uint_as_float(hv[e + 3])),
+                            tc::pack_bf16x2(__uint_as_float(hv[e + 4]), __uint_as_float(hv[e + 5])),
+                            tc::pack_bf16x2(__uint_as_float(hv[e + 6]), __uint_as_float(hv[e + 7])));
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
+                tc::tmem_st32(tm_h + lane_base + 32 * m, hv);
+            }
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[kBarUFree + ub]);
+            return true;
+        };
+
+        bool ok = true;
+        for (int sb = 0; ok && sb < p.nsb; ++sb) ok = fold(sb);
+        for (int c = 0; ok && c < (int)g.nchunks; ++c) {
+            if (c + 1 < (int)g.nchunks)
+                for (int sb = 0; ok && sb < p.nsb; ++sb) ok = fold((c + 1) * p.nsb + sb);
+            if (ok) ok = scan(c);
+        }
+        if (ok && p.final_state && valid) {
+            for (int m = 0; m < H / 32; ++m) {
+                uint32_t hv[32];
+                tc::tmem_ld32(tm_h + lane_base + 32 * m, hv);
+                float4* d4 = reinterpret_cast<float4*>(p.final_state + (bh * S + s) * H + 32 * m);
+#pragma unroll
+                for (int s4 = 0; s4 < 8; ++s4)
+                    d4[s4] = make_float4(__uint_as_float(hv[4 * s4]), __uint_as_float(hv[4 * s4 + 1]),
+                                         __uint_as_float(hv[4 * s4 + 2]), __uint_as_float(hv[4 * s4 + 3]));
+            }
+        }
+        if (!ok) set_abort(ctl, p.status);
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+bool plan(const Geom& g, SpTcParams& p) {
+    const int H = (int)g.headdim;
+    p.nsb = (int)(g.chunk / kKb);
+    p.off_x_in_stage = 2 * kKb * 128;
+    p.stage_bytes = p.off_x_in_stage + (H / 64) * kKb * 128;
+    p.tmem_cols = (3 * H <= 256) ? 256 : 512;
+    // two CTAs per SM when TMEM allows, else one with a deeper ring
+    const uint32_t budget = (p.tmem_cols == 256) ? (kSmemLimit / 2 - 2048) : kSmemLimit;
+    const uint32_t fixed = kNumBars * 8 + 64 + 1024;
+    int nst = (int)((budget - fixed) / p.stage_bytes);
+    if (nst > kMaxStages) nst = kMaxStages;
+    if (nst < 2) return false;
+    p.nst = nst;
+    p.off_bar = nst * p.stage_bytes;
+    p.smem_bytes = p.off_bar + fixed;
+    return true;
+}
+
+}  // namespace
+
+bool state_pass_tc_fits(const Geom& g) {
+    if (g.chunk != 64 && g.chunk != 128 && g.chunk != 256) return false;
+    if (g.headdim != 64 && g.headdim != 128) return false;
+    if (g.dstate != 64 && g.dstate != 128 && g.dstate != 256) return false;
+    if (g.batch * g.seqlen >= (int64_t(1) << 31)) return false;
+    SpTcParams p;
+    return plan(g, p);
+}
+
+cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStream_t st) {
+    SpTcParams p{};
+    p.g = g;
+    if (!plan(g, p)) return cudaErrorInvalidConfiguration;
+    p.dt = a.dt;
+    p.G = a.G;
+    p.init = a.init;
+    p.chunk_states = static_cast<__nv_bfloat16*>(a.chunk_states);
+    p.final_state = a.final_state;
+    p.status = device_status_word();
+    const uint64_t H = g.headdim, S = g.dstate, nh = g.nheads, L = g.seqlen, G = g.ngroups;
+    CUtensorMap tm_x, tm_b;
+    {
+        const uint64_t dims[4] = {H, nh, L, (uint64_t)g.batch};
+        const uint64_t strides[3] = {H * 2, nh * H * 2, L * nh * H * 2};
+        const uint32_t box[4] = {64, 1, kKb, 1};
+        if (!make_tmap_bf16(&tm_x, a.x, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[4] = {S, G, L, (uint64_t)g.batch};
+        const uint64_t strides[3] = {S * 2, G * S * 2, L * G * S * 2};
+        const uint32_t box[4] = {64, 1, kKb, 1};
+        if (!make_tmap_bf16(&tm_b, a.B, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(k_state_pass_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    const int mtiles = (int)((g.dstate + 127) / 128);
+    dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)g.batch);
+    k_state_pass_tc<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, p);
+    return cudaGetLastError();
+}
+
+}  // namespace m2

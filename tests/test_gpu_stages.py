@@ -136,3 +136,26 @@ def test_chunk_out_skip_only_is_exact(spec):
     y = bd.mamba2_chunk_out(d["x"], d["dt"], zB, zB, G, cs, w.chunk_size, D=d["D"])
     ref = (d["D"][None, None, :, None] * d["x"].float()).to(d["x"].dtype)
     assert torch.equal(y, ref)
+
+
+@pytest.mark.parametrize("spec", SHAPES, ids=[s[0] for s in SHAPES])
+@pytest.mark.parametrize("term", ["carried_state_only", "interaction_only"])
+def test_chunk_out_single_term(spec, term):
+    """One term of the output at a time: x = 0 leaves exp2(G_i) C_i^T h_c
+    (the carried-state product); zero states leave the decayed, masked
+    interaction term plus the skip."""
+    w = _w(*spec)
+    inp = make_inputs(w)
+    if term == "carried_state_only":
+        inp["x"].zero_()
+    d = to_dev(inp)
+    G32, cs_ref, _ = _oracle_stage_inputs(inp, w)
+    if term == "interaction_only":
+        cs_ref = np.zeros_like(cs_ref)
+    cs_dev = torch.from_numpy(cs_ref).to(d["x"].dtype).cuda()
+    y = bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], torch.from_numpy(G32).cuda(), cs_dev,
+                            w.chunk_size, D=d["D"])
+    bd.mamba2_check_device_status()
+    y_ref = oracle.chunk_out(inp["x"], inp["dt"], inp["B"], inp["C"], G32, cs_dev.cpu(), w.chunk_size,
+                             D=inp["D"])
+    assert rel_err(np64(y), y_ref) <= TOL[w.dtype]
