@@ -3,23 +3,35 @@
 // [blog §Kernel 3] computes, per chunk and head,
 //     Y = exp2(G) (C h_c) + ((C B^T) . exp2(G_i - G_j) . dt_j . causal M) X + D X.
 // GB300 design.  One CTA owns (batch, chunk, 128-row block I of the chunk,
-// a block of heads sharing one B/C group):
-//   warp 0      TMA producer: C rows of the block and B rows 0..Tj-1 once
-//               (Tj = 128 (I + 1)), then per head X rows 0..Tj-1 and h_c;
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
-//               CB = C B^T once into TMEM (per group, reused by every head),
-//               per head Y = C h_c, then Y += P X;
-//   warps 2..9  epilogue (two warps per TMEM lane quadrant, each taking half
-//               of the columns): P = CB . decay . dt . mask from TMEM into
-//               shared memory as bf16, Y <- exp2(G_i) Y in TMEM, and finally
-//               y = Y + D x to global memory.
-// The T x T interaction matrix lives only in TMEM, registers and shared
-// memory.  Decays: for 32-column groups strictly below the diagonal the
-// pairwise factor is evaluated as exp2(G_i - G_r) * exp2(G_r - G_j) with r the
-// group's last column (both factors <= 1 because a_t <= 0 makes G
-// non-increasing inside a chunk), which needs one exp2 per row and column
-// instead of one per element; the diagonal 32 x 32 groups use exp2(G_i - G_j)
-// directly and masked entries are selected to zero, never multiplied.
+// a block of heads sharing one B/C group); T = 128 has one row block, T = 256
+// two.  Rows of block I see columns j < 128 (I + 1); the interaction matrix
+// is split along j into the block on the diagonal (j in block I) and, for
+// I = 1, the block below it (j in block 0).
+//   warp 0       TMA producer: C (rows of block I) and B (rows 0 .. 128I+127)
+//                once, then per head X (same rows) and h_c;
+//   warp 1       TMEM allocator and single-thread tcgen05.mma issuer;
+//   warps 2..17  epilogue, split into head streams (two when H = 64, one when
+//                H = 128) that take alternate heads, each stream with its own
+//                TMEM accumulators so one stream's arithmetic overlaps the
+//                other's tensor-core work.
+// Once per CTA (per group, shared by every head):
+//   CB_II = C_I B_I^T -> TMEM;  for I = 1 also CB_10 = C_1 B_0^T, converted to
+//   bf16 into shared memory as an MMA operand.
+// Per head, with a = exp2(G_127) and v_j = exp2(G_127 - G_j) dt_j for I = 1
+// (a = 1 and no second term for I = 0):
+//   Z  = C_I (a h_c) + CB_10 (v . X_0)     tcgen05; a h_c and v . X_0 are
+//                                          formed on chip by the epilogue
+//   P  = CB_II . exp2(G_i - G_j) dt_j . M  epilogue, written back to TMEM as
+//                                          bf16 and consumed there as operand A
+//   Y2 = P X_I                             tcgen05, A from TMEM
+//   y_i = exp2(G_i - G_ref) Z + Y2 + D x_i  (G_ref = G_127 for I = 1, else 0).
+// This is the exact identity exp2(G_i - G_j) = exp2(G_i - G_127) exp2(G_127 - G_j)
+// for j <= 127 < i, with both factors <= 1 because a_t <= 0 keeps G
+// non-increasing inside a chunk.  Inside the diagonal block the same identity
+// is used per 32-column group strictly below the diagonal (reference column =
+// the group's last one); the diagonal 32 x 32 groups use exp2(G_i - G_j)
+// directly and masked entries are selected to zero, never multiplied.  The
+// T x T matrix never reaches global memory.
 // Every wait is bounded; a timeout sets the status word and the CTA unwinds.
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -28,17 +40,27 @@
 namespace m2 {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kSmemLimit = 232448;
+constexpr int kMaxStages = 2;
+constexpr int kMaxStreams = 2;
+
+// TMEM columns (512 allocated): CB_II at 0 (128 fp32 columns); stream s keeps
+// P (128 bf16 = 64 columns) at 128 + 64 s, Z at 256 + 2 H s and Y2 right after
+// Z.  During set-up CB_10 is staged in columns [256, 384).
+constexpr uint32_t kColCB = 0;
+__host__ __device__ constexpr uint32_t col_p(int s) { return 128u + 64u * (uint32_t)s; }
+__host__ __device__ constexpr uint32_t col_z(int s, int H) { return 256u + 2u * (uint32_t)H * (uint32_t)s; }
 
 struct CoTcParams {
     Geom g;
-    int T;           // chunk size (128 or 256)
-    int nhb;         // heads per CTA (all in one group)
-    int nst;         // X/h pipeline stages
-    int head_blocks; // nheads / nhb
-    uint32_t off_C, off_P, off_stage, stage_bytes, off_h_in_stage, off_small, off_bar, smem_bytes;
+    int T;            // chunk size (128 or 256)
+    int nhb;          // heads per CTA (all in one group)
+    int nst;          // X / h pipeline stages
+    int nstr;         // epilogue head streams (2 for H = 64, 1 for H = 128)
+    int head_blocks;  // nheads / nhb
+    uint32_t off_C, off_CB10, off_X0v, off_stage, stage_bytes, off_h_in_stage, off_small, off_bar, smem_bytes;
     const float* dt;
     const float* G;
     const float* D;
@@ -46,20 +68,18 @@ struct CoTcParams {
     unsigned int* status;
 };
 
-// Barrier slots (uint64 each) inside the barrier area.
 enum : int {
     kBarCbFull = 0,
-    kBarCbDone = 1,
-    kBarPReady = 2,
-    kBarEpiSync = 3,
-    kBarChDone = 4,     // [2]
-    kBarYDone = 6,      // [2]
-    kBarYFree = 8,      // [2]
-    kBarFull = 10,      // [kMaxStages]
-    kBarSlotFree = 12,  // [kMaxStages]
-    kNumBars = 14
+    kBarCbDone,
+    kBarCb10Ready,
+    kBarOpsReady,                            // [kMaxStreams]
+    kBarPReady = kBarOpsReady + kMaxStreams,   // [kMaxStreams]
+    kBarYDone = kBarPReady + kMaxStreams,      // [kMaxStreams]
+    kBarYFree = kBarYDone + kMaxStreams,       // [kMaxStreams]
+    kBarFull = kBarYFree + kMaxStreams,        // [kMaxStages]
+    kBarSlotFree = kBarFull + kMaxStages,      // [kMaxStages]
+    kNumBars = kBarSlotFree + kMaxStages
 };
-constexpr int kMaxStages = 2;
 
 struct SharedCtl {
     uint32_t tmem_base;
@@ -71,6 +91,33 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
     if (status) atomicExch(status, kStatusTimeout);
 }
 
+// Scales the 16-byte bf16 chunks [c_begin, c_end) of one 128-byte-swizzled row
+// (chunk index = physical position, rotated by the row to spread banks) from
+// src into dst by f.  Boxes of 64 columns sit box_stride bytes apart.
+__device__ __forceinline__ void scale_row_chunks(const uint8_t* src, uint8_t* dst, uint32_t src_box_stride,
+                                                 uint32_t dst_box_stride, int row, int c_begin, int n, float f) {
+    uint4 v[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        if (t >= n) break;
+        const int c = c_begin + t;
+        const int pc = ((c & 7) + row) & 7;
+        v[t] = *reinterpret_cast<const uint4*>(src + (c >> 3) * src_box_stride + row * 128 + pc * 16);
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        if (t >= n) break;
+        const int c = c_begin + t;
+        const int pc = ((c & 7) + row) & 7;
+        uint4 w = v[t];
+        w.x = tc::pack_bf16x2(tc::bf16_lo(w.x) * f, tc::bf16_hi(w.x) * f);
+        w.y = tc::pack_bf16x2(tc::bf16_lo(w.y) * f, tc::bf16_hi(w.y) * f);
+        w.z = tc::pack_bf16x2(tc::bf16_lo(w.z) * f, tc::bf16_hi(w.z) * f);
+        w.w = tc::pack_bf16x2(tc::bf16_lo(w.w) * f, tc::bf16_hi(w.w) * f);
+        *reinterpret_cast<uint4*>(dst + (c >> 3) * dst_box_stride + row * 128 + pc * 16) = w;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_h,
@@ -80,41 +127,40 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const Geom& g = p.g;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // ---- which tile
-    const int nrb = p.T / 128;
     const int hb = blockIdx.x % p.head_blocks;
     const int I = blockIdx.x / p.head_blocks;  // row block inside the chunk
     const int64_t c = blockIdx.y;
     const int64_t b = blockIdx.z;
-    const int h0 = hb * p.nhb;
-    const int grp = (int)(h0 / g.heads_per_group);
     const int64_t t0 = c * g.chunk;
     const int tc = (int)imin64(g.chunk, g.seqlen - t0);  // valid tokens of the chunk
-    const int Tj = 128 * (I + 1);                         // columns j that rows of block I can see
+    if (128 * I >= tc) return;                           // ragged tail: no valid row here
+    const int h0 = hb * p.nhb;
+    const int grp = (int)(h0 / g.heads_per_group);
+    const int Tj = 128 * (I + 1);  // columns j that rows of block I can see
     const int S = (int)g.dstate, H = (int)g.headdim;
-    (void)nrb;
+    const int nstr = p.nstr;
+    const int wps = kEpiWarps / nstr;  // warps per stream
 
     uint8_t* sC = smem + p.off_C;
-    uint8_t* sP = smem + p.off_P;
-    uint8_t* sB = sP;  // B lives in [P .. stages) until CB has been computed
+    uint8_t* sCB10 = smem + p.off_CB10;
     uint8_t* sStage = smem + p.off_stage;
-    float* sSmall = reinterpret_cast<float*>(smem + p.off_small);  // [2][3][T]: G, dt, v
+    uint8_t* sB = sCB10;  // B occupies [CB_10 .. stages) until the CB products are done
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + p.off_bar + kNumBars * 8);
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&bars[kBarCbFull], 1);
         tc::mbar_init(&bars[kBarCbDone], 1);
-        tc::mbar_init(&bars[kBarPReady], kEpiWarps);
-        tc::mbar_init(&bars[kBarEpiSync], kEpiWarps);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&bars[kBarChDone + i], 1);
+        tc::mbar_init(&bars[kBarCb10Ready], kEpiWarps);
+        for (int i = 0; i < kMaxStreams; ++i) {
+            tc::mbar_init(&bars[kBarOpsReady + i], wps);
+            tc::mbar_init(&bars[kBarPReady + i], wps);
             tc::mbar_init(&bars[kBarYDone + i], 1);
-            tc::mbar_init(&bars[kBarYFree + i], kEpiWarps);
+            tc::mbar_init(&bars[kBarYFree + i], wps);
         }
         for (int i = 0; i < kMaxStages; ++i) {
             tc::mbar_init(&bars[kBarFull + i], 1);
-            tc::mbar_init(&bars[kBarSlotFree + i], 1 + kEpiWarps);
+            tc::mbar_init(&bars[kBarSlotFree + i], 1 + wps);
         }
         ctl->abort = 0;
         tc::fence_barrier_init();
@@ -127,10 +173,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    const uint32_t tm_cb = tmem;                          // columns [0, Tj)
-    const uint32_t tm_y0 = tmem + 256;                    // Y buffers: 256 .. 256 + 2H
     volatile int* abort_flag = &ctl->abort;
-
     const uint32_t x_bytes = (uint32_t)Tj * H * 2;
     const uint32_t h_bytes = (uint32_t)S * H * 2;
 
@@ -148,7 +191,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tc::tma_load_4d(sB + kb * (Tj * 128) + rb * 16384, &tm_b, &bars[kBarCbFull], kb * 64, grp,
                                     (int)(t0 + 128 * rb), (int)b);
             }
-            bool ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);  // B region is reused
+            bool ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);  // the B area is reused
             for (int k = 0; ok && k < p.nhb; ++k) {
                 const int st = k % p.nst;
                 if (k >= p.nst && !tc::mbar_wait(&bars[kBarSlotFree + st], ((k / p.nst) - 1) & 1, abort_flag)) {
@@ -173,185 +216,255 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // ============================ MMA issuer ============================
         if (lane == 0) {
             bool ok = tc::mbar_wait(&bars[kBarCbFull], 0, abort_flag);
+            const uint32_t aC = tc::smem_u32(sC), aB = tc::smem_u32(sB);
             if (ok) {
                 tc::tc_fence_after();
-                const uint32_t id_cb = tc::idesc_bf16(128, Tj, false, false);
-                const uint32_t aC = tc::smem_u32(sC), aB = tc::smem_u32(sB);
+                // CB_II = C_I B_I^T (both K-major over S); for I = 1 also CB_10 = C_1 B_0^T.
+                const uint32_t id_cb = tc::idesc_bf16(128, 128, false, false);
                 for (int k16 = 0; k16 < S / 16; ++k16) {
                     const uint64_t da = tc::sdesc_sw128(aC + (k16 >> 2) * 16384 + (k16 & 3) * 32, 16, 1024);
-                    const uint64_t db = tc::sdesc_sw128(aB + (k16 >> 2) * (Tj * 128) + (k16 & 3) * 32, 16, 1024);
-                    tc::mma_bf16_ss(tm_cb, da, db, id_cb, k16 > 0);
+                    const uint32_t bbase = aB + (k16 >> 2) * (Tj * 128) + (k16 & 3) * 32;
+                    tc::mma_bf16_ss(tmem + kColCB, da, tc::sdesc_sw128(bbase + I * 16384, 16, 1024), id_cb, k16 > 0);
+                    if (I == 1) tc::mma_bf16_ss(tmem + 256, da, tc::sdesc_sw128(bbase, 16, 1024), id_cb, k16 > 0);
                 }
                 tc::mma_commit(&bars[kBarCbDone]);
+                if (I == 1) ok = tc::mbar_wait(&bars[kBarCb10Ready], 0, abort_flag);
             }
             const uint32_t id_y = tc::idesc_bf16(128, H, false, true);
-            const uint32_t aC = tc::smem_u32(sC), aP = tc::smem_u32(sP);
+            const uint32_t aCB10 = tc::smem_u32(sCB10);
             for (int k = 0; ok && k < p.nhb; ++k) {
-                const int st = k % p.nst, yb = k & 1;
-                const uint32_t tm_y = tm_y0 + yb * H;
+                const int st = k % p.nst, s = k % nstr, n = k / nstr;
                 uint8_t* sX = sStage + st * p.stage_bytes;
                 const uint32_t aX = tc::smem_u32(sX), aH = tc::smem_u32(sX + p.off_h_in_stage);
+                const uint32_t aX0v = tc::smem_u32(smem + p.off_X0v + s * (128 * H * 2));
+                const uint32_t tz = tmem + col_z(s, H), ty2 = tz + H;
                 if (!tc::mbar_wait(&bars[kBarFull + st], (k / p.nst) & 1, abort_flag)) { ok = false; break; }
-                if (k >= 2 && !tc::mbar_wait(&bars[kBarYFree + yb], ((k >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+                if (n >= 1 && !tc::mbar_wait(&bars[kBarYFree + s], (n - 1) & 1, abort_flag)) { ok = false; break; }
+                if (I == 1 && !tc::mbar_wait(&bars[kBarOpsReady + s], n & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
-                // Y = C h_c   (A: C, K-major over S; B: h_c, MN-major: rows s, columns H)
+                // Z = C_I (a h_c)   (B operand: rows s = K, columns H = N, MN-major)
                 for (int k16 = 0; k16 < S / 16; ++k16) {
                     const uint64_t da = tc::sdesc_sw128(aC + (k16 >> 2) * 16384 + (k16 & 3) * 32, 16, 1024);
                     const uint64_t db = tc::sdesc_sw128(aH + k16 * 2048, S * 128, 1024);
-                    tc::mma_bf16_ss(tm_y, da, db, id_y, k16 > 0);
+                    tc::mma_bf16_ss(tz, da, db, id_y, k16 > 0);
                 }
-                tc::mma_commit(&bars[kBarChDone + yb]);
-                if (!tc::mbar_wait(&bars[kBarPReady], k & 1, abort_flag)) { ok = false; break; }
+                if (I == 1) {
+                    // Z += CB_10 (v . X_0)   (A: CB_10 bf16, K-major over j; B: v . X_0, MN-major)
+                    for (int k16 = 0; k16 < 8; ++k16) {
+                        const uint64_t da = tc::sdesc_sw128(aCB10 + (k16 >> 2) * 16384 + (k16 & 3) * 32, 16, 1024);
+                        const uint64_t db = tc::sdesc_sw128(aX0v + k16 * 2048, 16384, 1024);
+                        tc::mma_bf16_ss(tz, da, db, id_y, 1);
+                    }
+                }
+                // Y2 = P X_I   (A: P in TMEM; B: rows 128I.. of X, MN-major)
+                if (!tc::mbar_wait(&bars[kBarPReady + s], n & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
-                // Y += P X   (A: P, K-major over j; B: X, MN-major: rows j, columns H)
-                for (int k16 = 0; k16 < Tj / 16; ++k16) {
-                    const uint64_t da = tc::sdesc_sw128(aP + (k16 >> 2) * 16384 + (k16 & 3) * 32, 16, 1024);
-                    const uint64_t db = tc::sdesc_sw128(aX + k16 * 2048, Tj * 128, 1024);
-                    tc::mma_bf16_ss(tm_y, da, db, id_y, 1);
+                for (int k16 = 0; k16 < 8; ++k16) {
+                    const uint64_t db = tc::sdesc_sw128(aX + I * 16384 + k16 * 2048, Tj * 128, 1024);
+                    tc::mma_bf16_ts(ty2, tmem + col_p(s) + k16 * 8, db, id_y, k16 > 0);
                 }
-                tc::mma_commit(&bars[kBarYDone + yb]);
+                tc::mma_commit(&bars[kBarYDone + s]);
                 tc::mma_commit(&bars[kBarSlotFree + st]);
             }
             if (!ok) set_abort(ctl, p.status);
         }
     } else {
         // ============================== epilogue ==============================
-        const int ew = warp - 2;          // 0..7
-        const int q = warp & 3;           // TMEM lane quadrant this warp may access
-        const int hf = ew >> 2;           // column half of P and Y handled by this warp
-        const int et = ew * 32 + lane;    // 0..255: this thread's column j for per-head vectors
-        const int il = q * 32 + lane;     // row inside the block = TMEM lane
-        const int i = 128 * I + il;       // row inside the chunk (< Tj)
+        const int e = warp - 2;                 // 0..15
+        const int sid = e / wps;                // head stream of this warp
+        const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+        const int nparts = wps / 4;             // warps per quadrant within a stream
+        const int part = (e % wps) >> 2;        // column part handled by this warp
+        const int gpw = 4 / nparts;             // 32-column groups of P per warp
+        const int ncoly = H / nparts;           // output columns per thread
+        const int cpt = 8 * (H / 64) / nparts;  // 16-byte chunks per row per thread in the folds
+        const int il = q * 32 + lane;           // row inside the block = TMEM lane
+        const int i = 128 * I + il;             // row inside the chunk
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        const int T = p.T;
-        const int ilo = 128 * I + 32 * q;  // first row of this warp
+        const uint32_t tz = tmem + col_z(sid, H), ty2 = tz + H, tp = tmem + col_p(sid);
+        float* wv = reinterpret_cast<float*>(smem + p.off_small) + e * 192;  // per warp: 2 x (G, dt, v)
+        uint8_t* sX0v = smem + p.off_X0v + sid * (128 * H * 2);
         bool ok = true;
-        int epi_phase = 0;
 
-        // Per-head vectors G_j, dt_j (j = et), fetched one head ahead.
-        float g_next = 0.f, dt_next = 0.f;
-        auto fetch = [&](int k) {
-            const int64_t bh = b * g.nheads + h0 + k;
-            const int j = et < tc ? et : tc - 1;  // padding columns repeat the last G, dt = 0
-            g_next = (et < Tj) ? p.G[bh * g.seqlen + t0 + j] : 0.f;
-            dt_next = (et < Tj && et < tc) ? p.dt[(b * g.seqlen + t0 + et) * g.nheads + h0 + k] : 0.f;
+        // Per-head scalars of this thread, fetched one head of the stream ahead.
+        struct Scalars {
+            float gcol[2], dtcol[2], grow, gx, dtx, g127, dh;
         };
-        fetch(0);
+        auto fetch = [&](int k, Scalars& o) {
+            const int h = h0 + k;
+            const float* Gh = p.G + (b * g.nheads + h) * g.seqlen + t0;
+            const float* dth = p.dt + (b * g.seqlen + t0) * g.nheads + h;
+            const int last = tc - 1;  // padding repeats the last G with dt = 0
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int jc = 128 * I + 32 * (part * gpw + (t < gpw ? t : 0)) + lane;
+                o.gcol[t] = Gh[jc < tc ? jc : last];
+                o.dtcol[t] = jc < tc ? dth[(int64_t)jc * g.nheads] : 0.f;
+            }
+            o.grow = Gh[i < tc ? i : last];
+            if (I == 1) {
+                o.gx = Gh[il];
+                o.dtx = dth[(int64_t)il * g.nheads];
+                o.g127 = Gh[127];
+            } else {
+                o.gx = o.dtx = o.g127 = 0.f;
+            }
+            o.dh = p.D ? p.D[h] : 0.f;
+        };
+        Scalars nxt;
+        if (sid < p.nhb) fetch(sid, nxt);
         ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
         tc::tc_fence_after();
-        for (int k = 0; ok && k < p.nhb; ++k) {
-            const int h = h0 + k, st = k % p.nst, yb = k & 1;
-            float* sG = sSmall + (k & 1) * 3 * T;
-            float* sDt = sG + T;
-            float* sV = sDt + T;
-            {
-                // v_j = exp2(G_r - G_j) dt_j, r = last column of j's 32-group (lane 31)
-                const float g_r = __shfl_sync(0xffffffffu, g_next, 31);
-                if (et < Tj) {
-                    sG[et] = g_next;
-                    sDt[et] = dt_next;
-                    sV[et] = exp2f(g_r - g_next) * dt_next;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[kBarEpiSync]);
-            if (!tc::mbar_wait(&bars[kBarEpiSync], epi_phase & 1, abort_flag)) { ok = false; break; }
-            ++epi_phase;
-            if (k + 1 < p.nhb) fetch(k + 1);
-            const float gi = sG[i];
-
-            // ---- P = CB . decay . dt . mask -> shared memory (bf16, K-major, 128B swizzle)
-            for (int gi32 = hf; gi32 < Tj / 32; gi32 += 2) {
-                const int j0 = gi32 * 32;
-                uint32_t pk[16];
-                if (j0 > ilo + 31) {
+        if (ok && I == 1) {
+            // CB_10 (staged in TMEM) -> bf16 [128 rows i x 128 columns j], K-major, 128B swizzle
+            const int cg = e >> 2;  // 32-column group 0..3
+            uint8_t* row = sCB10 + (cg >> 1) * 16384 + il * 128;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) pk[e] = 0u;
-                } else {
-                    uint32_t r[32];
-                    tc::tmem_ld32(tm_cb + lane_base + j0, r);
-                    if (j0 + 31 <= ilo) {
-                        const float u = exp2f(gi - sG[j0 + 31]);
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t r[16];
+                tc::tmem_ld16(tmem + 256 + lane_base + 32 * cg + 16 * hh, r);
+                const int c0 = (cg & 1) * 4 + 2 * hh;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float a = __uint_as_float(r[2 * e]) * u * sV[j0 + 2 * e];
-                            const float bb = __uint_as_float(r[2 * e + 1]) * u * sV[j0 + 2 * e + 1];
-                            pk[e] = tc::pack_bf16x2(a, bb);
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int ja = j0 + 2 * e, jb = ja + 1;
-                            const float a = (ja <= i) ? __uint_as_float(r[2 * e]) * exp2f(gi - sG[ja]) * sDt[ja] : 0.f;
-                            const float bb = (jb <= i) ? __uint_as_float(r[2 * e + 1]) * exp2f(gi - sG[jb]) * sDt[jb] : 0.f;
-                            pk[e] = tc::pack_bf16x2(a, bb);
-                        }
-                    }
-                }
-                uint8_t* pbase = sP + (j0 >> 6) * 16384 + il * 128;
-                const int c0 = (j0 & 63) >> 3;
-#pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4) {
-                    uint4* dst = reinterpret_cast<uint4*>(pbase + (((c0 + s4) ^ (il & 7)) << 4));
-                    *dst = make_uint4(pk[4 * s4], pk[4 * s4 + 1], pk[4 * s4 + 2], pk[4 * s4 + 3]);
+                for (int s4 = 0; s4 < 2; ++s4) {
+                    const int x = 8 * s4;
+                    *reinterpret_cast<uint4*>(row + (((c0 + s4) ^ (il & 7)) << 4)) = make_uint4(
+                        tc::pack_bf16x2(__uint_as_float(r[x]), __uint_as_float(r[x + 1])),
+                        tc::pack_bf16x2(__uint_as_float(r[x + 2]), __uint_as_float(r[x + 3])),
+                        tc::pack_bf16x2(__uint_as_float(r[x + 4]), __uint_as_float(r[x + 5])),
+                        tc::pack_bf16x2(__uint_as_float(r[x + 6]), __uint_as_float(r[x + 7])));
                 }
             }
             tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[kBarCb10Ready]);
+        }
 
-            // ---- Y <- exp2(G_i) Y (carried-state term) once C h_c is in TMEM
-            if (!tc::mbar_wait(&bars[kBarChDone + yb], (k >> 1) & 1, abort_flag)) { ok = false; break; }
-            tc::tc_fence_after();
-            const float ei = exp2f(gi);
-            const uint32_t ycol = tm_y0 + yb * H + hf * (H / 2);
-            for (int m = 0; m < H / 64; ++m) {
-                uint32_t r[32];
-                tc::tmem_ld32(ycol + lane_base + 32 * m, r);
+        for (int k = sid; ok && k < p.nhb; k += nstr) {
+            const int h = h0 + k, st = k % p.nst, n = k / nstr;
+            const Scalars cur = nxt;
+            if (k + nstr < p.nhb) fetch(k + nstr, nxt);
+            // this warp's column vectors: G_j, dt_j, v_j = exp2(G_r - G_j) dt_j (r = group's last column)
+            float g_r[2];
+            __syncwarp();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * ei);
-                tc::tmem_st32(ycol + lane_base + 32 * m, r);
+            for (int t = 0; t < 2; ++t) {
+                if (t >= gpw) break;
+                g_r[t] = __shfl_sync(0xffffffffu, cur.gcol[t], 31);
+                wv[96 * t + lane] = cur.gcol[t];
+                wv[96 * t + 32 + lane] = cur.dtcol[t];
+                wv[96 * t + 64 + lane] = exp2f(g_r[t] - cur.gcol[t]) * cur.dtcol[t];
+            }
+            __syncwarp();
+            if (!tc::mbar_wait(&bars[kBarFull + st], (k / p.nst) & 1, abort_flag)) { ok = false; break; }
+            uint8_t* sX = sStage + st * p.stage_bytes;
+
+            if (I == 1) {
+                // a h_c (in place) and v . X_0 (into this stream's buffer)
+                uint8_t* sH = sX + p.off_h_in_stage;
+                const float a = exp2f(cur.g127);
+                for (int r = il; r < S; r += 128)
+                    scale_row_chunks(sH, sH, S * 128, S * 128, r, part * cpt, cpt, a);
+                const float vj = exp2f(cur.g127 - cur.gx) * cur.dtx;
+                scale_row_chunks(sX, sX0v, Tj * 128, 16384, il, part * cpt, cpt, vj);
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[kBarOpsReady + sid]);
+            }
+
+            // ---- P on the diagonal block -> TMEM as bf16
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (t >= gpw) break;
+                const int gi = part * gpw + t;  // 32-column group 0..3 of the diagonal block
+                const float* w = wv + 96 * t;
+                uint32_t pk[16];
+                if (gi > q) {
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) pk[x] = 0u;
+                } else {
+                    uint32_t ra[16], rb[16];
+                    tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi, ra);
+                    tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi + 16, rb);
+                    tc::tmem_wait_ld16(ra);
+                    tc::tmem_wait_ld16(rb);
+                    if (gi < q) {
+                        const float u = exp2f(cur.grow - g_r[t]);
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 v4 = *reinterpret_cast<const float4*>(w + 64 + 4 * e4);
+                            const uint32_t* r = (e4 < 4) ? ra : rb;
+                            const int o = 4 * (e4 & 3);
+                            pk[2 * e4] = tc::pack_bf16x2(__uint_as_float(r[o]) * u * v4.x,
+                                                         __uint_as_float(r[o + 1]) * u * v4.y);
+                            pk[2 * e4 + 1] = tc::pack_bf16x2(__uint_as_float(r[o + 2]) * u * v4.z,
+                                                             __uint_as_float(r[o + 3]) * u * v4.w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 g4 = *reinterpret_cast<const float4*>(w + 4 * e4);
+                            const float4 d4 = *reinterpret_cast<const float4*>(w + 32 + 4 * e4);
+                            const uint32_t* r = (e4 < 4) ? ra : rb;
+                            const int o = 4 * (e4 & 3), x = 4 * e4;  // column offset inside the group
+                            const float a0 = (x <= lane) ? __uint_as_float(r[o]) * exp2f(cur.grow - g4.x) * d4.x : 0.f;
+                            const float a1 = (x + 1 <= lane) ? __uint_as_float(r[o + 1]) * exp2f(cur.grow - g4.y) * d4.y : 0.f;
+                            const float a2 = (x + 2 <= lane) ? __uint_as_float(r[o + 2]) * exp2f(cur.grow - g4.z) * d4.z : 0.f;
+                            const float a3 = (x + 3 <= lane) ? __uint_as_float(r[o + 3]) * exp2f(cur.grow - g4.w) * d4.w : 0.f;
+                            pk[2 * e4] = tc::pack_bf16x2(a0, a1);
+                            pk[2 * e4 + 1] = tc::pack_bf16x2(a2, a3);
+                        }
+                    }
+                }
+                tc::tmem_st16(tp + lane_base + 16 * gi, pk);
             }
             tc::tmem_wait_st();
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[kBarPReady]);
+            if (lane == 0) tc::mbar_arrive(&bars[kBarPReady + sid]);
 
-            // ---- y = Y + D x once P X has been accumulated
-            if (!tc::mbar_wait(&bars[kBarYDone + yb], (k >> 1) & 1, abort_flag)) { ok = false; break; }
+            // ---- y = exp2(G_i - G_ref) Z + Y2 + D x
+            if (!tc::mbar_wait(&bars[kBarYDone + sid], n & 1, abort_flag)) { ok = false; break; }
             tc::tc_fence_after();
-            const float dh = p.D ? p.D[h] : 0.f;
-            const uint8_t* sX = sStage + st * p.stage_bytes;
+            const float si = exp2f(cur.grow - cur.g127);  // g127 = 0 for I = 0
             __nv_bfloat16* yrow = p.y + ((b * g.seqlen + t0 + i) * g.nheads + h) * H;
-            for (int m = 0; m < H / 64; ++m) {
-                const int k0 = hf * (H / 2) + 32 * m;
-                uint32_t r[32];
-                tc::tmem_ld32(ycol + lane_base + 32 * m, r);
-                const uint8_t* xrow = sX + (k0 >> 6) * (Tj * 128) + i * 128;
-                const int c0 = (k0 & 63) >> 3;
-                uint32_t out[16];
+            for (int m = 0; m < ncoly / 16; ++m) {
+                const int kk = part * ncoly + 16 * m;
+                float acc[16];
+                {
+                    uint32_t ya[16], yb[16];
+                    tc::tmem_ld16_nowait(tz + lane_base + kk, ya);
+                    tc::tmem_ld16_nowait(ty2 + lane_base + kk, yb);
+                    tc::tmem_wait_ld16(ya);
+                    tc::tmem_wait_ld16(yb);
 #pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4) {
-                    const uint4 xv = *reinterpret_cast<const uint4*>(xrow + (((c0 + s4) ^ (i & 7)) << 4));
+                    for (int x = 0; x < 16; ++x) acc[x] = fmaf(si, __uint_as_float(ya[x]), __uint_as_float(yb[x]));
+                }
+                const uint8_t* xrow = sX + (kk >> 6) * (Tj * 128) + i * 128;
+                const int lc0 = (kk & 63) >> 3;
+                uint32_t out[8];
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                    const uint4 xv = *reinterpret_cast<const uint4*>(xrow + (((lc0 + s2) ^ (i & 7)) << 4));
                     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int cidx = s4 * 8 + 2 * e;
-                        const float lo = __uint_as_float(r[cidx]) + dh * tc::bf16_lo(xw[e]);
-                        const float hi = __uint_as_float(r[cidx + 1]) + dh * tc::bf16_hi(xw[e]);
-                        out[s4 * 4 + e] = tc::pack_bf16x2(lo, hi);
+                    for (int x = 0; x < 4; ++x) {
+                        const int ci = s2 * 8 + 2 * x;
+                        out[s2 * 4 + x] = tc::pack_bf16x2(fmaf(cur.dh, tc::bf16_lo(xw[x]), acc[ci]),
+                                                          fmaf(cur.dh, tc::bf16_hi(xw[x]), acc[ci + 1]));
                     }
                 }
                 if (i < tc) {
-                    uint4* dst = reinterpret_cast<uint4*>(yrow + k0);
-#pragma unroll
-                    for (int s4 = 0; s4 < 4; ++s4)
-                        dst[s4] = make_uint4(out[4 * s4], out[4 * s4 + 1], out[4 * s4 + 2], out[4 * s4 + 3]);
+                    uint4* dst = reinterpret_cast<uint4*>(yrow + kk);
+                    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+                    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
                 }
             }
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 tc::mbar_arrive(&bars[kBarSlotFree + st]);
-                tc::mbar_arrive(&bars[kBarYFree + yb]);
+                tc::mbar_arrive(&bars[kBarYFree + sid]);
             }
         }
         if (!ok) set_abort(ctl, p.status);
@@ -365,38 +478,27 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     }
 }
 
-}  // namespace
-
-// Shapes the tensor-core stage-3 kernel covers; others use the CUDA-core kernel.
-bool chunk_out_tc_supported(const Geom& g) {
-    if (g.chunk != 128 && g.chunk != 256) return false;
-    if (g.headdim != 64 && g.headdim != 128) return false;
-    if (g.dstate != 64 && g.dstate != 128 && g.dstate != 256) return false;
-    if (g.batch * g.nheads * g.nchunks * g.dstate >= (int64_t(1) << 31)) return false;
-    if (g.batch * g.seqlen >= (int64_t(1) << 31)) return false;
-    return true;
-}
-
-namespace {
 int pick_heads_per_cta(const Geom& g) {
     const int r = (int)g.heads_per_group;
-    for (int n = 8; n >= 1; --n)
+    for (int n = 16; n >= 1; --n)
         if (r % n == 0) return n;
     return 1;
 }
 
 bool plan_smem(const Geom& g, CoTcParams& p) {
     const int T = (int)g.chunk, S = (int)g.dstate, H = (int)g.headdim;
+    p.nstr = (H == 64) ? 2 : 1;
     p.off_C = 0;
-    p.off_P = p.off_C + 128 * S * 2;
-    p.off_stage = p.off_P + 128 * T * 2;
+    p.off_CB10 = p.off_C + 128 * S * 2;
+    p.off_X0v = p.off_CB10 + (T == 256 ? 32768 : 0);
+    p.off_stage = p.off_X0v + (T == 256 ? p.nstr * 128 * H * 2 : 0);
     p.off_h_in_stage = T * H * 2;
     p.stage_bytes = T * H * 2 + S * H * 2;
     for (int nst = kMaxStages; nst >= 1; --nst) {
         const uint32_t stages_end = p.off_stage + nst * p.stage_bytes;
-        if (stages_end - p.off_P < (uint32_t)(T * S * 2)) continue;  // B must fit over P + stages
+        if (stages_end - p.off_CB10 < (uint32_t)(T * S * 2)) continue;  // B must fit until CB is done
         const uint32_t off_small = stages_end;
-        const uint32_t off_bar = off_small + 2 * 3 * T * 4;
+        const uint32_t off_bar = off_small + kEpiWarps * 192 * 4;
         const uint32_t total = off_bar + kNumBars * 8 + 64 + 1024;  // + ctl + alignment slack
         if (total <= (uint32_t)kSmemLimit) {
             p.nst = nst;
@@ -408,11 +510,18 @@ bool plan_smem(const Geom& g, CoTcParams& p) {
     }
     return false;
 }
+
 }  // namespace
 
+// Shapes the tensor-core stage-3 kernel covers; others use the CUDA-core kernel.
 bool chunk_out_tc_fits(const Geom& g) {
+    if (g.chunk != 128 && g.chunk != 256) return false;
+    if (g.headdim != 64 && g.headdim != 128) return false;
+    if (g.dstate != 64 && g.dstate != 128 && g.dstate != 256) return false;
+    if (g.batch * g.nheads * g.nchunks * g.dstate >= (int64_t(1) << 31)) return false;
+    if (g.batch * g.seqlen >= (int64_t(1) << 31)) return false;
     CoTcParams p;
-    return chunk_out_tc_supported(g) && plan_smem(g, p);
+    return plan_smem(g, p);
 }
 
 cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream_t st) {

@@ -10,10 +10,11 @@
 //               U_c = B_c^T (w . X_c) accumulated over the chunk's sub-blocks
 //               into one of two TMEM buffers (A = B_c^T and B = w . X_c are
 //               both read "MN-major" straight from the TMA layout);
-//   warps 2..5  fold the weights w_t into the X rows in shared memory (so the
+//   warps 2..9  fold the weights w_t into the X rows in shared memory (so the
 //               weighted operand is formed once, on chip), and run the scan:
 //               the state h lives in TMEM next to U; per chunk each thread
-//               (one state row) stores h_c, then sets h <- exp2(G_last) h + U_c.
+//               (one state row, half of the columns) stores h_c, then sets
+//               h <- exp2(G_last) h + U_c.
 // The weighted-operand fold applies the blog's "pre-multiplied operand" to X
 // instead of B (same product; X is the smaller per-head tile).  States past
 // dstate (when dstate = 64) are zero-filled by TMA and never stored.
@@ -24,8 +25,8 @@
 namespace m2 {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kWorkWarps = 4;
+constexpr int kWorkWarps = 8;
+constexpr int kThreads = (2 + kWorkWarps) * 32;
 constexpr int kKb = 64;  // tokens per sub-block
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;
@@ -62,7 +63,7 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
     if (status) atomicExch(status, kStatusTimeout);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                 const SpTcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -162,49 +163,83 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!ok) set_abort(ctl, p.status);
         }
     } else {
-        // ================= weight fold + scan (warps 2..5) =================
-        const int et = (warp - 2) * 32 + lane;   // 0..127
-        const int q = warp & 3;
+        // ================= weight fold + scan (warps 2..9) =================
+        const int ew = warp - 2;                 // 0..7
+        const int et = ew * 32 + lane;           // 0..255
+        const int q = warp & 3;                  // TMEM lane quadrant
+        const int half = ew >> 2;                // column half of the state handled by this warp
         const int s_local = q * 32 + lane;
         const int s = mt * 128 + s_local;
         const bool valid = s < S;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const float* Gbh = p.G + bh * g.seqlen;
+        const int hcols = H / 2;                 // state columns per thread
+        const int col0 = half * hcols;
 
         // h <- initial state (or zeros), kept in TMEM columns [2H, 3H)
-        for (int m = 0; m < H / 32; ++m) {
-            uint32_t r[32];
+        for (int m = 0; m < hcols / 16; ++m) {
+            uint32_t r[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-                r[e] = __float_as_uint((valid && p.init) ? p.init[(bh * S + s) * H + 32 * m + e] : 0.f);
-            tc::tmem_st32(tm_h + lane_base + 32 * m, r);
+            for (int e = 0; e < 16; ++e)
+                r[e] = __float_as_uint((valid && p.init) ? p.init[(bh * S + s) * H + col0 + 16 * m + e] : 0.f);
+            tc::tmem_st16(tm_h + lane_base + col0 + 16 * m, r);
         }
         tc::tmem_wait_st();
 
-        // Fold w_t into the X rows of sub-block u (two threads per token row).
-        auto fold = [&](int u) -> bool {
-            const int st = u % p.nst, c = u / p.nsb, sb = u % p.nsb;
+        // Fold mapping: four threads per token row of a 64-token sub-block, each
+        // taking a quarter of the row's 16-byte chunks (rotated to spread banks).
+        const int frow = et >> 2, fq = et & 3;
+        const int per = 2 * (H / 64);  // chunks per thread (2 or 4)
+        // Raw inputs of the weight w_t = dt_t exp2(G_last - G_t) of this thread's token
+        // row in sub-block u, loaded two sub-blocks ahead; G_last of every chunk is
+        // also kept for the scan.
+        struct Raw {
+            float g_last, g_t, dt_t;
+        };
+        auto load_raw = [&](int u, Raw& r) {
+            const int c = u / p.nsb, sb = u % p.nsb;
             const int64_t t0 = c * g.chunk;
             const int tc = (int)imin64(g.chunk, g.seqlen - t0);
-            const int row = et & 63, half = et >> 6;
-            const int tl = sb * kKb + row;
-            float w = 0.f;
-            if (tl < tc) {
-                const float g_last = Gbh[t0 + tc - 1];
-                w = p.dt[(b * g.seqlen + t0 + tl) * g.nheads + h] * exp2f(g_last - Gbh[t0 + tl]);
+            const int tl = sb * kKb + frow;
+            r.g_last = Gbh[t0 + tc - 1];
+            r.g_t = Gbh[t0 + (tl < tc ? tl : tc - 1)];
+            r.dt_t = (tl < tc) ? p.dt[(b * g.seqlen + t0 + tl) * g.nheads + h] : 0.f;
+        };
+        Raw raw0, raw1;
+        load_raw(0, raw0);
+        if (nsub > 1) load_raw(1, raw1);
+        float glast_even = 0.f, glast_odd = 0.f;  // G_last of the two chunks in flight
+        auto fold = [&](int u) -> bool {
+            const int st = u % p.nst;
+            const Raw cur = raw0;
+            raw0 = raw1;
+            if (u + 2 < nsub) load_raw(u + 2, raw1);
+            if (u % p.nsb == 0) {
+                if ((u / p.nsb) & 1) glast_odd = cur.g_last;
+                else glast_even = cur.g_last;
             }
+            const float w = cur.dt_t * exp2f(cur.g_last - cur.g_t);
             if (!tc::mbar_wait(&bars[kBarFull + st], (u / p.nst) & 1, abort_flag)) return false;
             uint8_t* sX = smem + st * p.stage_bytes + p.off_x_in_stage;
-            const int per = 4 * (H / 64);  // 16-byte chunks per thread
-            for (int f = half * per; f < (half + 1) * per; ++f) {
-                const int box = f >> 3, pc = ((f & 7) + row) & 7;  // rotate to spread banks
-                uint4* ptr = reinterpret_cast<uint4*>(sX + box * x_box_bytes + row * 128 + pc * 16);
-                uint4 v = *ptr;
-                v.x = tc::pack_bf16x2(tc::bf16_lo(v.x) * w, tc::bf16_hi(v.x) * w);
-                v.y = tc::pack_bf16x2(tc::bf16_lo(v.y) * w, tc::bf16_hi(v.y) * w);
-                v.z = tc::pack_bf16x2(tc::bf16_lo(v.z) * w, tc::bf16_hi(v.z) * w);
-                v.w = tc::pack_bf16x2(tc::bf16_lo(v.w) * w, tc::bf16_hi(v.w) * w);
-                *ptr = v;
+            uint8_t* rowp = sX + frow * 128;
+            uint4 v[4];
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+                if (f >= per) break;
+                const int flat = fq * per + f;                  // 0 .. 8 (H/64) - 1
+                v[f] = *reinterpret_cast<const uint4*>(rowp + (flat >> 3) * x_box_bytes +
+                                                       ((((flat & 7) + frow) & 7) << 4));
+            }
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+                if (f >= per) break;
+                const int flat = fq * per + f;
+                uint4 a = v[f];
+                a.x = tc::pack_bf16x2(tc::bf16_lo(a.x) * w, tc::bf16_hi(a.x) * w);
+                a.y = tc::pack_bf16x2(tc::bf16_lo(a.y) * w, tc::bf16_hi(a.y) * w);
+                a.z = tc::pack_bf16x2(tc::bf16_lo(a.z) * w, tc::bf16_hi(a.z) * w);
+                a.w = tc::pack_bf16x2(tc::bf16_lo(a.w) * w, tc::bf16_hi(a.w) * w);
+                *reinterpret_cast<uint4*>(rowp + (flat >> 3) * x_box_bytes + ((((flat & 7) + frow) & 7) << 4)) = a;
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
@@ -215,20 +250,18 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         // Store h_c, then h <- exp2(G_last) h + U_c.
         auto scan = [&](int c) -> bool {
             const int ub = c & 1;
-            const int64_t t0 = c * g.chunk;
-            const int tc = (int)imin64(g.chunk, g.seqlen - t0);
-            const float alpha = exp2f(Gbh[t0 + tc - 1]);
+            const float alpha = exp2f((c & 1) ? glast_odd : glast_even);
             if (!tc::mbar_wait(&bars[kBarUDone + ub], (c >> 1) & 1, abort_flag)) return false;
             tc::tc_fence_after();
-            __nv_bfloat16* dst = p.chunk_states + ((bh * g.nchunks + c) * S + s) * H;
-            for (int m = 0; m < H / 32; ++m) {
-                uint32_t hv[32], uv[32];
-                tc::tmem_ld32(tm_h + lane_base + 32 * m, hv);
-                tc::tmem_ld32(tm_u0 + ub * H + lane_base + 32 * m, uv);
+            __nv_bfloat16* dst = p.chunk_states + ((bh * g.nchunks + c) * S + s) * H + col0;
+            for (int m = 0; m < hcols / 16; ++m) {
+                uint32_t hv[16], uv[16];
+                tc::tmem_ld16(tm_h + lane_base + col0 + 16 * m, hv);
+                tc::tmem_ld16(tm_u0 + ub * H + lane_base + col0 + 16 * m, uv);
                 if (valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * m);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * m);
 #pragma unroll
-                    for (int s4 = 0; s4 < 4; ++s4) {
+                    for (int s4 = 0; s4 < 2; ++s4) {
                         const int e = 8 * s4;
                         d4[s4] = make_uint4(
                             tc::pack_bf16x2(__uint_as_float(hv[e]), __uint_as_float(hv[e + 1])),
@@ -238,9 +271,9 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
+                for (int e = 0; e < 16; ++e)
                     hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
-                tc::tmem_st32(tm_h + lane_base + 32 * m, hv);
+                tc::tmem_st16(tm_h + lane_base + col0 + 16 * m, hv);
             }
             tc::tmem_wait_st();
             tc::tc_fence_before();
@@ -257,12 +290,12 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (ok) ok = scan(c);
         }
         if (ok && p.final_state && valid) {
-            for (int m = 0; m < H / 32; ++m) {
-                uint32_t hv[32];
-                tc::tmem_ld32(tm_h + lane_base + 32 * m, hv);
-                float4* d4 = reinterpret_cast<float4*>(p.final_state + (bh * S + s) * H + 32 * m);
+            for (int m = 0; m < hcols / 16; ++m) {
+                uint32_t hv[16];
+                tc::tmem_ld16(tm_h + lane_base + col0 + 16 * m, hv);
+                float4* d4 = reinterpret_cast<float4*>(p.final_state + (bh * S + s) * H + col0 + 16 * m);
 #pragma unroll
-                for (int s4 = 0; s4 < 8; ++s4)
+                for (int s4 = 0; s4 < 4; ++s4)
                     d4[s4] = make_float4(__uint_as_float(hv[4 * s4]), __uint_as_float(hv[4 * s4 + 1]),
                                          __uint_as_float(hv[4 * s4 + 2]), __uint_as_float(hv[4 * s4 + 3]));
             }
