@@ -135,6 +135,26 @@ MAMBA2_API mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x
                              const float* initial_state, void* y, float* final_state,
                              void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
+/* The whole forward pass for callers that cannot allocate device memory
+ * (code running under a custom pool or an allocator-free runtime, or a host
+ * that must not grow device memory mid-flight).  The blog has no counterpart;
+ * this is a convenience of the library.  Same inputs, outputs and semantics as
+ * mamba2_ssd_fwd, but the intermediates live in a fixed 32 MiB device array
+ * inside the library (held on every GPU that loads the library until the
+ * process exits), so no workspace is passed and nothing is allocated.
+ *  - Problems with mamba2_ssd_fwd_workspace_size(shape) > 32 MiB return
+ *    MAMBA2_ERR_UNSUPPORTED with nothing enqueued.
+ *  - The first call on a device looks up the array's device address (a
+ *    runtime query, no allocation) and caches it; make that first call before
+ *    any stream capture on that device.
+ *  - All calls share the one array: calls that overlap on the GPU race on it
+ *    and must be ordered by the caller (one stream, or explicit events).  The
+ *    array's previous contents never affect a result. */
+MAMBA2_API mamba2_status mamba2_ssd_fwd_noalloc(const mamba2_shape* shape, const void* x, const float* dt,
+                                                const float* A, const void* B, const void* C, const float* D,
+                                                const float* initial_state, void* y, float* final_state,
+                                                struct CUstream_st* stream);
+
 /* Reads (and clears) the current device's status word.  SYNCHRONISES `stream`.
  * Returns MAMBA2_ERR_TIMEOUT if a kernel's bounded wait ran out since the
  * last check, MAMBA2_ERR_CUDA if the stream reports an error, else MAMBA2_OK. */

@@ -58,6 +58,7 @@ def load_library(path: str = LIB_PATH):
         "mamba2_chunk_out": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P]),
         "mamba2_ssd_fwd_workspace_size": (ctypes.c_size_t, [S]),
         "mamba2_ssd_fwd": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]),
+        "mamba2_ssd_fwd_noalloc": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P]),
         "mamba2_check_device_status": (ctypes.c_int, [P]),
         "mamba2_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "mamba2_version": (ctypes.c_int, []),
@@ -180,6 +181,26 @@ def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, D=None, initial_state=None, y=Non
         ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
         _ptr(initial_state), _ptr(y), _ptr(final_state), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return y, final_state
+
+
+def mamba2_ssd_fwd_noalloc(x, dt, A, B, C, chunk_size, D=None, initial_state=None, y=None,
+                           final_state=None, want_final_state=True, stream=None):
+    """Whole forward pass with the library's fixed internal scratch (no
+    workspace argument; the C entry point allocates nothing).  Missing outputs
+    are allocated here, by the caller side, with torch."""
+    for t, n in ((x, "x"), (dt, "dt"), (A, "A"), (B, "B"), (C, "C"), (D, "D"),
+                 (initial_state, "initial_state")):
+        _need(t, n)
+    shape = shape_of(x, B, chunk_size)
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(shape.batch, shape.nheads, shape.dstate, shape.headdim,
+                                  device=x.device, dtype=torch.float32)
+    _check("mamba2_ssd_fwd_noalloc", load_library().mamba2_ssd_fwd_noalloc(
+        ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+        _ptr(initial_state), _ptr(y), _ptr(final_state), _stream(stream)))
     return y, final_state
 
 
