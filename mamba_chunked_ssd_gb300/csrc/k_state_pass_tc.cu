@@ -4,8 +4,11 @@
 //     h_{c+1} = exp2(G_last) h_c + (w . B_c)^T X_c,   w_t = dt_t exp2(G_last - G_t).
 // GB300 design.  One CTA owns (batch, head, 128-row tile of the S x H state)
 // and walks the chunks in order:
-//   warp 0      TMA producer: 64-token sub-blocks of B (the tile's 128 state
-//               columns) and of X, through a ring of shared-memory stages;
+//   warp 0      producer: TMA of 64-token sub-blocks of B (the tile's 128
+//               state columns) and of X into a ring of shared-memory stages;
+//               its lanes also gather dt and G for the sub-block (loaded one
+//               sub-block ahead) and write the weights w_t and exp2(G_last)
+//               into the stage, so the other warps never touch global memory;
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
 //               U_c = B_c^T (w . X_c) accumulated over the chunk's sub-blocks
 //               into one of two TMEM buffers (A = B_c^T and B = w . X_c are
@@ -35,7 +38,7 @@ struct SpTcParams {
     Geom g;
     int nsb;            // sub-blocks per chunk = chunk / 64
     int nst;            // ring stages
-    uint32_t stage_bytes, off_x_in_stage, off_bar, smem_bytes, tmem_cols;
+    uint32_t stage_bytes, off_x_in_stage, off_w_in_stage, off_bar, smem_bytes, tmem_cols;
     const float* dt;
     const float* G;
     const float* init;
@@ -50,7 +53,8 @@ enum : int {
     kBarFull = 4,      // [kMaxStages]
     kBarXform = 4 + kMaxStages,
     kBarSlotFree = 4 + 2 * kMaxStages,
-    kNumBars = 4 + 3 * kMaxStages
+    kBarWReady = 4 + 3 * kMaxStages,
+    kNumBars = 4 + 4 * kMaxStages
 };
 
 struct SharedCtl {
@@ -90,6 +94,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tc::mbar_init(&bars[kBarFull + i], 1);
             tc::mbar_init(&bars[kBarXform + i], kWorkWarps);
             tc::mbar_init(&bars[kBarSlotFree + i], 1);
+            tc::mbar_init(&bars[kBarWReady + i], 1);
         }
         ctl->abort = 0;
         tc::fence_barrier_init();
@@ -108,21 +113,41 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const uint32_t x_box_bytes = kKb * 128;
 
     if (warp == 0) {
-        // =========================== TMA producer ===========================
+        // ===================== TMA producer + weight gather =====================
         if (lane == 0) {
             tc::tma_prefetch_desc(&tm_x);
             tc::tma_prefetch_desc(&tm_b);
-            bool ok = true;
-            for (int u = 0; u < nsub; ++u) {
-                const int st = u % p.nst;
-                if (u >= p.nst && !tc::mbar_wait(&bars[kBarSlotFree + st], ((u / p.nst) - 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const int c = u / p.nsb, sb = u % p.nsb;
-                const int tok = (int)(c * g.chunk + sb * kKb);
-                uint8_t* sB = smem + st * p.stage_bytes;
-                uint8_t* sX = sB + p.off_x_in_stage;
+        }
+        const float* Gbh = p.G + bh * g.seqlen;
+        // raw inputs of one sub-block for this lane's two tokens (lane, lane + 32)
+        float rg[2], rdt[2], rlast;
+        auto gather = [&](int u) {
+            const int c = u / p.nsb, sb = u % p.nsb;
+            const int64_t t0 = c * g.chunk;
+            const int tc = (int)imin64(g.chunk, g.seqlen - t0);
+            rlast = Gbh[t0 + tc - 1];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int tl = sb * kKb + lane + 32 * r;
+                rg[r] = Gbh[t0 + (tl < tc ? tl : tc - 1)];
+                rdt[r] = (tl < tc) ? p.dt[(b * g.seqlen + t0 + tl) * g.nheads + h] : 0.f;
+            }
+        };
+        gather(0);
+        bool ok = true;
+        for (int u = 0; u < nsub; ++u) {
+            const int st = u % p.nst;
+            if (u >= p.nst) {
+                bool w_ok = true;
+                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], ((u / p.nst) - 1) & 1, abort_flag);
+                if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) { ok = false; break; }
+            }
+            const int c = u / p.nsb, sb = u % p.nsb;
+            const int tok = (int)(c * g.chunk + sb * kKb);
+            uint8_t* sB = smem + st * p.stage_bytes;
+            uint8_t* sX = sB + p.off_x_in_stage;
+            float* sW = reinterpret_cast<float*>(sB + p.off_w_in_stage);  // w[64], then exp2(G_last)
+            if (lane == 0) {
                 tc::mbar_arrive_expect_tx(&bars[kBarFull + st], (2 + H / 64) * x_box_bytes);
                 for (int kb = 0; kb < 2; ++kb)
                     tc::tma_load_4d(sB + kb * x_box_bytes, &tm_b, &bars[kBarFull + st], mt * 128 + kb * 64, grp, tok,
@@ -130,8 +155,15 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 for (int cb = 0; cb < H / 64; ++cb)
                     tc::tma_load_4d(sX + cb * x_box_bytes, &tm_x, &bars[kBarFull + st], cb * 64, h, tok, (int)b);
             }
-            if (!ok) set_abort(ctl, p.status);
+            // w_t = dt_t exp2(G_last - G_t) for the sub-block, from the gathered values
+#pragma unroll
+            for (int r = 0; r < 2; ++r) sW[lane + 32 * r] = rdt[r] * exp2f(rlast - rg[r]);
+            if (lane == 0) sW[64] = exp2f(rlast);
+            if (u + 1 < nsub) gather(u + 1);  // in flight while the stage fills
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[kBarWReady + st]);
         }
+        if (!ok && lane == 0) set_abort(ctl, p.status);
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
         if (lane == 0) {
@@ -172,7 +204,6 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         const int s = mt * 128 + s_local;
         const bool valid = s < S;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        const float* Gbh = p.G + bh * g.seqlen;
         const int hcols = H / 2;                 // state columns per thread
         const int col0 = half * hcols;
 
@@ -190,35 +221,16 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         // taking a quarter of the row's 16-byte chunks (rotated to spread banks).
         const int frow = et >> 2, fq = et & 3;
         const int per = 2 * (H / 64);  // chunks per thread (2 or 4)
-        // Raw inputs of the weight w_t = dt_t exp2(G_last - G_t) of this thread's token
-        // row in sub-block u, loaded two sub-blocks ahead; G_last of every chunk is
-        // also kept for the scan.
-        struct Raw {
-            float g_last, g_t, dt_t;
-        };
-        auto load_raw = [&](int u, Raw& r) {
-            const int c = u / p.nsb, sb = u % p.nsb;
-            const int64_t t0 = c * g.chunk;
-            const int tc = (int)imin64(g.chunk, g.seqlen - t0);
-            const int tl = sb * kKb + frow;
-            r.g_last = Gbh[t0 + tc - 1];
-            r.g_t = Gbh[t0 + (tl < tc ? tl : tc - 1)];
-            r.dt_t = (tl < tc) ? p.dt[(b * g.seqlen + t0 + tl) * g.nheads + h] : 0.f;
-        };
-        Raw raw0, raw1;
-        load_raw(0, raw0);
-        if (nsub > 1) load_raw(1, raw1);
-        float glast_even = 0.f, glast_odd = 0.f;  // G_last of the two chunks in flight
+        float alpha_even = 1.f, alpha_odd = 1.f;  // exp2(G_last) of the two chunks in flight
         auto fold = [&](int u) -> bool {
             const int st = u % p.nst;
-            const Raw cur = raw0;
-            raw0 = raw1;
-            if (u + 2 < nsub) load_raw(u + 2, raw1);
+            if (!tc::mbar_wait(&bars[kBarWReady + st], (u / p.nst) & 1, abort_flag)) return false;
+            const float* sW = reinterpret_cast<const float*>(smem + st * p.stage_bytes + p.off_w_in_stage);
+            const float w = sW[frow];
             if (u % p.nsb == 0) {
-                if ((u / p.nsb) & 1) glast_odd = cur.g_last;
-                else glast_even = cur.g_last;
+                if ((u / p.nsb) & 1) alpha_odd = sW[64];
+                else alpha_even = sW[64];
             }
-            const float w = cur.dt_t * exp2f(cur.g_last - cur.g_t);
             if (!tc::mbar_wait(&bars[kBarFull + st], (u / p.nst) & 1, abort_flag)) return false;
             uint8_t* sX = smem + st * p.stage_bytes + p.off_x_in_stage;
             uint8_t* rowp = sX + frow * 128;
@@ -250,7 +262,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         // Store h_c, then h <- exp2(G_last) h + U_c.
         auto scan = [&](int c) -> bool {
             const int ub = c & 1;
-            const float alpha = exp2f((c & 1) ? glast_odd : glast_even);
+            const float alpha = (c & 1) ? alpha_odd : alpha_even;
             if (!tc::mbar_wait(&bars[kBarUDone + ub], (c >> 1) & 1, abort_flag)) return false;
             tc::tc_fence_after();
             __nv_bfloat16* dst = p.chunk_states + ((bh * g.nchunks + c) * S + s) * H + col0;
@@ -315,7 +327,8 @@ bool plan(const Geom& g, SpTcParams& p) {
     const int H = (int)g.headdim;
     p.nsb = (int)(g.chunk / kKb);
     p.off_x_in_stage = 2 * kKb * 128;
-    p.stage_bytes = p.off_x_in_stage + (H / 64) * kKb * 128;
+    p.off_w_in_stage = p.off_x_in_stage + (H / 64) * kKb * 128;
+    p.stage_bytes = p.off_w_in_stage + 1024;  // w[64] and exp2(G_last), padded to keep stages 1 KB aligned
     p.tmem_cols = (3 * H <= 256) ? 256 : 512;
     // two CTAs per SM when TMEM allows, else one with a deeper ring
     const uint32_t budget = (p.tmem_cols == 256) ? (kSmemLimit / 2 - 2048) : kSmemLimit;

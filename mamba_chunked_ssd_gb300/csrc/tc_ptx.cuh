@@ -126,6 +126,19 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy (no register staging); with
+// src_bytes = 0 the destination is zero-filled and nothing is read.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Generic-proxy writes to shared memory (st.shared) become visible to the
 // async proxy (TMA, tcgen05.mma) after this fence plus a thread sync.
 __device__ __forceinline__ void fence_proxy_async_smem() {
