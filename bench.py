@@ -98,6 +98,27 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of
+    this workload, or None when there is none or the kernel's source has
+    changed since the counters were taken (the summary records its hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_{workload}.md")
+    try:
+        fields = {}
+        for line in open(path):
+            if ":" in line and not line.startswith((" ", "|", "#")):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        src = os.path.join(ROOT, fields["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != fields["source_sha256_16"]:
+            return None
+        return float(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 # ------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
@@ -361,7 +382,8 @@ def main():
                           "tensor_frac": flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                           "peaks": peaks["source"]},
         "roofline": {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None},
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": load_traffic(top, w.name), "algorithmic_bytes": kb[top]},
         "kernel_ms": r["kernel_ms"],
         "gpu_launches": 3 * args.steps,
         "e2e": None if r["e2e_ms"] is None else {
