@@ -45,6 +45,12 @@ constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kSmemLimit = 232448;
 constexpr int kMaxStages = 2;
 constexpr int kMaxStreams = 2;
+// Fill barriers of the X / h stages.  Head k fills stage k % nst and is read
+// by stream k % nstr; its fill is signalled on barrier k % nfill with
+// nfill = max(nst, nstr), so that each barrier's fills all go to one stage and
+// one stream and every waiter sees each phase of it in order (a waiter that
+// skipped a phase would take the next-but-one phase parity for its own).
+constexpr int kMaxFill = kMaxStages > kMaxStreams ? kMaxStages : kMaxStreams;
 
 // TMEM columns (512 allocated): CB_II at 0 (128 fp32 columns); stream s keeps
 // P (128 bf16 = 64 columns) at 128 + 64 s, Z at 256 + 2 H s and Y2 right after
@@ -59,6 +65,7 @@ struct CoTcParams {
     int nhb;          // heads per CTA (all in one group)
     int nst;          // X / h pipeline stages
     int nstr;         // epilogue head streams (2 for H = 64, 1 for H = 128)
+    int nfill;        // stage-fill barriers, max(nst, nstr)
     int head_blocks;  // nheads / nhb
     uint32_t off_C, off_CB10, off_X0v, off_stage, stage_bytes, off_h_in_stage, off_small, off_bar, smem_bytes;
     const float* dt;
@@ -76,8 +83,8 @@ enum : int {
     kBarPReady = kBarOpsReady + kMaxStreams,   // [kMaxStreams]
     kBarYDone = kBarPReady + kMaxStreams,      // [kMaxStreams]
     kBarYFree = kBarYDone + kMaxStreams,       // [kMaxStreams]
-    kBarFull = kBarYFree + kMaxStreams,        // [kMaxStages]
-    kBarSlotFree = kBarFull + kMaxStages,      // [kMaxStages]
+    kBarFull = kBarYFree + kMaxStreams,        // [kMaxFill]
+    kBarSlotFree = kBarFull + kMaxFill,        // [kMaxStages]
     kNumBars = kBarSlotFree + kMaxStages
 };
 
@@ -158,10 +165,8 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::mbar_init(&bars[kBarYDone + i], 1);
             tc::mbar_init(&bars[kBarYFree + i], wps);
         }
-        for (int i = 0; i < kMaxStages; ++i) {
-            tc::mbar_init(&bars[kBarFull + i], 1);
-            tc::mbar_init(&bars[kBarSlotFree + i], 1 + wps);
-        }
+        for (int i = 0; i < kMaxFill; ++i) tc::mbar_init(&bars[kBarFull + i], 1);
+        for (int i = 0; i < kMaxStages; ++i) tc::mbar_init(&bars[kBarSlotFree + i], 1 + wps);
         ctl->abort = 0;
         tc::fence_barrier_init();
     }
@@ -200,13 +205,14 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 }
                 uint8_t* sX = sStage + st * p.stage_bytes;
                 uint8_t* sH = sX + p.off_h_in_stage;
-                tc::mbar_arrive_expect_tx(&bars[kBarFull + st], x_bytes + h_bytes);
+                uint64_t* full = &bars[kBarFull + k % p.nfill];
+                tc::mbar_arrive_expect_tx(full, x_bytes + h_bytes);
                 const int h = h0 + k;
                 for (int cb = 0; cb < H / 64; ++cb) {
                     for (int rb = 0; rb < Tj / 128; ++rb)
-                        tc::tma_load_4d(sX + cb * (Tj * 128) + rb * 16384, &tm_x, &bars[kBarFull + st], cb * 64, h,
+                        tc::tma_load_4d(sX + cb * (Tj * 128) + rb * 16384, &tm_x, full, cb * 64, h,
                                         (int)(t0 + 128 * rb), (int)b);
-                    tc::tma_load_2d(sH + cb * (S * 128), &tm_h, &bars[kBarFull + st], cb * 64,
+                    tc::tma_load_2d(sH + cb * (S * 128), &tm_h, full, cb * 64,
                                     (int)(((b * g.nheads + h) * g.nchunks + c) * S));
                 }
             }
@@ -238,7 +244,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 const uint32_t aX = tc::smem_u32(sX), aH = tc::smem_u32(sX + p.off_h_in_stage);
                 const uint32_t aX0v = tc::smem_u32(smem + p.off_X0v + s * (128 * H * 2));
                 const uint32_t tz = tmem + col_z(s, H), ty2 = tz + H;
-                if (!tc::mbar_wait(&bars[kBarFull + st], (k / p.nst) & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarFull + k % p.nfill], (k / p.nfill) & 1, abort_flag)) { ok = false; break; }
                 if (n >= 1 && !tc::mbar_wait(&bars[kBarYFree + s], (n - 1) & 1, abort_flag)) { ok = false; break; }
                 if (I == 1 && !tc::mbar_wait(&bars[kBarOpsReady + s], n & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
@@ -356,7 +362,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 wv[96 * t + 64 + lane] = exp2f(g_r[t] - cur.gcol[t]) * cur.dtcol[t];
             }
             __syncwarp();
-            if (!tc::mbar_wait(&bars[kBarFull + st], (k / p.nst) & 1, abort_flag)) { ok = false; break; }
+            if (!tc::mbar_wait(&bars[kBarFull + k % p.nfill], (k / p.nfill) & 1, abort_flag)) { ok = false; break; }
             uint8_t* sX = sStage + st * p.stage_bytes;
 
             if (I == 1) {
@@ -502,6 +508,7 @@ bool plan_smem(const Geom& g, CoTcParams& p) {
         const uint32_t total = off_bar + kNumBars * 8 + 64 + 1024;  // + ctl + alignment slack
         if (total <= (uint32_t)kSmemLimit) {
             p.nst = nst;
+            p.nfill = nst > p.nstr ? nst : p.nstr;
             p.off_small = off_small;
             p.off_bar = off_bar;
             p.smem_bytes = total;

@@ -40,6 +40,9 @@ SMALL = [
     Workload("bf16_t128_groups", 2, 640, 8, 64, 64, 4, 128, init_state=True),
     Workload("bf16_h128_s256", 1, 384, 8, 128, 256, 2, 128, dt_mu=-4.0, init_state=True),
     Workload("bf16_t64", 1, 320, 2, 64, 128, 1, 64, init_state=True),
+    # one X/h stage with two head streams in the output kernel
+    Workload("bf16_t256_s256_h64", 1, 700, 6, 64, 256, 1, 256, init_state=True),
+    Workload("bf16_t256_s256_h64_4heads_per_cta", 2, 512, 8, 64, 256, 2, 256),
 ]
 
 
@@ -152,3 +155,31 @@ def test_misaligned_device_pointer_rejected():
     with pytest.raises(bd.Mamba2Error) as e:
         bd.mamba2_ssd_fwd(x_off, d["dt"], d["A"], d["B"], d["C"], w.chunk_size)
     assert e.value.code == 1
+
+
+def _sweep_cover():
+    """One sweep shape for every (S, H, T) combination; the sequence lengths
+    rotate so that each (H, T) pair meets three of the four lengths and each
+    length appears three times."""
+    from mamba_chunked_ssd_gb300.synthetic import sweep_workloads
+    by_name = {w.name: w for w in sweep_workloads(seeds=(0,))}
+    Ls = (1024, 4096, 16384, 32768)
+    combos = [(S, H, T) for S in (64, 128, 256) for H in (64, 128) for T in (128, 256)]
+    return [by_name[f"sweep_L{Ls[(i + i // 4) % 4]}_S{S}_H{H}_T{T}"] for i, (S, H, T) in enumerate(combos)]
+
+
+SWEEP = _sweep_cover()
+
+
+@pytest.mark.parametrize("w", SWEEP, ids=[w.name for w in SWEEP])
+def test_sweep_shape_sampled(w):
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    y, fin = _fwd(d, w)
+    pairs = sample_pairs(w.batch, w.nheads, 3, seed=w.seqlen)
+    ref = oracle_pairs(inp, pairs)
+    y_c, fin_c = y.cpu(), fin.cpu()
+    for b, h in pairs:
+        assert rel_err(np64(y_c[b, :, h]), ref[(b, h)][0]) <= TOL[w.dtype], (b, h)
+        assert rel_err(np64(fin_c[b, h]), ref[(b, h)][1]) <= TOL[w.dtype], (b, h)
+    assert torch.isfinite(y.float()).all()
