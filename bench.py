@@ -44,6 +44,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
     p.add_argument("--soak-s", type=float, default=1.0,
                    help="seconds of untimed steps run under the clock sampler before the timed region")
+    p.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     p.add_argument("--cpu-pairs", type=int, default=256,
                    help="(batch, head) pairs the oracle runs for the CPU baseline sample")
     return p.parse_args()
@@ -222,7 +223,61 @@ def run_oracle_sample(w, inp, npairs, prepared=None):
                       f"tokens/s scaled by the fraction of sequences covered"}
 
 
+def decode_bytes(w):
+    """Algorithmic bytes of one decode step: the fp32 state read and written,
+    x read and y written, B, C, dt read (A, D are negligible)."""
+    e = 2 if w.dtype == "bf16" else 4
+    state = 4 * w.batch * w.nheads * w.dstate * w.headdim
+    return 2 * state + 2 * w.batch * w.nheads * w.headdim * e + 2 * w.batch * w.ngroups * w.dstate * e \
+        + 4 * w.batch * w.nheads
+
+
 # ----------------------------------------------------------------- GPU arm
+def run_decode(args, w, peaks):
+    """mamba2_ssd_step on `w` (seqlen 1), state updated in place, L2 flushed
+    before each timed step; returns the decode_step object of the JSON line."""
+    import torch
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+
+    inp = make_inputs(w)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    x, dt, B, C = (d[k][:, 0].contiguous() for k in ("x", "dt", "B", "C"))
+    state = d["initial_state"]
+    y = torch.empty_like(x)
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        bd.mamba2_ssd_step(x, dt, d["A"], B, C, state_in=state, D=d["D"], state_out=state, y=y)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(max(args.steps, 10)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        ms.append((a, b))
+    torch.cuda.synchronize()
+    bd.mamba2_check_device_status()
+    t = statistics.mean(a.elapsed_time(b) for a, b in ms)
+    nbytes = decode_bytes(w)
+    achieved = nbytes / (t * 1e-3) / 1e9
+    return {"workload": w.name, "batch": w.batch, "nheads": w.nheads, "headdim": w.headdim,
+            "dstate": w.dstate, "ngroups": w.ngroups, "dtype": w.dtype,
+            "value": w.batch / (t * 1e-3), "unit": "tokens/s", "ms_per_step": t,
+            "roofline": {"kernel": "k_ssd_step", "bound": "hbm", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "algorithmic_bytes": nbytes, "traffic": load_traffic("ssd_step", w.name)},
+            "l2": "flushed before every timed step; state updated in place"}
+
+
+
 def run_gpu(args, w, rank, world):
     import torch
     import torch.distributed as dist
@@ -391,6 +446,8 @@ def main():
             "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "clocks": r["clocks"],
     }
+    if not args.no_decode and w.seqlen > 1:
+        out["decode_step"] = run_decode(args, WORKLOADS["decode_b256"], peaks)
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = run_oracle_sample(w, r["inp"], args.cpu_pairs)
         out["cpu_baseline"].pop("seconds", None)

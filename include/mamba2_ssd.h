@@ -155,6 +155,33 @@ MAMBA2_API mamba2_status mamba2_ssd_fwd_noalloc(const mamba2_shape* shape, const
                                                 const float* initial_state, void* y, float* final_state,
                                                 struct CUstream_st* stream);
 
+/* One recurrent step: the single-token decode step that continues each
+ * (batch, head) sequence from a carried state [blog §Mamba-2 architecture:
+ * the recurrent form is the one suited to sequential inference; §Kernel 2:
+ * the final state of a pass is fed back as the next call's initial state].
+ *
+ *   h  <- exp(A[h] dt[b,h]) h + dt[b,h] B[b,g] x[b,h]^T    (g = h / (nh/G))
+ *   y[b,h] = C[b,g]^T h + D[h] x[b,h]                      (updated h)
+ *
+ * This is mamba2_ssd_fwd on a one-token sequence: `shape->seqlen` must be 1
+ * (else MAMBA2_ERR_INVALID_ARG) and chunk_size is not used (any valid value).
+ * Layouts are mamba2_ssd_fwd's with L = 1:
+ *   x, y        [b, nh, H]  dtype of shape->dtype
+ *   dt          [b, nh]     fp32 (already activated, >= 0)
+ *   A, D        [nh]        fp32 (D may be NULL: no skip term)
+ *   B, C        [b, G, S]   dtype of shape->dtype
+ *   state_in    [b, nh, S, H] fp32, NULL means zeros
+ *   state_out   [b, nh, S, H] fp32, required
+ * state_out may be the same pointer as state_in (update in place); any other
+ * overlap between tensors is MAMBA2_ERR_INVALID_ARG.  The decay is computed
+ * as exp2(log2(e) * A * dt) in fp32, like stage 1 of the forward pass.  All
+ * pointers are caller-owned device memory, 16-byte aligned; nothing is
+ * allocated; the step is enqueued on `stream` and never synchronises. */
+MAMBA2_API mamba2_status mamba2_ssd_step(const mamba2_shape* shape, const void* x, const float* dt,
+                                         const float* A, const void* B, const void* C, const float* D,
+                                         const float* state_in, float* state_out, void* y,
+                                         struct CUstream_st* stream);
+
 /* Reads (and clears) the current device's status word.  SYNCHRONISES `stream`.
  * Returns MAMBA2_ERR_TIMEOUT if a kernel's bounded wait ran out since the
  * last check, MAMBA2_ERR_CUDA if the stream reports an error, else MAMBA2_OK. */

@@ -59,6 +59,7 @@ def load_library(path: str = LIB_PATH):
         "mamba2_ssd_fwd_workspace_size": (ctypes.c_size_t, [S]),
         "mamba2_ssd_fwd": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]),
         "mamba2_ssd_fwd_noalloc": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P]),
+        "mamba2_ssd_step": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P]),
         "mamba2_check_device_status": (ctypes.c_int, [P]),
         "mamba2_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "mamba2_version": (ctypes.c_int, []),
@@ -202,6 +203,25 @@ def mamba2_ssd_fwd_noalloc(x, dt, A, B, C, chunk_size, D=None, initial_state=Non
         ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
         _ptr(initial_state), _ptr(y), _ptr(final_state), _stream(stream)))
     return y, final_state
+
+
+def mamba2_ssd_step(x, dt, A, B, C, state_in=None, D=None, state_out=None, y=None, stream=None):
+    """One decode step: x [b, nh, H], dt [b, nh], B, C [b, G, S], state
+    [b, nh, S, H] fp32.  Returns (y [b, nh, H], state_out).  Pass
+    state_out=state_in to update the state in place."""
+    for t, n in ((x, "x"), (dt, "dt"), (A, "A"), (B, "B"), (C, "C"), (D, "D"),
+                 (state_in, "state_in"), (state_out, "state_out")):
+        _need(t, n)
+    b, nh, H = x.shape
+    shape = make_shape(b, 1, nh, H, B.shape[2], B.shape[1], 1, _dtype_code(x))
+    if y is None:
+        y = torch.empty_like(x)
+    if state_out is None:
+        state_out = torch.empty(b, nh, B.shape[2], H, device=x.device, dtype=torch.float32)
+    _check("mamba2_ssd_step", load_library().mamba2_ssd_step(
+        ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+        _ptr(state_in), _ptr(state_out), _ptr(y), _stream(stream)))
+    return y, state_out
 
 
 def mamba2_check_device_status(stream=None):

@@ -8,7 +8,7 @@
 namespace m2 {
 namespace {
 
-constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kVersion = 1 * 10000 + 1 * 100 + 0;
 
 // Per-device status word: kernels with bounded waits record a timeout here.
 __device__ unsigned int g_status_word = 0;
@@ -207,6 +207,26 @@ mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const flo
     if ((rc = run_state_pass(*shape, sp, st)) != MAMBA2_OK) return rc;
     const ChunkOutArgs co{x, dt, B, C, D, G, cs, y};
     return run_chunk_out(*shape, co, st);
+}
+
+mamba2_status mamba2_ssd_step(const mamba2_shape* shape, const void* x, const float* dt, const float* A,
+                              const void* B, const void* C, const float* D, const float* state_in,
+                              float* state_out, void* y, struct CUstream_st* stream) {
+    mamba2_status rc = check_shape(shape);
+    if (rc != MAMBA2_OK) return rc;
+    if (shape->seqlen != 1) return MAMBA2_ERR_INVALID_ARG;
+    const Sizes z = sizes_of(*shape);
+    // In place (state_in == state_out) is allowed: each state element is read
+    // and then written by the same thread.  Any other overlap is rejected.
+    const bool in_place = state_in != nullptr && state_in == state_out;
+    const Arg in[] = {{x, z.x, false},  {dt, z.dt, false}, {A, z.A, false},
+                      {B, z.bc, false}, {C, z.bc, false},  {D, z.D, true},
+                      {in_place ? nullptr : state_in, z.state, true}};
+    const Arg out[] = {{y, z.x, false}, {state_out, z.state, false}};
+    if ((rc = check_ptrs(in, 7, out, 2)) != MAMBA2_OK) return rc;
+    if (shape->batch == 0) return MAMBA2_OK;
+    const SsdStepArgs a{x, dt, A, B, C, D, state_in, state_out, y};
+    return from_cuda(launch_ssd_step(make_geom(*shape), shape->dtype == MAMBA2_BF16, a, (cudaStream_t)stream));
 }
 
 mamba2_status mamba2_check_device_status(struct CUstream_st* stream) {

@@ -76,10 +76,24 @@ struct ChunkOutArgs {
     void* y;
 };
 
+struct SsdStepArgs {
+    const void* x;  // [b, nh, H]
+    const float* dt;
+    const float* A;
+    const void* B;  // [b, G, S]
+    const void* C;
+    const float* D;         // may be null
+    const float* state_in;  // may be null (zeros); may equal state_out
+    float* state_out;
+    void* y;
+};
+
 cudaError_t launch_chunk_cumsum(const Geom& g, const float* dt, const float* A, float* G,
                                 cudaStream_t st);
 cudaError_t launch_state_pass_simt(const Geom& g, bool bf16, const StatePassArgs& a, cudaStream_t st);
 cudaError_t launch_chunk_out_simt(const Geom& g, bool bf16, const ChunkOutArgs& a, cudaStream_t st);
+
+cudaError_t launch_ssd_step(const Geom& g, bool bf16, const SsdStepArgs& a, cudaStream_t st);
 
 // Tensor-core kernels (bf16) and the shapes they cover.
 bool chunk_out_tc_fits(const Geom& g);

@@ -57,6 +57,9 @@ WORKLOADS = {
     "long_seq_carried_state": Workload("long_seq_carried_state", 4, 8192, 64, 64, 128, 1, 256,
                                        init_state=True),
     "large_state": Workload("large_state", 2, 16384, 32, 128, 256, 8, 128, dt_mu=-4.0),
+    # one decode step (seqlen 1) for 256 sequences of the same layer, each
+    # carrying a state: the inference use of the carried final state
+    "decode_b256": Workload("decode_b256", 256, 1, 64, 64, 128, 1, 1, init_state=True),
 }
 
 

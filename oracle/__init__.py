@@ -133,6 +133,17 @@ def ssd_recurrence(x, dt, A, B, C, D=None, init=None, chunk_size=None, pairs=Non
     return out
 
 
+def ssd_step(x, dt, A, B, C, state=None, D=None):
+    """One decode step: the recurrence advanced by one token from ``state``
+    ("Accelerating Mamba-2 ...", §Mamba-2 architecture, core recurrence; the
+    carried state of §Kernel 2).  x [b, nh, H], dt [b, nh], B, C [b, G, S],
+    state [b, nh, S, H] or None (zeros).  It is the token-by-token recurrence
+    on a one-token sequence.  Returns (y [b, nh, H], new state [b, nh, S, H])."""
+    x, dt, B, C = (_f64(t)[:, None] for t in (x, dt, B, C))
+    r = ssd_recurrence(x, dt, A, B, C, D=D, init=state)
+    return r["y"][:, 0], r["final_state"]
+
+
 def chunk_cumsum(dt, A, chunk_size, pairs=None, nthreads=None):
     """Stage 1: G [batch, nheads, L] (log2 units), fp64."""
     dt, A = _f64(dt), _f64(A)

@@ -19,13 +19,13 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = bd.header_functions()
-    assert len(names) == 9
+    assert len(names) == 10
     for n in names:
         assert hasattr(lib, n), f"{n} declared in the header but not exported"
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mamba2_version() == 10000
+    assert lib.mamba2_version() == 10100
     for code in range(5):
         s = lib.mamba2_status_string(code).decode()
         assert s.startswith(bd.STATUS[code])
@@ -113,3 +113,32 @@ def test_ssd_fwd_rejects_small_or_misaligned_workspace(lib):
     assert small == INVALID
     misaligned = lib.mamba2_ssd_fwd(ctypes.byref(s), *ptrs, _p(FAKE * 4096 + 16), need, None)
     assert misaligned == INVALID
+
+
+def _step(lib, shape, x=FAKE, dt=FAKE * 2, A=FAKE * 3, B=FAKE * 4, C=FAKE * 5, D=None,
+          state_in=FAKE * 8, state_out=FAKE * 16, y=FAKE * 6):
+    return lib.mamba2_ssd_step(ctypes.byref(shape), _p(x), _p(dt), _p(A), _p(B), _p(C),
+                               _p(D) if D else None, _p(state_in) if state_in else None,
+                               _p(state_out) if state_out else None, _p(y), None)
+
+
+def test_step_requires_one_token(lib):
+    assert _step(lib, _shape(seqlen=2)) == INVALID
+    assert _step(lib, _shape(seqlen=0)) == INVALID
+
+
+def test_step_requires_state_out(lib):
+    assert _step(lib, _shape(seqlen=1), state_out=None) == INVALID
+
+
+def test_step_rejects_partial_state_overlap(lib):
+    # state [1, 2, 16, 16] fp32 = 2048 bytes; a 16-byte shift overlaps
+    assert _step(lib, _shape(seqlen=1), state_in=FAKE * 16, state_out=FAKE * 16 + 16) == INVALID
+
+
+def test_step_rejects_y_over_state(lib):
+    assert _step(lib, _shape(seqlen=1), y=FAKE * 16 + 64) == INVALID
+
+
+def test_step_rejects_misaligned(lib):
+    assert _step(lib, _shape(seqlen=1), x=FAKE + 8) == INVALID

@@ -67,3 +67,46 @@ def test_rejects_bad_group_count(oracle_mod):
     with pytest.raises(ValueError):
         oracle_mod.ssd_recurrence(p["x"], p["dt"], p["A"], np.repeat(p["B"], 2, axis=2),
                                   np.repeat(p["C"], 2, axis=2))
+
+
+def _step_slice(p, t):
+    """Token t of a problem, in the decode step's layouts."""
+    return p["x"][:, t], p["dt"][:, t], p["B"][:, t], p["C"][:, t]
+
+
+def test_step_matches_brute_force(oracle_mod):
+    """The decode step against the unrolled expansion on a one-token problem
+    (groups, S != H, a carried state: a transposed or mis-grouped operand fails)."""
+    p = pins.random_problem(15, 2, 1, 4, 3, 5, 2)
+    y, h = oracle_mod.ssd_step(*_step_slice(p, 0)[:2], p["A"], *_step_slice(p, 0)[2:], state=p["init"],
+                               D=p["D"])
+    y_bf, h_bf = pins.brute_force(p)
+    assert pins.rel_err(y, y_bf[:, 0]) <= pins.TOL
+    assert pins.rel_err(h, h_bf) <= pins.TOL
+
+
+def test_steps_compose_to_the_recurrence(oracle_mod):
+    """K decode steps from a prefill state equal the recurrence over the whole
+    sequence, bit for bit (the state hand-off of the blog's §Kernel 2)."""
+    p = pins.random_problem(16, 2, 9, 4, 3, 5, 2)
+    full = oracle_mod.ssd_recurrence(p["x"], p["dt"], p["A"], p["B"], p["C"], D=p["D"], init=p["init"])
+    pre = oracle_mod.ssd_recurrence(p["x"][:, :6], p["dt"][:, :6], p["A"], p["B"][:, :6], p["C"][:, :6],
+                                    D=p["D"], init=p["init"])
+    h = pre["final_state"]
+    for t in range(6, 9):
+        x, dt, B, C = _step_slice(p, t)
+        y, h = oracle_mod.ssd_step(x, dt, p["A"], B, C, state=h, D=p["D"])
+        assert np.array_equal(y, full["y"][:, t])
+    assert np.array_equal(h, full["final_state"])
+
+
+def test_step_scalar_closed_form(oracle_mod):
+    """S = H = 1: h' = e^{A dt} h + dt b x and y = c h' + D x, by hand."""
+    import math
+    x, dt, A, b, c, D, h0 = 0.7, 0.25, -1.3, 1.9, -0.4, 0.6, 2.0
+    y, h = oracle_mod.ssd_step(np.full((1, 1, 1), x), np.full((1, 1), dt), np.array([A]),
+                               np.full((1, 1, 1), b), np.full((1, 1, 1), c), state=np.full((1, 1, 1, 1), h0),
+                               D=np.array([D]))
+    h_ref = math.exp(A * dt) * h0 + dt * b * x
+    assert abs(h[0, 0, 0, 0] - h_ref) <= 1e-15 * abs(h_ref)
+    assert abs(y[0, 0, 0] - (c * h_ref + D * x)) <= 1e-14
