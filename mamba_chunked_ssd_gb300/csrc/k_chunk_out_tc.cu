@@ -1,37 +1,42 @@
 // k_chunk_out_tc.cu — stage 3 on the 5th-generation tensor cores (bf16).
 //
-// [blog §Kernel 3] computes, per chunk and head,
+// "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA
+// CUDA Tile", §Kernel 3, computes per chunk and head
 //     Y = exp2(G) (C h_c) + ((C B^T) . exp2(G_i - G_j) . dt_j . causal M) X + D X.
 // GB300 design.  One CTA owns (batch, chunk, 128-row block I of the chunk,
 // a block of heads sharing one B/C group); T = 128 has one row block, T = 256
 // two.  Rows of block I see columns j < 128 (I + 1); the interaction matrix
 // is split along j into the block on the diagonal (j in block I) and, for
 // I = 1, the block below it (j in block 0).
-//   warp 0       TMA producer: C (rows of block I) and B (rows 0 .. 128I+127)
-//                once, then per head X (same rows) and h_c;
+//   warp 0       producer: TMA of C and B once, then per head X (rows of
+//                blocks 0 .. I) and h_c into a ring of stages; its 32 lanes
+//                gather the head's G, dt and D into the same stage with
+//                cp.async, so the epilogue never waits on a global load;
 //   warp 1       TMEM allocator and single-thread tcgen05.mma issuer;
 //   warps 2..17  epilogue, split into head streams (two when H = 64, one when
 //                H = 128) that take alternate heads, each stream with its own
 //                TMEM accumulators so one stream's arithmetic overlaps the
 //                other's tensor-core work.
 // Once per CTA (per group, shared by every head):
-//   CB_II = C_I B_I^T -> TMEM;  for I = 1 also CB_10 = C_1 B_0^T, converted to
-//   bf16 into shared memory as an MMA operand.
+//   CB_II = C_I B_I^T -> TMEM, causally masked in place;  for I = 1 also
+//   CB_10 = C_1 B_0^T, converted to bf16 into shared memory as an MMA operand.
 // Per head, with a = exp2(G_127) and v_j = exp2(G_127 - G_j) dt_j for I = 1
 // (a = 1 and no second term for I = 0):
 //   Z  = C_I (a h_c) + CB_10 (v . X_0)     tcgen05; a h_c and v . X_0 are
-//                                          formed on chip by the epilogue
-//   P  = CB_II . exp2(G_i - G_j) dt_j . M  epilogue, written back to TMEM as
-//                                          bf16 and consumed there as operand A
+//                                          scaled in place in the stage
+//   P  = CB_II . w_j                       epilogue, written to TMEM as bf16 and
+//                                          consumed there as operand A
 //   Y2 = P X_I                             tcgen05, A from TMEM
-//   y_i = exp2(G_i - G_ref) Z + Y2 + D x_i  (G_ref = G_127 for I = 1, else 0).
-// This is the exact identity exp2(G_i - G_j) = exp2(G_i - G_127) exp2(G_127 - G_j)
-// for j <= 127 < i, with both factors <= 1 because a_t <= 0 keeps G
-// non-increasing inside a chunk.  Inside the diagonal block the same identity
-// is used per 32-column group strictly below the diagonal (reference column =
-// the group's last one); the diagonal 32 x 32 groups use exp2(G_i - G_j)
-// directly and masked entries are selected to zero, never multiplied.  The
-// T x T matrix never reaches global memory.
+//   y_i = exp2(G_i - G_ref) Z + u_i Y2 + D x_i  (G_ref = G_127 for I = 1, else 0)
+// with the decay of each row split at r, the last column before the row's
+// 32-row quadrant:  exp2(G_i - G_j) dt_j = u_i w_j,  u_i = exp2(G_i - G_r),
+// w_j = exp2(G_r - G_j) dt_j.  Both splits are exact identities; a_t <= 0
+// keeps G non-increasing inside a chunk, so u_i <= 1 and w_j <= dt_j left of
+// the quadrant.  A row whose u_i would fall below 2^-96 (a very strong decay
+// inside its quadrant) takes exp2(G_i - G_j) per entry and u_i = 1.  Every
+// row's arithmetic depends only on its own and earlier tokens.  Masked
+// entries are zero in CB before any weight multiplies them.  The T x T matrix
+// never reaches global memory.
 // Every wait is bounded; a timeout sets the status word and the CTA unwinds.
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -43,18 +48,21 @@ namespace {
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kSmemLimit = 232448;
-constexpr int kMaxStages = 2;
+constexpr int kMaxStages = 3;
 constexpr int kMaxStreams = 2;
-// Fill barriers of the X / h stages.  Head k fills stage k % nst and is read
-// by stream k % nstr; its fill is signalled on barrier k % nfill with
-// nfill = max(nst, nstr), so that each barrier's fills all go to one stage and
+// Fill barriers of the stages.  Head k fills stage k % nst and is read by
+// stream k % nstr; its fill is signalled on barrier k % nfill with
+// nfill = lcm(nst, nstr), so that each barrier's fills all go to one stage and
 // one stream and every waiter sees each phase of it in order (a waiter that
 // skipped a phase would take the next-but-one phase parity for its own).
-constexpr int kMaxFill = kMaxStages > kMaxStreams ? kMaxStages : kMaxStreams;
+constexpr int kMaxFill = 6;  // lcm(3, 2)
+// Arrivals that complete a fill: the producer's expect-tx, then one per lane
+// when that lane's cp.async gathers have landed.
+constexpr int kFillArrivals = 1 + 32;
 
-// TMEM columns (512 allocated): CB_II at 0 (128 fp32 columns); stream s keeps
-// P (128 bf16 = 64 columns) at 128 + 64 s, Z at 256 + 2 H s and Y2 right after
-// Z.  During set-up CB_10 is staged in columns [256, 384).
+// TMEM columns (512 allocated): CB_II fp32 at [0, 128); P of stream s (bf16,
+// 64 columns) at 128 + 64 s; Z and Y2 of stream s (fp32, H columns each) at
+// 256 + 2 H s.  CB_10 is staged at [256, 384) before any stream uses it.
 constexpr uint32_t kColCB = 0;
 __host__ __device__ constexpr uint32_t col_p(int s) { return 128u + 64u * (uint32_t)s; }
 __host__ __device__ constexpr uint32_t col_z(int s, int H) { return 256u + 2u * (uint32_t)H * (uint32_t)s; }
@@ -63,11 +71,14 @@ struct CoTcParams {
     Geom g;
     int T;            // chunk size (128 or 256)
     int nhb;          // heads per CTA (all in one group)
-    int nst;          // X / h pipeline stages
+    int nst;          // pipeline stages
     int nstr;         // epilogue head streams (2 for H = 64, 1 for H = 128)
-    int nfill;        // stage-fill barriers, max(nst, nstr)
+    int nfill;        // stage-fill barriers, lcm(nst, nstr)
     int head_blocks;  // nheads / nhb
-    uint32_t off_C, off_CB10, off_X0v, off_stage, stage_bytes, off_h_in_stage, off_small, off_bar, smem_bytes;
+    // shared-memory layout: C, CB_10, then the stages; a stage holds
+    // X [T rows x H] | h_c [S x H] | G[T] dt[T] D
+    uint32_t off_C, off_CB10, off_stage, stage_bytes, off_h_in_stage, off_vec_in_stage, off_small, off_bar,
+        smem_bytes;
     const float* dt;
     const float* G;
     const float* D;
@@ -79,7 +90,7 @@ enum : int {
     kBarCbFull = 0,
     kBarCbDone,
     kBarCb10Ready,
-    kBarOpsReady,                            // [kMaxStreams]
+    kBarOpsReady,                              // [kMaxStreams]
     kBarPReady = kBarOpsReady + kMaxStreams,   // [kMaxStreams]
     kBarYDone = kBarPReady + kMaxStreams,      // [kMaxStreams]
     kBarYFree = kBarYDone + kMaxStreams,       // [kMaxStreams]
@@ -98,30 +109,49 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
     if (status) atomicExch(status, kStatusTimeout);
 }
 
-// Scales the 16-byte bf16 chunks [c_begin, c_end) of one 128-byte-swizzled row
-// (chunk index = physical position, rotated by the row to spread banks) from
-// src into dst by f.  Boxes of 64 columns sit box_stride bytes apart.
-__device__ __forceinline__ void scale_row_chunks(const uint8_t* src, uint8_t* dst, uint32_t src_box_stride,
-                                                 uint32_t dst_box_stride, int row, int c_begin, int n, float f) {
-    uint4 v[4];
+// Largest exponent (log2 units) either factor of the split decay may carry:
+// P entries then stay below 2^96 |CB| dt, far from the bf16 / fp32 range.
+constexpr float kMildSpan = 96.f;
+// Upper clamp of a column weight: keeps 0 x weight = 0 for the masked entries
+// whatever dt is (a NaN weight is kept: the comparison is false for NaN).
+constexpr float kWMax = 0x1p120f;
+
+// exp2(G_i - G_j) dt_j for the direct path, exponent clamped at kMildSpan so
+// that masked entries (j > i) multiply a finite weight.
+__device__ __forceinline__ float exact_weight(float gi, float gj, float dtj) {
+    const float w = exp2f(fminf(gi - gj, kMildSpan)) * dtj;
+    return w > kWMax ? kWMax : w;
+}
+
+// Scales, in place, the 16-byte bf16 chunks [c_begin, c_begin + n) of one
+// 128-byte-swizzled row (chunk index = physical position, rotated by the row
+// to spread banks) by f, rounded once to bf16 per element (bf16x2 multiplies
+// by f rounded to bf16).  Boxes of 64 columns sit box_stride bytes apart.
+__device__ __forceinline__ void scale_row_chunks(uint8_t* base, uint32_t box_stride, int row, int c_begin, int n,
+                                                 float f) {
+    const uint32_t f2 = tc::pack_bf16x2(f, f);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        if (t >= n) break;
-        const int c = c_begin + t;
-        const int pc = ((c & 7) + row) & 7;
-        v[t] = *reinterpret_cast<const uint4*>(src + (c >> 3) * src_box_stride + row * 128 + pc * 16);
-    }
+    for (int t0 = 0; t0 < 4; t0 += 2) {  // two chunks in flight
+        uint4 v[2];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        if (t >= n) break;
-        const int c = c_begin + t;
-        const int pc = ((c & 7) + row) & 7;
-        uint4 w = v[t];
-        w.x = tc::pack_bf16x2(tc::bf16_lo(w.x) * f, tc::bf16_hi(w.x) * f);
-        w.y = tc::pack_bf16x2(tc::bf16_lo(w.y) * f, tc::bf16_hi(w.y) * f);
-        w.z = tc::pack_bf16x2(tc::bf16_lo(w.z) * f, tc::bf16_hi(w.z) * f);
-        w.w = tc::pack_bf16x2(tc::bf16_lo(w.w) * f, tc::bf16_hi(w.w) * f);
-        *reinterpret_cast<uint4*>(dst + (c >> 3) * dst_box_stride + row * 128 + pc * 16) = w;
+        for (int t = 0; t < 2; ++t) {
+            if (t0 + t >= n) break;
+            const int c = c_begin + t0 + t;
+            const int pc = ((c & 7) + row) & 7;
+            v[t] = *reinterpret_cast<const uint4*>(base + (c >> 3) * box_stride + row * 128 + pc * 16);
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (t0 + t >= n) break;
+            const int c = c_begin + t0 + t;
+            const int pc = ((c & 7) + row) & 7;
+            uint4 w = v[t];
+            w.x = tc::mul_bf16x2(w.x, f2);
+            w.y = tc::mul_bf16x2(w.y, f2);
+            w.z = tc::mul_bf16x2(w.z, f2);
+            w.w = tc::mul_bf16x2(w.w, f2);
+            *reinterpret_cast<uint4*>(base + (c >> 3) * box_stride + row * 128 + pc * 16) = w;
+        }
     }
 }
 
@@ -151,7 +181,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     uint8_t* sC = smem + p.off_C;
     uint8_t* sCB10 = smem + p.off_CB10;
     uint8_t* sStage = smem + p.off_stage;
-    uint8_t* sB = sCB10;  // B occupies [CB_10 .. stages) until the CB products are done
+    uint8_t* sB = sCB10;  // B overlays CB_10 and the stages until the CB products are done
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + p.off_bar + kNumBars * 8);
 
@@ -165,7 +195,9 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::mbar_init(&bars[kBarYDone + i], 1);
             tc::mbar_init(&bars[kBarYFree + i], wps);
         }
-        for (int i = 0; i < kMaxFill; ++i) tc::mbar_init(&bars[kBarFull + i], 1);
+        for (int i = 0; i < kMaxFill; ++i) tc::mbar_init(&bars[kBarFull + i], kFillArrivals);
+        // a stage is free once the MMAs have read it and the stream's warps have
+        // read x for the skip term
         for (int i = 0; i < kMaxStages; ++i) tc::mbar_init(&bars[kBarSlotFree + i], 1 + wps);
         ctl->abort = 0;
         tc::fence_barrier_init();
@@ -183,7 +215,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const uint32_t h_bytes = (uint32_t)S * H * 2;
 
     if (warp == 0) {
-        // =========================== TMA producer ===========================
+        // ============== TMA producer + per-head G / dt / D gather ==============
         if (lane == 0) {
             tc::tma_prefetch_desc(&tm_x);
             tc::tma_prefetch_desc(&tm_b);
@@ -196,18 +228,29 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tc::tma_load_4d(sB + kb * (Tj * 128) + rb * 16384, &tm_b, &bars[kBarCbFull], kb * 64, grp,
                                     (int)(t0 + 128 * rb), (int)b);
             }
-            bool ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);  // the B area is reused
-            for (int k = 0; ok && k < p.nhb; ++k) {
-                const int st = k % p.nst;
-                if (k >= p.nst && !tc::mbar_wait(&bars[kBarSlotFree + st], ((k / p.nst) - 1) & 1, abort_flag)) {
+        }
+        // the B area is reused by the stages
+        bool ok = true;
+        if (lane == 0) ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
+        ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+        for (int k = 0; ok && k < p.nhb; ++k) {
+            const int st = k % p.nst;
+            if (k >= p.nst) {
+                bool w_ok = true;
+                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], ((k / p.nst) - 1) & 1, abort_flag);
+                if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) {
                     ok = false;
                     break;
                 }
-                uint8_t* sX = sStage + st * p.stage_bytes;
-                uint8_t* sH = sX + p.off_h_in_stage;
-                uint64_t* full = &bars[kBarFull + k % p.nfill];
+            }
+            uint8_t* sX = sStage + st * p.stage_bytes;
+            uint8_t* sH = sX + p.off_h_in_stage;
+            float* vG = reinterpret_cast<float*>(sX + p.off_vec_in_stage);  // G[T], dt[T], D
+            float* vDt = vG + p.T;
+            uint64_t* full = &bars[kBarFull + k % p.nfill];
+            const int h = h0 + k;
+            if (lane == 0) {
                 tc::mbar_arrive_expect_tx(full, x_bytes + h_bytes);
-                const int h = h0 + k;
                 for (int cb = 0; cb < H / 64; ++cb) {
                     for (int rb = 0; rb < Tj / 128; ++rb)
                         tc::tma_load_4d(sX + cb * (Tj * 128) + rb * 16384, &tm_x, full, cb * 64, h,
@@ -216,8 +259,18 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                                     (int)(((b * g.nheads + h) * g.nchunks + c) * S));
                 }
             }
-            if (!ok) set_abort(ctl, p.status);
+            // G_j (past the last valid token: G of the last one) and dt_j (zero there)
+            const float* Gh = p.G + (b * g.nheads + h) * g.seqlen + t0;
+            const float* dth = p.dt + (b * g.seqlen + t0) * g.nheads + h;
+            for (int j = lane; j < Tj; j += 32) {
+                const int jv = j < tc ? j : tc - 1;
+                tc::cp_async4(vG + j, Gh + jv, 4);
+                tc::cp_async4(vDt + j, dth + (int64_t)jv * g.nheads, j < tc ? 4u : 0u);
+            }
+            if (lane == 0) tc::cp_async4(vDt + p.T, p.D ? p.D + h : p.dt, p.D ? 4u : 0u);
+            tc::cp_async_mbar_arrive_noinc(full);
         }
+        if (!ok && lane == 0) set_abort(ctl, p.status);
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
         if (lane == 0) {
@@ -242,7 +295,6 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 const int st = k % p.nst, s = k % nstr, n = k / nstr;
                 uint8_t* sX = sStage + st * p.stage_bytes;
                 const uint32_t aX = tc::smem_u32(sX), aH = tc::smem_u32(sX + p.off_h_in_stage);
-                const uint32_t aX0v = tc::smem_u32(smem + p.off_X0v + s * (128 * H * 2));
                 const uint32_t tz = tmem + col_z(s, H), ty2 = tz + H;
                 if (!tc::mbar_wait(&bars[kBarFull + k % p.nfill], (k / p.nfill) & 1, abort_flag)) { ok = false; break; }
                 if (n >= 1 && !tc::mbar_wait(&bars[kBarYFree + s], (n - 1) & 1, abort_flag)) { ok = false; break; }
@@ -255,10 +307,11 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tc::mma_bf16_ss(tz, da, db, id_y, k16 > 0);
                 }
                 if (I == 1) {
-                    // Z += CB_10 (v . X_0)   (A: CB_10 bf16, K-major over j; B: v . X_0, MN-major)
+                    // Z += CB_10 (v . X_0)   (A: CB_10 bf16, K-major over j; B: rows 0..127 of
+                    // the stage's X, scaled in place, MN-major)
                     for (int k16 = 0; k16 < 8; ++k16) {
                         const uint64_t da = tc::sdesc_sw128(aCB10 + (k16 >> 2) * 16384 + (k16 & 3) * 32, 16, 1024);
-                        const uint64_t db = tc::sdesc_sw128(aX0v + k16 * 2048, 16384, 1024);
+                        const uint64_t db = tc::sdesc_sw128(aX + k16 * 2048, Tj * 128, 1024);
                         tc::mma_bf16_ss(tz, da, db, id_y, 1);
                     }
                 }
@@ -282,44 +335,16 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         const int nparts = wps / 4;             // warps per quadrant within a stream
         const int part = (e % wps) >> 2;        // column part handled by this warp
         const int gpw = 4 / nparts;             // 32-column groups of P per warp
-        const int ncoly = H / nparts;           // output columns per thread
+        const int ncoly = H / nparts;           // output columns per thread (32)
         const int cpt = 8 * (H / 64) / nparts;  // 16-byte chunks per row per thread in the folds
         const int il = q * 32 + lane;           // row inside the block = TMEM lane
         const int i = 128 * I + il;             // row inside the chunk
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t tz = tmem + col_z(sid, H), ty2 = tz + H, tp = tmem + col_p(sid);
-        float* wv = reinterpret_cast<float*>(smem + p.off_small) + e * 192;  // per warp: 2 x (G, dt, v)
-        uint8_t* sX0v = smem + p.off_X0v + sid * (128 * H * 2);
-        bool ok = true;
+        float* wv = reinterpret_cast<float*>(smem + p.off_small) + e * 64;  // per warp: w of 2 column groups
+        const int rq = 128 * I + 32 * q - 1;   // the column before this quadrant (-1: before the chunk)
 
-        // Per-head scalars of this thread, fetched one head of the stream ahead.
-        struct Scalars {
-            float gcol[2], dtcol[2], grow, gx, dtx, g127, dh;
-        };
-        auto fetch = [&](int k, Scalars& o) {
-            const int h = h0 + k;
-            const float* Gh = p.G + (b * g.nheads + h) * g.seqlen + t0;
-            const float* dth = p.dt + (b * g.seqlen + t0) * g.nheads + h;
-            const int last = tc - 1;  // padding repeats the last G with dt = 0
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int jc = 128 * I + 32 * (part * gpw + (t < gpw ? t : 0)) + lane;
-                o.gcol[t] = Gh[jc < tc ? jc : last];
-                o.dtcol[t] = jc < tc ? dth[(int64_t)jc * g.nheads] : 0.f;
-            }
-            o.grow = Gh[i < tc ? i : last];
-            if (I == 1) {
-                o.gx = Gh[il];
-                o.dtx = dth[(int64_t)il * g.nheads];
-                o.g127 = Gh[127];
-            } else {
-                o.gx = o.dtx = o.g127 = 0.f;
-            }
-            o.dh = p.D ? p.D[h] : 0.f;
-        };
-        Scalars nxt;
-        if (sid < p.nhb) fetch(sid, nxt);
-        ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
+        bool ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
         tc::tc_fence_after();
         if (ok && I == 1) {
             // CB_10 (staged in TMEM) -> bf16 [128 rows i x 128 columns j], K-major, 128B swizzle
@@ -345,126 +370,162 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[kBarCb10Ready]);
         }
+        if (ok && e < 4) {
+            // Causal mask, once for every head: zero CB_II above the diagonal
+            // inside this quadrant's diagonal 32 x 32 group (the groups right
+            // of it are never read).
+            uint32_t ra[16], rb[16];
+            tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * q, ra);
+            tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * q + 16, rb);
+            tc::tmem_wait_ld16(ra);
+            tc::tmem_wait_ld16(rb);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                if (x > lane) ra[x] = 0u;
+                if (16 + x > lane) rb[x] = 0u;
+            }
+            tc::tmem_st16(tmem + kColCB + lane_base + 32 * q, ra);
+            tc::tmem_st16(tmem + kColCB + lane_base + 32 * q + 16, rb);
+            tc::tmem_wait_st();
+        }
+        // Every epilogue warp sees the masked CB before it forms P.
+        tc::tc_fence_before();
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        tc::tc_fence_after();
 
         for (int k = sid; ok && k < p.nhb; k += nstr) {
-            const int h = h0 + k, st = k % p.nst, n = k / nstr;
-            const Scalars cur = nxt;
-            if (k + nstr < p.nhb) fetch(k + nstr, nxt);
-            // this warp's column vectors: G_j, dt_j, v_j = exp2(G_r - G_j) dt_j (r = group's last column)
-            float g_r[2];
-            __syncwarp();
+            const int st = k % p.nst, n = k / nstr;
+            if (!tc::mbar_wait(&bars[kBarFull + k % p.nfill], (k / p.nfill) & 1, abort_flag)) { ok = false; break; }
+            uint8_t* sX = sStage + st * p.stage_bytes;
+            const float* vG = reinterpret_cast<const float*>(sX + p.off_vec_in_stage);
+            const float* vDt = vG + p.T;
+            const float grow = vG[i];
+            const float gref = rq < 0 ? 0.f : vG[rq];
+
+            // Decays of this quadrant's rows split at r = rq (see the file
+            // comment).  mild: u_i >= 2^-kMildSpan, so w_j <= dt_j / u_i stays
+            // in range for every column the row uses.  The test reads only G_r
+            // and G_i, so a row's path never depends on later tokens; the
+            // warp-wide fast loop gives mild rows the same products as the
+            // mixed loop.
+            const bool mild = gref - grow <= kMildSpan;  // false for NaN
+            const bool all_mild = __all_sync(0xffffffffu, mild);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (t >= gpw) break;
-                g_r[t] = __shfl_sync(0xffffffffu, cur.gcol[t], 31);
-                wv[96 * t + lane] = cur.gcol[t];
-                wv[96 * t + 32 + lane] = cur.dtcol[t];
-                wv[96 * t + 64 + lane] = exp2f(g_r[t] - cur.gcol[t]) * cur.dtcol[t];
+                const int gi = part * gpw + t;
+                if (gi > q) continue;
+                const int j = 128 * I + 32 * gi + lane;
+                const float wj = exp2f(fminf(gref - vG[j], kMildSpan)) * vDt[j];
+                wv[32 * t + lane] = wj > kWMax ? kWMax : wj;
             }
             __syncwarp();
-            if (!tc::mbar_wait(&bars[kBarFull + k % p.nfill], (k / p.nfill) & 1, abort_flag)) { ok = false; break; }
-            uint8_t* sX = sStage + st * p.stage_bytes;
 
             if (I == 1) {
-                // a h_c (in place) and v . X_0 (into this stream's buffer)
+                // a h_c and v . X_0, in place in the stage
                 uint8_t* sH = sX + p.off_h_in_stage;
-                const float a = exp2f(cur.g127);
-                for (int r = il; r < S; r += 128)
-                    scale_row_chunks(sH, sH, S * 128, S * 128, r, part * cpt, cpt, a);
-                const float vj = exp2f(cur.g127 - cur.gx) * cur.dtx;
-                scale_row_chunks(sX, sX0v, Tj * 128, 16384, il, part * cpt, cpt, vj);
+                const float g127 = vG[127];
+                const float a = exp2f(g127);
+                for (int r = il; r < S; r += 128) scale_row_chunks(sH, S * 128, r, part * cpt, cpt, a);
+                const float vj = exp2f(g127 - vG[il]) * vDt[il];
+                scale_row_chunks(sX, Tj * 128, il, part * cpt, cpt, vj);
                 tc::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&bars[kBarOpsReady + sid]);
             }
 
-            // ---- P on the diagonal block -> TMEM as bf16
+            // ---- P on the diagonal block -> TMEM as bf16 (CB is masked already),
+            // 16 columns at a time
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (t >= gpw) break;
                 const int gi = part * gpw + t;  // 32-column group 0..3 of the diagonal block
-                const float* w = wv + 96 * t;
-                uint32_t pk[16];
-                if (gi > q) {
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) pk[x] = 0u;
-                } else {
-                    uint32_t ra[16], rb[16];
-                    tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi, ra);
-                    tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi + 16, rb);
-                    tc::tmem_wait_ld16(ra);
-                    tc::tmem_wait_ld16(rb);
-                    if (gi < q) {
-                        const float u = exp2f(cur.grow - g_r[t]);
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t col = 32 * gi + 16 * hh;  // first column of this piece
+                    const float* w = wv + 32 * t + 16 * hh;
+                    const float* gj = vG + 128 * I + col;
+                    const float* dj = vDt + 128 * I + col;
+                    uint32_t pk[8];
+                    if (gi > q) {
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 v4 = *reinterpret_cast<const float4*>(w + 64 + 4 * e4);
-                            const uint32_t* r = (e4 < 4) ? ra : rb;
-                            const int o = 4 * (e4 & 3);
-                            pk[2 * e4] = tc::pack_bf16x2(__uint_as_float(r[o]) * u * v4.x,
-                                                         __uint_as_float(r[o + 1]) * u * v4.y);
-                            pk[2 * e4 + 1] = tc::pack_bf16x2(__uint_as_float(r[o + 2]) * u * v4.z,
-                                                             __uint_as_float(r[o + 3]) * u * v4.w);
-                        }
+                        for (int x = 0; x < 8; ++x) pk[x] = 0u;
                     } else {
+                        uint32_t r[16];
+                        tc::tmem_ld16_nowait(tmem + kColCB + lane_base + col, r);
+                        tc::tmem_wait_ld16(r);
+                        if (all_mild) {
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 g4 = *reinterpret_cast<const float4*>(w + 4 * e4);
-                            const float4 d4 = *reinterpret_cast<const float4*>(w + 32 + 4 * e4);
-                            const uint32_t* r = (e4 < 4) ? ra : rb;
-                            const int o = 4 * (e4 & 3), x = 4 * e4;  // column offset inside the group
-                            const float a0 = (x <= lane) ? __uint_as_float(r[o]) * exp2f(cur.grow - g4.x) * d4.x : 0.f;
-                            const float a1 = (x + 1 <= lane) ? __uint_as_float(r[o + 1]) * exp2f(cur.grow - g4.y) * d4.y : 0.f;
-                            const float a2 = (x + 2 <= lane) ? __uint_as_float(r[o + 2]) * exp2f(cur.grow - g4.z) * d4.z : 0.f;
-                            const float a3 = (x + 3 <= lane) ? __uint_as_float(r[o + 3]) * exp2f(cur.grow - g4.w) * d4.w : 0.f;
-                            pk[2 * e4] = tc::pack_bf16x2(a0, a1);
-                            pk[2 * e4 + 1] = tc::pack_bf16x2(a2, a3);
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                const float4 v4 = *reinterpret_cast<const float4*>(w + 4 * e4);
+                                const int o = 4 * e4;
+                                const float2 p0 = tc::mul_f32x2(
+                                    make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1])), make_float2(v4.x, v4.y));
+                                const float2 p1 = tc::mul_f32x2(
+                                    make_float2(__uint_as_float(r[o + 2]), __uint_as_float(r[o + 3])), make_float2(v4.z, v4.w));
+                                pk[2 * e4] = tc::pack_bf16x2(p0.x, p0.y);
+                                pk[2 * e4 + 1] = tc::pack_bf16x2(p1.x, p1.y);
+                            }
+                        } else {
+                            // per row: the split weight (mild rows, the same products
+                            // as above) or the direct one
+#pragma unroll
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                const float4 v4 = *reinterpret_cast<const float4*>(w + 4 * e4);
+                                const float4 g4 = *reinterpret_cast<const float4*>(gj + 4 * e4);
+                                const float4 d4 = *reinterpret_cast<const float4*>(dj + 4 * e4);
+                                const int o = 4 * e4;
+                                const float f0 = mild ? v4.x : exact_weight(grow, g4.x, d4.x);
+                                const float f1 = mild ? v4.y : exact_weight(grow, g4.y, d4.y);
+                                const float f2 = mild ? v4.z : exact_weight(grow, g4.z, d4.z);
+                                const float f3 = mild ? v4.w : exact_weight(grow, g4.w, d4.w);
+                                pk[2 * e4] = tc::pack_bf16x2(__uint_as_float(r[o]) * f0, __uint_as_float(r[o + 1]) * f1);
+                                pk[2 * e4 + 1] =
+                                    tc::pack_bf16x2(__uint_as_float(r[o + 2]) * f2, __uint_as_float(r[o + 3]) * f3);
+                            }
                         }
                     }
+                    tc::tmem_st8(tp + lane_base + col / 2, pk);
                 }
-                tc::tmem_st16(tp + lane_base + 16 * gi, pk);
             }
             tc::tmem_wait_st();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[kBarPReady + sid]);
 
-            // ---- y = exp2(G_i - G_ref) Z + Y2 + D x
+            // ---- y = exp2(G_i - G_ref) Z + u_i Y2 + D x_i   (G_ref = G_127 for I = 1, else 0)
+            const float si = exp2f(grow - (I == 1 ? vG[127] : 0.f));
+            const float ui = mild ? exp2f(grow - gref) : 1.f;
+            const float dh = vDt[p.T];
+            const float2 si2 = make_float2(si, si), ui2 = make_float2(ui, ui), d2 = make_float2(dh, dh);
+            __nv_bfloat16* yrow = p.y + ((b * g.seqlen + t0 + i) * g.nheads + (h0 + k)) * H;
+            const uint8_t* xrow = sX + i * 128;
             if (!tc::mbar_wait(&bars[kBarYDone + sid], n & 1, abort_flag)) { ok = false; break; }
             tc::tc_fence_after();
-            const float si = exp2f(cur.grow - cur.g127);  // g127 = 0 for I = 0
-            __nv_bfloat16* yrow = p.y + ((b * g.seqlen + t0 + i) * g.nheads + h) * H;
-            for (int m = 0; m < ncoly / 16; ++m) {
-                const int kk = part * ncoly + 16 * m;
-                float acc[16];
-                {
-                    uint32_t ya[16], yb[16];
-                    tc::tmem_ld16_nowait(tz + lane_base + kk, ya);
-                    tc::tmem_ld16_nowait(ty2 + lane_base + kk, yb);
-                    tc::tmem_wait_ld16(ya);
-                    tc::tmem_wait_ld16(yb);
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) acc[x] = fmaf(si, __uint_as_float(ya[x]), __uint_as_float(yb[x]));
-                }
-                const uint8_t* xrow = sX + (kk >> 6) * (Tj * 128) + i * 128;
-                const int lc0 = (kk & 63) >> 3;
-                uint32_t out[8];
+            for (int m = 0; m < 4; ++m) {
+                if (m >= ncoly / 8) break;
+                const int kk = part * ncoly + 8 * m;
+                uint32_t za[8], yb[8];
+                tc::tmem_ld8_nowait(tz + lane_base + kk, za);
+                tc::tmem_ld8_nowait(ty2 + lane_base + kk, yb);
+                const uint4 xv = *reinterpret_cast<const uint4*>(xrow + (kk >> 6) * (Tj * 128) +
+                                                                 ((((kk & 63) >> 3) ^ (i & 7)) << 4));
+                tc::tmem_wait_ld8(za);
+                tc::tmem_wait_ld8(yb);
+                // y = si Z + ui Y2 + D x, in fp32, rounded once to bf16
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                uint32_t yw[4];
 #pragma unroll
-                for (int s2 = 0; s2 < 2; ++s2) {
-                    const uint4 xv = *reinterpret_cast<const uint4*>(xrow + (((lc0 + s2) ^ (i & 7)) << 4));
-                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int ci = s2 * 8 + 2 * x;
-                        out[s2 * 4 + x] = tc::pack_bf16x2(fmaf(cur.dh, tc::bf16_lo(xw[x]), acc[ci]),
-                                                          fmaf(cur.dh, tc::bf16_hi(xw[x]), acc[ci + 1]));
-                    }
+                for (int x = 0; x < 4; ++x) {
+                    const float2 t2 = tc::fma_f32x2(d2, make_float2(tc::bf16_lo(xw[x]), tc::bf16_hi(xw[x])),
+                                                    tc::mul_f32x2(ui2, make_float2(__uint_as_float(yb[2 * x]),
+                                                                                   __uint_as_float(yb[2 * x + 1]))));
+                    const float2 a2 =
+                        tc::fma_f32x2(si2, make_float2(__uint_as_float(za[2 * x]), __uint_as_float(za[2 * x + 1])), t2);
+                    yw[x] = tc::pack_bf16x2(a2.x, a2.y);
                 }
-                if (i < tc) {
-                    uint4* dst = reinterpret_cast<uint4*>(yrow + kk);
-                    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-                    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
-                }
+                if (i < tc) *reinterpret_cast<uint4*>(yrow + kk) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
             }
             tc::tc_fence_before();
             __syncwarp();
@@ -491,28 +552,37 @@ int pick_heads_per_cta(const Geom& g) {
     return 1;
 }
 
+int lcm_small(int a, int b) {
+    int m = a;
+    while (m % b != 0) m += a;
+    return m;
+}
+
 bool plan_smem(const Geom& g, CoTcParams& p) {
     const int T = (int)g.chunk, S = (int)g.dstate, H = (int)g.headdim;
     p.nstr = (H == 64) ? 2 : 1;
     p.off_C = 0;
     p.off_CB10 = p.off_C + 128 * S * 2;
-    p.off_X0v = p.off_CB10 + (T == 256 ? 32768 : 0);
-    p.off_stage = p.off_X0v + (T == 256 ? p.nstr * 128 * H * 2 : 0);
+    p.off_stage = p.off_CB10 + (T == 256 ? 32768 : 0);
     p.off_h_in_stage = T * H * 2;
-    p.stage_bytes = T * H * 2 + S * H * 2;
+    p.off_vec_in_stage = p.off_h_in_stage + S * H * 2;
+    const uint32_t vec_bytes = (uint32_t)(2 * T + 4) * 4;
+    p.stage_bytes = (p.off_vec_in_stage + vec_bytes + 1023) / 1024 * 1024;  // swizzled tiles: 1024-aligned
     for (int nst = kMaxStages; nst >= 1; --nst) {
+        // B (for the CB products) overlays CB_10, the stages and, if it is
+        // longer, the per-warp area: all are written only after CB is done.
         const uint32_t stages_end = p.off_stage + nst * p.stage_bytes;
-        if (stages_end - p.off_CB10 < (uint32_t)(T * S * 2)) continue;  // B must fit until CB is done
-        const uint32_t off_small = stages_end;
-        const uint32_t off_bar = off_small + kEpiWarps * 192 * 4;
+        const uint32_t b_end = p.off_CB10 + (uint32_t)(T * S * 2);
+        const uint32_t off_small = stages_end > b_end ? stages_end : b_end;
+        const uint32_t off_bar = off_small + kEpiWarps * 64 * 4;
         const uint32_t total = off_bar + kNumBars * 8 + 64 + 1024;  // + ctl + alignment slack
         if (total <= (uint32_t)kSmemLimit) {
             p.nst = nst;
-            p.nfill = nst > p.nstr ? nst : p.nstr;
+            p.nfill = lcm_small(nst, p.nstr);
             p.off_small = off_small;
             p.off_bar = off_bar;
             p.smem_bytes = total;
-            return true;
+            return p.nfill <= kMaxFill;
         }
     }
     return false;
