@@ -9,7 +9,8 @@
 // GB300 mapping: one CTA per (chunk, block of 32 heads, batch).  dt rows of 32
 // heads (128 B) are read coalesced into shared memory, each warp scans whole
 // heads (per-lane serial prefix + warp-shuffle scan of the lane totals), and
-// the tile is written back transposed, coalesced along t.  Pure streaming.
+// the tile is written back transposed, coalesced along t.  Pure streaming:
+// every thread issues all of its loads before it stores any of them.
 #include "common.cuh"
 
 namespace m2 {
@@ -30,44 +31,71 @@ k_chunk_cumsum(const float* __restrict__ dt, const float* __restrict__ A, float*
     const int tc = (int)imin64(g.chunk, g.seqlen - t0);  // valid tokens (ragged tail)
     const int nh_here = (int)imin64(kHeadsPerCta, g.nheads - h0);
 
-    // a_t = A[h] * dt[b, t, h], coalesced over heads.
-    for (int i = threadIdx.x; i < tc * kHeadsPerCta; i += kThreads) {
-        const int t = i / kHeadsPerCta, hh = i % kHeadsPerCta;
-        float v = 0.f;
-        if (hh < nh_here) v = A[h0 + hh] * dt[(b * g.seqlen + t0 + t) * g.nheads + h0 + hh];
-        tile[t][hh] = v;
+    // a_t = A[h] * dt[b, t, h], coalesced over heads.  Thread (r, hh) owns
+    // head column hh and rows r, r + 8, ...: all of its loads are issued
+    // before the first store, so their latencies overlap.
+    constexpr int kRowsPerPass = kThreads / kHeadsPerCta;       // 8
+    constexpr int kPasses = kMaxChunk / kRowsPerPass;           // 32
+    const int hh = threadIdx.x % kHeadsPerCta, r = threadIdx.x / kHeadsPerCta;
+    const bool hv = hh < nh_here;
+    const float a = hv ? A[h0 + hh] : 0.f;
+    const float* dcol = dt + (b * g.seqlen + t0) * g.nheads + h0 + hh;
+    float v[kPasses];
+#pragma unroll
+    for (int k = 0; k < kPasses; ++k) {
+        const int t = r + kRowsPerPass * k;
+        v[k] = (hv && t < tc) ? dcol[(int64_t)t * g.nheads] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kPasses; ++k) {
+        const int t = r + kRowsPerPass * k;
+        if (t < tc) tile[t][hh] = a * v[k];
     }
     __syncthreads();
 
-    // Inclusive scan along t, one warp per head.
+    // Inclusive scan along t.  Warp w scans heads w, w + 8, w + 16, w + 24
+    // together: per lane a serial prefix over its run of tokens, then a
+    // warp-shuffle scan of the lane totals.
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    constexpr int kHeadsPerWarp = kHeadsPerCta / (kThreads / 32);  // 4
     const int per_lane = (tc + 31) / 32;
-    for (int hh = warp; hh < nh_here; hh += kThreads / 32) {
-        const int lo = lane * per_lane;
-        const int hi = min(lo + per_lane, tc);
-        float run = 0.f;
-        for (int t = lo; t < hi; ++t) {
-            run += tile[t][hh];
-            tile[t][hh] = run;
+    const int lo = lane * per_lane;
+    const int hi = min(lo + per_lane, tc);
+    float run[kHeadsPerWarp];
+#pragma unroll
+    for (int u = 0; u < kHeadsPerWarp; ++u) run[u] = 0.f;
+    for (int t = lo; t < hi; ++t) {
+#pragma unroll
+        for (int u = 0; u < kHeadsPerWarp; ++u) {
+            run[u] += tile[t][warp + 8 * u];
+            tile[t][warp + 8 * u] = run[u];
         }
-        // exclusive prefix of the lane totals, formed from lower lanes only
-        // (never as inclusive - own), so G_t cannot depend on tokens after t
-        float incl = run;
+    }
+    // exclusive prefix of the lane totals, formed from lower lanes only
+    // (never as inclusive - own), so G_t cannot depend on tokens after t
+    float excl[kHeadsPerWarp];
+#pragma unroll
+    for (int u = 0; u < kHeadsPerWarp; ++u) {
+        float incl = run[u];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float n = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += n;
         }
-        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) excl = 0.f;
-        for (int t = lo; t < hi; ++t) tile[t][hh] = (tile[t][hh] + excl) * kLog2e;
+        excl[u] = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) excl[u] = 0.f;
+    }
+    for (int t = lo; t < hi; ++t) {
+#pragma unroll
+        for (int u = 0; u < kHeadsPerWarp; ++u)
+            tile[t][warp + 8 * u] = (tile[t][warp + 8 * u] + excl[u]) * kLog2e;
     }
     __syncthreads();
 
     // G[b, h, t0 + t], coalesced along t.
-    for (int hh = warp; hh < nh_here; hh += kThreads / 32) {
-        float* out = G + ((b * g.nheads) + h0 + hh) * g.seqlen + t0;
-        for (int t = lane; t < tc; t += 32) out[t] = tile[t][hh];
+    for (int hw = warp; hw < nh_here; hw += kThreads / 32) {
+        float* out = G + ((b * g.nheads) + h0 + hw) * g.seqlen + t0;
+        for (int t = lane; t < tc; t += 32) out[t] = tile[t][hw];
     }
 }
 

@@ -6,15 +6,16 @@
 // and walks the chunks in order:
 //   warp 0      producer: TMA of 64-token sub-blocks of B (the tile's 128
 //               state columns) and of X into a ring of shared-memory stages;
-//               its lanes also gather dt and G for the sub-block (loaded one
-//               sub-block ahead) and write the weights w_t and exp2(G_last)
-//               into the stage, so the other warps never touch global memory;
+//               its lanes also gather the sub-block's G_t and dt_t and the
+//               chunk's G_last into the stage with cp.async, so the other
+//               warps never wait on a global load;
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
 //               U_c = B_c^T (w . X_c) accumulated over the chunk's sub-blocks
 //               into one of two TMEM buffers (A = B_c^T and B = w . X_c are
 //               both read "MN-major" straight from the TMA layout);
-//   warps 2..9  fold the weights w_t into the X rows in shared memory (so the
-//               weighted operand is formed once, on chip), and run the scan:
+//   warps 2..9  form w_t = dt_t exp2(G_last - G_t) and fold it into the X rows
+//               in shared memory (so the weighted operand is formed once, on
+//               chip), and run the scan:
 //               the state h lives in TMEM next to U; per chunk each thread
 //               (one state row, half of the columns) stores h_c, then sets
 //               h <- exp2(G_last) h + U_c.
@@ -53,8 +54,7 @@ enum : int {
     kBarFull = 4,      // [kMaxStages]
     kBarXform = 4 + kMaxStages,
     kBarSlotFree = 4 + 2 * kMaxStages,
-    kBarWReady = 4 + 3 * kMaxStages,
-    kNumBars = 4 + 4 * kMaxStages
+    kNumBars = 4 + 3 * kMaxStages
 };
 
 struct SharedCtl {
@@ -91,10 +91,9 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tc::mbar_init(&bars[kBarUFree + i], kWorkWarps);
         }
         for (int i = 0; i < kMaxStages; ++i) {
-            tc::mbar_init(&bars[kBarFull + i], 1);
+            tc::mbar_init(&bars[kBarFull + i], 1 + 32);  // expect-tx + one cp.async arrival per lane
             tc::mbar_init(&bars[kBarXform + i], kWorkWarps);
             tc::mbar_init(&bars[kBarSlotFree + i], 1);
-            tc::mbar_init(&bars[kBarWReady + i], 1);
         }
         ctl->abort = 0;
         tc::fence_barrier_init();
@@ -119,21 +118,6 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tc::tma_prefetch_desc(&tm_b);
         }
         const float* Gbh = p.G + bh * g.seqlen;
-        // raw inputs of one sub-block for this lane's two tokens (lane, lane + 32)
-        float rg[2], rdt[2], rlast;
-        auto gather = [&](int u) {
-            const int c = u / p.nsb, sb = u % p.nsb;
-            const int64_t t0 = c * g.chunk;
-            const int tc = (int)imin64(g.chunk, g.seqlen - t0);
-            rlast = Gbh[t0 + tc - 1];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int tl = sb * kKb + lane + 32 * r;
-                rg[r] = Gbh[t0 + (tl < tc ? tl : tc - 1)];
-                rdt[r] = (tl < tc) ? p.dt[(b * g.seqlen + t0 + tl) * g.nheads + h] : 0.f;
-            }
-        };
-        gather(0);
         bool ok = true;
         for (int u = 0; u < nsub; ++u) {
             const int st = u % p.nst;
@@ -143,10 +127,12 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) { ok = false; break; }
             }
             const int c = u / p.nsb, sb = u % p.nsb;
-            const int tok = (int)(c * g.chunk + sb * kKb);
+            const int64_t t0 = c * g.chunk;
+            const int tc = (int)imin64(g.chunk, g.seqlen - t0);
+            const int tok = (int)(t0 + sb * kKb);
             uint8_t* sB = smem + st * p.stage_bytes;
             uint8_t* sX = sB + p.off_x_in_stage;
-            float* sW = reinterpret_cast<float*>(sB + p.off_w_in_stage);  // w[64], then exp2(G_last)
+            float* sV = reinterpret_cast<float*>(sB + p.off_w_in_stage);  // G[64], dt[64], G_last
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(&bars[kBarFull + st], (2 + H / 64) * x_box_bytes);
                 for (int kb = 0; kb < 2; ++kb)
@@ -155,13 +141,20 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 for (int cb = 0; cb < H / 64; ++cb)
                     tc::tma_load_4d(sX + cb * x_box_bytes, &tm_x, &bars[kBarFull + st], cb * 64, h, tok, (int)b);
             }
-            // w_t = dt_t exp2(G_last - G_t) for the sub-block, from the gathered values
+            // G_t and dt_t of the sub-block's tokens (past the last valid token:
+            // G of the last one and dt = 0) and G_last of the chunk, gathered
+            // straight into the stage; each lane arrives on the stage barrier
+            // once its copies have landed.
 #pragma unroll
-            for (int r = 0; r < 2; ++r) sW[lane + 32 * r] = rdt[r] * exp2f(rlast - rg[r]);
-            if (lane == 0) sW[64] = exp2f(rlast);
-            if (u + 1 < nsub) gather(u + 1);  // in flight while the stage fills
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[kBarWReady + st]);
+            for (int r = 0; r < 2; ++r) {
+                const int tl = sb * kKb + lane + 32 * r;
+                const int tv = tl < tc ? tl : tc - 1;
+                tc::cp_async4(sV + lane + 32 * r, Gbh + t0 + tv, 4);
+                tc::cp_async4(sV + 64 + lane + 32 * r, p.dt + (b * g.seqlen + t0 + tv) * g.nheads + h,
+                              tl < tc ? 4u : 0u);
+            }
+            if (lane == 0) tc::cp_async4(sV + 128, Gbh + t0 + tc - 1, 4);
+            tc::cp_async_mbar_arrive_noinc(&bars[kBarFull + st]);
         }
         if (!ok && lane == 0) set_abort(ctl, p.status);
     } else if (warp == 1) {
@@ -224,14 +217,14 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         float alpha_even = 1.f, alpha_odd = 1.f;  // exp2(G_last) of the two chunks in flight
         auto fold = [&](int u) -> bool {
             const int st = u % p.nst;
-            if (!tc::mbar_wait(&bars[kBarWReady + st], (u / p.nst) & 1, abort_flag)) return false;
-            const float* sW = reinterpret_cast<const float*>(smem + st * p.stage_bytes + p.off_w_in_stage);
-            const float w = sW[frow];
-            if (u % p.nsb == 0) {
-                if ((u / p.nsb) & 1) alpha_odd = sW[64];
-                else alpha_even = sW[64];
-            }
             if (!tc::mbar_wait(&bars[kBarFull + st], (u / p.nst) & 1, abort_flag)) return false;
+            const float* sV = reinterpret_cast<const float*>(smem + st * p.stage_bytes + p.off_w_in_stage);
+            const float glast = sV[128];
+            const float w = sV[64 + frow] * exp2f(glast - sV[frow]);  // w_t = dt_t exp2(G_last - G_t)
+            if (u % p.nsb == 0) {
+                if ((u / p.nsb) & 1) alpha_odd = exp2f(glast);
+                else alpha_even = exp2f(glast);
+            }
             uint8_t* sX = smem + st * p.stage_bytes + p.off_x_in_stage;
             uint8_t* rowp = sX + frow * 128;
             uint4 v[4];
@@ -328,7 +321,7 @@ bool plan(const Geom& g, SpTcParams& p) {
     p.nsb = (int)(g.chunk / kKb);
     p.off_x_in_stage = 2 * kKb * 128;
     p.off_w_in_stage = p.off_x_in_stage + (H / 64) * kKb * 128;
-    p.stage_bytes = p.off_w_in_stage + 1024;  // w[64] and exp2(G_last), padded to keep stages 1 KB aligned
+    p.stage_bytes = p.off_w_in_stage + 1024;  // G[64], dt[64], G_last; padded to keep stages 1 KB aligned
     p.tmem_cols = (3 * H <= 256) ? 256 : 512;
     // two CTAs per SM when TMEM allows, else one with a deeper ring
     const uint32_t budget = (p.tmem_cols == 256) ? (kSmemLimit / 2 - 2048) : kSmemLimit;
