@@ -29,8 +29,9 @@
 namespace m2 {
 namespace {
 
-constexpr int kWorkWarps = 8;
-constexpr int kThreads = (2 + kWorkWarps) * 32;
+constexpr int kFoldWarps = 4;  // warps 2..5
+constexpr int kScanWarps = 4;  // warps 6..9, one per TMEM lane quadrant
+constexpr int kThreads = (2 + kFoldWarps + kScanWarps) * 32;
 constexpr int kKb = 64;  // tokens per sub-block
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;
@@ -88,11 +89,11 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&bars[kBarUDone + i], 1);
-            tc::mbar_init(&bars[kBarUFree + i], kWorkWarps);
+            tc::mbar_init(&bars[kBarUFree + i], kScanWarps);
         }
         for (int i = 0; i < kMaxStages; ++i) {
             tc::mbar_init(&bars[kBarFull + i], 1 + 32);  // expect-tx + one cp.async arrival per lane
-            tc::mbar_init(&bars[kBarXform + i], kWorkWarps);
+            tc::mbar_init(&bars[kBarXform + i], kFoldWarps);
             tc::mbar_init(&bars[kBarSlotFree + i], 1);
         }
         ctl->abort = 0;
@@ -188,121 +189,114 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!ok) set_abort(ctl, p.status);
         }
     } else {
-        // ================= weight fold + scan (warps 2..9) =================
-        const int ew = warp - 2;                 // 0..7
-        const int et = ew * 32 + lane;           // 0..255
-        const int q = warp & 3;                  // TMEM lane quadrant
-        const int half = ew >> 2;                // column half of the state handled by this warp
-        const int s_local = q * 32 + lane;
-        const int s = mt * 128 + s_local;
-        const bool valid = s < S;
-        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        const int hcols = H / 2;                 // state columns per thread
-        const int col0 = half * hcols;
-
-        // h <- initial state (or zeros), kept in TMEM columns [2H, 3H)
-        for (int m = 0; m < hcols / 16; ++m) {
-            uint32_t r[16];
+        bool ok = true;
+        if (warp < 2 + kFoldWarps) {
+            // ================= weight fold (warps 2..5) =================
+            // Two threads per token row of a 64-token sub-block, each taking
+            // half of the row's 16-byte chunks (rotated to spread banks).
+            const int ft = (warp - 2) * 32 + lane;  // 0..127
+            const int frow = ft >> 1, fh = ft & 1;
+            const int per = 4 * (H / 64);           // chunks per thread (4 or 8)
+            for (int u = 0; ok && u < nsub; ++u) {
+                const int st = u % p.nst;
+                if (!tc::mbar_wait(&bars[kBarFull + st], (u / p.nst) & 1, abort_flag)) { ok = false; break; }
+                const float* sV = reinterpret_cast<const float*>(smem + st * p.stage_bytes + p.off_w_in_stage);
+                const float w = sV[64 + frow] * exp2f(sV[128] - sV[frow]);  // w_t = dt_t exp2(G_last - G_t)
+                uint8_t* rowp = smem + st * p.stage_bytes + p.off_x_in_stage + frow * 128;
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                r[e] = __float_as_uint((valid && p.init) ? p.init[(bh * S + s) * H + col0 + 16 * m + e] : 0.f);
-            tc::tmem_st16(tm_h + lane_base + col0 + 16 * m, r);
-        }
-        tc::tmem_wait_st();
-
-        // Fold mapping: four threads per token row of a 64-token sub-block, each
-        // taking a quarter of the row's 16-byte chunks (rotated to spread banks).
-        const int frow = et >> 2, fq = et & 3;
-        const int per = 2 * (H / 64);  // chunks per thread (2 or 4)
-        float alpha_even = 1.f, alpha_odd = 1.f;  // exp2(G_last) of the two chunks in flight
-        auto fold = [&](int u) -> bool {
-            const int st = u % p.nst;
-            if (!tc::mbar_wait(&bars[kBarFull + st], (u / p.nst) & 1, abort_flag)) return false;
-            const float* sV = reinterpret_cast<const float*>(smem + st * p.stage_bytes + p.off_w_in_stage);
-            const float glast = sV[128];
-            const float w = sV[64 + frow] * exp2f(glast - sV[frow]);  // w_t = dt_t exp2(G_last - G_t)
-            if (u % p.nsb == 0) {
-                if ((u / p.nsb) & 1) alpha_odd = exp2f(glast);
-                else alpha_even = exp2f(glast);
-            }
-            uint8_t* sX = smem + st * p.stage_bytes + p.off_x_in_stage;
-            uint8_t* rowp = sX + frow * 128;
-            uint4 v[4];
+                for (int f0 = 0; f0 < 8; f0 += 2) {  // two chunks in flight
+                    if (f0 >= per) break;
+                    uint4 v[2];
 #pragma unroll
-            for (int f = 0; f < 4; ++f) {
-                if (f >= per) break;
-                const int flat = fq * per + f;                  // 0 .. 8 (H/64) - 1
-                v[f] = *reinterpret_cast<const uint4*>(rowp + (flat >> 3) * x_box_bytes +
-                                                       ((((flat & 7) + frow) & 7) << 4));
-            }
+                    for (int f = 0; f < 2; ++f) {
+                        const int flat = fh * per + f0 + f;  // 0 .. 8 (H/64) - 1
+                        v[f] = *reinterpret_cast<const uint4*>(rowp + (flat >> 3) * x_box_bytes +
+                                                               ((((flat & 7) + frow) & 7) << 4));
+                    }
 #pragma unroll
-            for (int f = 0; f < 4; ++f) {
-                if (f >= per) break;
-                const int flat = fq * per + f;
-                uint4 a = v[f];
-                a.x = tc::pack_bf16x2(tc::bf16_lo(a.x) * w, tc::bf16_hi(a.x) * w);
-                a.y = tc::pack_bf16x2(tc::bf16_lo(a.y) * w, tc::bf16_hi(a.y) * w);
-                a.z = tc::pack_bf16x2(tc::bf16_lo(a.z) * w, tc::bf16_hi(a.z) * w);
-                a.w = tc::pack_bf16x2(tc::bf16_lo(a.w) * w, tc::bf16_hi(a.w) * w);
-                *reinterpret_cast<uint4*>(rowp + (flat >> 3) * x_box_bytes + ((((flat & 7) + frow) & 7) << 4)) = a;
-            }
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[kBarXform + st]);
-            return true;
-        };
-
-        // Store h_c, then h <- exp2(G_last) h + U_c.
-        auto scan = [&](int c) -> bool {
-            const int ub = c & 1;
-            const float alpha = (c & 1) ? alpha_odd : alpha_even;
-            if (!tc::mbar_wait(&bars[kBarUDone + ub], (c >> 1) & 1, abort_flag)) return false;
-            tc::tc_fence_after();
-            __nv_bfloat16* dst = p.chunk_states + ((bh * g.nchunks + c) * S + s) * H + col0;
-            for (int m = 0; m < hcols / 16; ++m) {
-                uint32_t hv[16], uv[16];
-                tc::tmem_ld16(tm_h + lane_base + col0 + 16 * m, hv);
-                tc::tmem_ld16(tm_u0 + ub * H + lane_base + col0 + 16 * m, uv);
-                if (valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * m);
-#pragma unroll
-                    for (int s4 = 0; s4 < 2; ++s4) {
-                        const int e = 8 * s4;
-                        d4[s4] = make_uint4(
-                            tc::pack_bf16x2(__uint_as_float(hv[e]), __uint_as_float(hv[e + 1])),
-                            tc::pack_bf16x2(__uint_as_float(hv[e + 2]), __uint_as_float(hv[e + 3])),
-                            tc::pack_bf16x2(__uint_as_float(hv[e + 4]), __uint_as_float(hv[e + 5])),
-                            tc::pack_bf16x2(__uint_as_float(hv[e + 6]), __uint_as_float(hv[e + 7])));
+                    for (int f = 0; f < 2; ++f) {
+                        const int flat = fh * per + f0 + f;
+                        uint4 a = v[f];
+                        a.x = tc::pack_bf16x2(tc::bf16_lo(a.x) * w, tc::bf16_hi(a.x) * w);
+                        a.y = tc::pack_bf16x2(tc::bf16_lo(a.y) * w, tc::bf16_hi(a.y) * w);
+                        a.z = tc::pack_bf16x2(tc::bf16_lo(a.z) * w, tc::bf16_hi(a.z) * w);
+                        a.w = tc::pack_bf16x2(tc::bf16_lo(a.w) * w, tc::bf16_hi(a.w) * w);
+                        *reinterpret_cast<uint4*>(rowp + (flat >> 3) * x_box_bytes +
+                                                  ((((flat & 7) + frow) & 7) << 4)) = a;
                     }
                 }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[kBarXform + st]);
+            }
+        } else {
+            // ============ scan (warps 6..9): one state row per thread ============
+            const int q = warp & 3;  // TMEM lane quadrant
+            const int s = mt * 128 + q * 32 + lane;
+            const bool valid = s < S;
+            const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+            const float* Gbh = p.G + bh * g.seqlen;
+            auto glast_of = [&](int c) -> float {
+                const int64_t t0 = (int64_t)c * g.chunk;
+                return Gbh[t0 + imin64(g.chunk, g.seqlen - t0) - 1];
+            };
+            // h <- initial state (or zeros)
+            for (int m = 0; m < H / 16; ++m) {
+                uint32_t r[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
-                tc::tmem_st16(tm_h + lane_base + col0 + 16 * m, hv);
+                    r[e] = __float_as_uint((valid && p.init) ? p.init[(bh * S + s) * H + 16 * m + e] : 0.f);
+                tc::tmem_st16(tm_h + lane_base + 16 * m, r);
             }
             tc::tmem_wait_st();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[kBarUFree + ub]);
-            return true;
-        };
-
-        bool ok = true;
-        for (int sb = 0; ok && sb < p.nsb; ++sb) ok = fold(sb);
-        for (int c = 0; ok && c < (int)g.nchunks; ++c) {
-            if (c + 1 < (int)g.nchunks)
-                for (int sb = 0; ok && sb < p.nsb; ++sb) ok = fold((c + 1) * p.nsb + sb);
-            if (ok) ok = scan(c);
-        }
-        if (ok && p.final_state && valid) {
-            for (int m = 0; m < hcols / 16; ++m) {
-                uint32_t hv[16];
-                tc::tmem_ld16(tm_h + lane_base + col0 + 16 * m, hv);
-                float4* d4 = reinterpret_cast<float4*>(p.final_state + (bh * S + s) * H + col0 + 16 * m);
+            // Store h_c, then h <- exp2(G_last) h + U_c; G_last of the next chunk
+            // is fetched while this one waits for its U.
+            float gl_next = glast_of(0);
+            for (int c = 0; ok && c < (int)g.nchunks; ++c) {
+                const int ub = c & 1;
+                const float alpha = exp2f(gl_next);
+                if (c + 1 < (int)g.nchunks) gl_next = glast_of(c + 1);
+                if (!tc::mbar_wait(&bars[kBarUDone + ub], (c >> 1) & 1, abort_flag)) { ok = false; break; }
+                tc::tc_fence_after();
+                __nv_bfloat16* dst = p.chunk_states + ((bh * g.nchunks + c) * S + s) * H;
+                for (int m = 0; m < H / 16; ++m) {
+                    uint32_t hv[16], uv[16];
+                    tc::tmem_ld16_nowait(tm_h + lane_base + 16 * m, hv);
+                    tc::tmem_ld16_nowait(tm_u0 + ub * H + lane_base + 16 * m, uv);
+                    tc::tmem_wait_ld16(hv);
+                    tc::tmem_wait_ld16(uv);
+                    if (valid) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * m);
 #pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4)
-                    d4[s4] = make_float4(__uint_as_float(hv[4 * s4]), __uint_as_float(hv[4 * s4 + 1]),
-                                         __uint_as_float(hv[4 * s4 + 2]), __uint_as_float(hv[4 * s4 + 3]));
+                        for (int s4 = 0; s4 < 2; ++s4) {
+                            const int e = 8 * s4;
+                            d4[s4] = make_uint4(
+                                tc::pack_bf16x2(__uint_as_float(hv[e]), __uint_as_float(hv[e + 1])),
+                                tc::pack_bf16x2(__uint_as_float(hv[e + 2]), __uint_as_float(hv[e + 3])),
+                                tc::pack_bf16x2(__uint_as_float(hv[e + 4]), __uint_as_float(hv[e + 5])),
+                                tc::pack_bf16x2(__uint_as_float(hv[e + 6]), __uint_as_float(hv[e + 7])));
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
+                    tc::tmem_st16(tm_h + lane_base + 16 * m, hv);
+                }
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[kBarUFree + ub]);
+            }
+            if (ok && p.final_state && valid) {
+                for (int m = 0; m < H / 16; ++m) {
+                    uint32_t hv[16];
+                    tc::tmem_ld16(tm_h + lane_base + 16 * m, hv);
+                    float4* d4 = reinterpret_cast<float4*>(p.final_state + (bh * S + s) * H + 16 * m);
+#pragma unroll
+                    for (int s4 = 0; s4 < 4; ++s4)
+                        d4[s4] = make_float4(__uint_as_float(hv[4 * s4]), __uint_as_float(hv[4 * s4 + 1]),
+                                             __uint_as_float(hv[4 * s4 + 2]), __uint_as_float(hv[4 * s4 + 3]));
+                }
             }
         }
         if (!ok) set_abort(ctl, p.status);
