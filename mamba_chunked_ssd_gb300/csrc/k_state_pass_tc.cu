@@ -40,7 +40,7 @@ struct SpTcParams {
     Geom g;
     int nsb;            // sub-blocks per chunk = chunk / 64
     int nst;            // ring stages
-    uint32_t stage_bytes, off_x_in_stage, off_w_in_stage, off_bar, smem_bytes, tmem_cols;
+    uint32_t stage_bytes, off_x_in_stage, off_w_in_stage, off_stg, off_bar, smem_bytes, tmem_cols;
     const float* dt;
     const float* G;
     const float* init;
@@ -70,7 +70,7 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
 
 __global__ void __launch_bounds__(kThreads, 2)
 k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
-                const SpTcParams p) {
+                const __grid_constant__ CUtensorMap tm_cs, const SpTcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Geom& g = p.g;
@@ -250,43 +250,64 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             }
             tc::tmem_wait_st();
             // Store h_c, then h <- exp2(G_last) h + U_c; G_last of the next chunk
-            // is fetched while this one waits for its U.
+            // is fetched while this one waits for its U.  h_c leaves through a
+            // 64-row shared-memory tile (128-byte swizzle) and a TMA store: the
+            // warps of quadrants 0-1 fill it first, then those of quadrants 2-3.
+            uint8_t* stg = smem + p.off_stg;
+            const int hrow = (q & 1) * 32 + lane;  // row inside the 64-row tile
+            const bool leader = (q == 0 && lane == 0);
             float gl_next = glast_of(0);
-            for (int c = 0; ok && c < (int)g.nchunks; ++c) {
+            // Every scan warp runs every iteration and every named barrier below,
+            // whatever its own waits return, so no warp is left at a barrier;
+            // after a failed wait a warp only skips the work.
+            for (int c = 0; c < (int)g.nchunks; ++c) {
                 const int ub = c & 1;
                 const float alpha = exp2f(gl_next);
                 if (c + 1 < (int)g.nchunks) gl_next = glast_of(c + 1);
-                if (!tc::mbar_wait(&bars[kBarUDone + ub], (c >> 1) & 1, abort_flag)) { ok = false; break; }
+                if (ok) ok = tc::mbar_wait(&bars[kBarUDone + ub], (c >> 1) & 1, abort_flag);
                 tc::tc_fence_after();
-                __nv_bfloat16* dst = p.chunk_states + ((bh * g.nchunks + c) * S + s) * H;
-                for (int m = 0; m < H / 16; ++m) {
-                    uint32_t hv[16], uv[16];
-                    tc::tmem_ld16_nowait(tm_h + lane_base + 16 * m, hv);
-                    tc::tmem_ld16_nowait(tm_u0 + ub * H + lane_base + 16 * m, uv);
-                    tc::tmem_wait_ld16(hv);
-                    tc::tmem_wait_ld16(uv);
-                    if (valid) {
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * m);
+                const int64_t row0 = (bh * g.nchunks + c) * S + mt * 128;  // first state row of the tile
+                for (int half = 0; half < 2; ++half) {
+                    if (mt * 128 + 64 * half >= S) break;  // dstate = 64: one half only
+                    if (ok && (q >> 1) == half) {
+                        for (int m = 0; m < H / 16; ++m) {
+                            uint32_t hv[16], uv[16];
+                            tc::tmem_ld16_nowait(tm_h + lane_base + 16 * m, hv);
+                            tc::tmem_ld16_nowait(tm_u0 + ub * H + lane_base + 16 * m, uv);
+                            tc::tmem_wait_ld16(hv);
+                            tc::tmem_wait_ld16(uv);
+                            uint8_t* rowp = stg + (m >> 2) * 8192 + hrow * 128;
 #pragma unroll
-                        for (int s4 = 0; s4 < 2; ++s4) {
-                            const int e = 8 * s4;
-                            d4[s4] = make_uint4(
-                                tc::pack_bf16x2(__uint_as_float(hv[e]), __uint_as_float(hv[e + 1])),
-                                tc::pack_bf16x2(__uint_as_float(hv[e + 2]), __uint_as_float(hv[e + 3])),
-                                tc::pack_bf16x2(__uint_as_float(hv[e + 4]), __uint_as_float(hv[e + 5])),
-                                tc::pack_bf16x2(__uint_as_float(hv[e + 6]), __uint_as_float(hv[e + 7])));
+                            for (int s4 = 0; s4 < 2; ++s4) {
+                                const int e = 8 * s4, j = 2 * (m & 3) + s4;  // 16-byte chunk in the row
+                                *reinterpret_cast<uint4*>(rowp + ((j ^ (hrow & 7)) << 4)) = make_uint4(
+                                    tc::pack_bf16x2(__uint_as_float(hv[e]), __uint_as_float(hv[e + 1])),
+                                    tc::pack_bf16x2(__uint_as_float(hv[e + 2]), __uint_as_float(hv[e + 3])),
+                                    tc::pack_bf16x2(__uint_as_float(hv[e + 4]), __uint_as_float(hv[e + 5])),
+                                    tc::pack_bf16x2(__uint_as_float(hv[e + 6]), __uint_as_float(hv[e + 7])));
+                            }
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
+                            tc::tmem_st16(tm_h + lane_base + 16 * m, hv);
                         }
+                        tc::fence_proxy_async_smem();
                     }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
-                    tc::tmem_st16(tm_h + lane_base + 16 * m, hv);
+                    asm volatile("bar.sync 1, %0;" ::"r"(kScanWarps * 32) : "memory");
+                    if (leader && ok) {
+                        for (int cb = 0; cb < H / 64; ++cb)
+                            tc::tma_store_2d(&tm_cs, stg + cb * 8192, cb * 64, (int)(row0 + 64 * half));
+                        tc::bulk_commit();
+                        tc::bulk_wait_read_all();  // the tile may be refilled
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"r"(kScanWarps * 32) : "memory");
                 }
                 tc::tmem_wait_st();
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&bars[kBarUFree + ub]);
+                if (ok && lane == 0) tc::mbar_arrive(&bars[kBarUFree + ub]);
             }
+            if (leader) tc::bulk_wait_all();
             if (ok && p.final_state && valid) {
                 for (int m = 0; m < H / 16; ++m) {
                     uint32_t hv[16];
@@ -320,11 +341,13 @@ bool plan(const Geom& g, SpTcParams& p) {
     // two CTAs per SM when TMEM allows, else one with a deeper ring
     const uint32_t budget = (p.tmem_cols == 256) ? (kSmemLimit / 2 - 2048) : kSmemLimit;
     const uint32_t fixed = kNumBars * 8 + 64 + 1024;
-    int nst = (int)((budget - fixed) / p.stage_bytes);
+    const uint32_t stg_bytes = (uint32_t)(H / 64) * 8192;  // 64 rows x H bf16, boxes of 64 columns
+    int nst = (int)((budget - fixed - stg_bytes) / p.stage_bytes);
     if (nst > kMaxStages) nst = kMaxStages;
     if (nst < 2) return false;
     p.nst = nst;
-    p.off_bar = nst * p.stage_bytes;
+    p.off_stg = nst * p.stage_bytes;
+    p.off_bar = p.off_stg + stg_bytes;
     p.smem_bytes = p.off_bar + fixed;
     return true;
 }
@@ -364,12 +387,20 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
         const uint32_t box[4] = {64, 1, kKb, 1};
         if (!make_tmap_bf16(&tm_b, a.B, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
+    CUtensorMap tm_cs;
+    {
+        const uint64_t rows = (uint64_t)g.batch * nh * g.nchunks * S;
+        const uint64_t dims[2] = {H, rows};
+        const uint64_t strides[1] = {H * 2};
+        const uint32_t box[2] = {64, 64};
+        if (!make_tmap_bf16(&tm_cs, a.chunk_states, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaFuncSetAttribute(k_state_pass_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     const int mtiles = (int)((g.dstate + 127) / 128);
     dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)g.batch);
-    k_state_pass_tc<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, p);
+    k_state_pass_tc<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, tm_cs, p);
     return cudaGetLastError();
 }
 
