@@ -82,7 +82,6 @@ struct CoTcParams {
     const float* dt;
     const float* G;
     const float* D;
-    __nv_bfloat16* y;
     unsigned int* status;
 };
 
@@ -158,7 +157,7 @@ __device__ __forceinline__ void scale_row_chunks(uint8_t* base, uint32_t box_str
 __global__ void __launch_bounds__(kThreads, 1)
 k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_h,
-               const CoTcParams p) {
+               const __grid_constant__ CUtensorMap tm_y, const CoTcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Geom& g = p.g;
@@ -196,9 +195,9 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::mbar_init(&bars[kBarYFree + i], wps);
         }
         for (int i = 0; i < kMaxFill; ++i) tc::mbar_init(&bars[kBarFull + i], kFillArrivals);
-        // a stage is free once the MMAs have read it and the stream's warps have
-        // read x for the skip term
-        for (int i = 0; i < kMaxStages; ++i) tc::mbar_init(&bars[kBarSlotFree + i], 1 + wps);
+        // a stage is free once the MMAs have read it and the TMA store of y
+        // (written over X_I in the stage) has read it
+        for (int i = 0; i < kMaxStages; ++i) tc::mbar_init(&bars[kBarSlotFree + i], 2);
         ctl->abort = 0;
         tc::fence_barrier_init();
     }
@@ -393,10 +392,15 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
         tc::tc_fence_after();
 
-        for (int k = sid; ok && k < p.nhb; k += nstr) {
+        // Every warp of a stream runs every head of the stream and the stream's
+        // named barrier below, whatever its own waits return, so no warp is
+        // left at the barrier; after a failed wait a warp only skips the work.
+        const bool stream_leader = (e % wps == 0) && lane == 0;
+        for (int k = sid; k < p.nhb; k += nstr) {
             const int st = k % p.nst, n = k / nstr;
-            if (!tc::mbar_wait(&bars[kBarFull + k % p.nfill], (k / p.nfill) & 1, abort_flag)) { ok = false; break; }
+            if (ok) ok = tc::mbar_wait(&bars[kBarFull + k % p.nfill], (k / p.nfill) & 1, abort_flag);
             uint8_t* sX = sStage + st * p.stage_bytes;
+          if (ok) {
             const float* vG = reinterpret_cast<const float*>(sX + p.off_vec_in_stage);
             const float* vDt = vG + p.T;
             const float grow = vG[i];
@@ -493,47 +497,61 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[kBarPReady + sid]);
 
-            // ---- y = exp2(G_i - G_ref) Z + u_i Y2 + D x_i   (G_ref = G_127 for I = 1, else 0)
+            // ---- y = exp2(G_i - G_ref) Z + u_i Y2 + D x_i   (G_ref = G_127 for I = 1, else 0),
+            // written over x_i in the stage (each thread rewrites exactly the
+            // 16-byte pieces it reads; Y2, the last reader of X_I, is done)
             const float si = exp2f(grow - (I == 1 ? vG[127] : 0.f));
             const float ui = mild ? exp2f(grow - gref) : 1.f;
             const float dh = vDt[p.T];
             const float2 si2 = make_float2(si, si), ui2 = make_float2(ui, ui), d2 = make_float2(dh, dh);
-            __nv_bfloat16* yrow = p.y + ((b * g.seqlen + t0 + i) * g.nheads + (h0 + k)) * H;
-            const uint8_t* xrow = sX + i * 128;
-            if (!tc::mbar_wait(&bars[kBarYDone + sid], n & 1, abort_flag)) { ok = false; break; }
+            uint8_t* xrow = sX + i * 128;
+            ok = tc::mbar_wait(&bars[kBarYDone + sid], n & 1, abort_flag);
             tc::tc_fence_after();
+            if (ok) {
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (m >= ncoly / 8) break;
-                const int kk = part * ncoly + 8 * m;
-                uint32_t za[8], yb[8];
-                tc::tmem_ld8_nowait(tz + lane_base + kk, za);
-                tc::tmem_ld8_nowait(ty2 + lane_base + kk, yb);
-                const uint4 xv = *reinterpret_cast<const uint4*>(xrow + (kk >> 6) * (Tj * 128) +
-                                                                 ((((kk & 63) >> 3) ^ (i & 7)) << 4));
-                tc::tmem_wait_ld8(za);
-                tc::tmem_wait_ld8(yb);
-                // y = si Z + ui Y2 + D x, in fp32, rounded once to bf16
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                uint32_t yw[4];
+                for (int m = 0; m < 4; ++m) {
+                    if (m >= ncoly / 8) break;
+                    const int kk = part * ncoly + 8 * m;
+                    uint32_t za[8], yb[8];
+                    tc::tmem_ld8_nowait(tz + lane_base + kk, za);
+                    tc::tmem_ld8_nowait(ty2 + lane_base + kk, yb);
+                    uint4* px = reinterpret_cast<uint4*>(xrow + (kk >> 6) * (Tj * 128) +
+                                                         ((((kk & 63) >> 3) ^ (i & 7)) << 4));
+                    const uint4 xv = *px;
+                    tc::tmem_wait_ld8(za);
+                    tc::tmem_wait_ld8(yb);
+                    // y = si Z + ui Y2 + D x, in fp32, rounded once to bf16
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    uint32_t yw[4];
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const float2 t2 = tc::fma_f32x2(d2, make_float2(tc::bf16_lo(xw[x]), tc::bf16_hi(xw[x])),
-                                                    tc::mul_f32x2(ui2, make_float2(__uint_as_float(yb[2 * x]),
-                                                                                   __uint_as_float(yb[2 * x + 1]))));
-                    const float2 a2 =
-                        tc::fma_f32x2(si2, make_float2(__uint_as_float(za[2 * x]), __uint_as_float(za[2 * x + 1])), t2);
-                    yw[x] = tc::pack_bf16x2(a2.x, a2.y);
+                    for (int x = 0; x < 4; ++x) {
+                        const float2 t2 = tc::fma_f32x2(d2, make_float2(tc::bf16_lo(xw[x]), tc::bf16_hi(xw[x])),
+                                                        tc::mul_f32x2(ui2, make_float2(__uint_as_float(yb[2 * x]),
+                                                                                       __uint_as_float(yb[2 * x + 1]))));
+                        const float2 a2 = tc::fma_f32x2(
+                            si2, make_float2(__uint_as_float(za[2 * x]), __uint_as_float(za[2 * x + 1])), t2);
+                        yw[x] = tc::pack_bf16x2(a2.x, a2.y);
+                    }
+                    *px = make_uint4(yw[0], yw[1], yw[2], yw[3]);
                 }
-                if (i < tc) *reinterpret_cast<uint4*>(yrow + kk) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
             }
+          }
+            // y leaves the stage through TMA stores (rows past the sequence end
+            // are clipped by the tensor bounds)
+            tc::fence_proxy_async_smem();
             tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
+            asm volatile("bar.sync %0, %1;" ::"r"(2 + sid), "r"(wps * 32) : "memory");
+            if (stream_leader && ok) {
+                for (int cb = 0; cb < H / 64; ++cb)
+                    tc::tma_store_4d(&tm_y, sX + cb * (Tj * 128) + I * 16384, cb * 64, h0 + k, (int)(t0 + 128 * I),
+                                     (int)b);
+                tc::bulk_commit();
+                tc::bulk_wait_read_all();
                 tc::mbar_arrive(&bars[kBarSlotFree + st]);
-                tc::mbar_arrive(&bars[kBarYFree + sid]);
             }
+            if (ok && lane == 0) tc::mbar_arrive(&bars[kBarYFree + sid]);
         }
+        if (stream_leader) tc::bulk_wait_all();
         if (!ok) set_abort(ctl, p.status);
     }
 
@@ -611,15 +629,15 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
     p.dt = a.dt;
     p.G = a.G;
     p.D = a.D;
-    p.y = static_cast<__nv_bfloat16*>(a.y);
     p.status = device_status_word();
     const uint64_t H = g.headdim, S = g.dstate, nh = g.nheads, L = g.seqlen, G = g.ngroups;
-    CUtensorMap tm_x, tm_b, tm_c, tm_h;
+    CUtensorMap tm_x, tm_b, tm_c, tm_h, tm_y;
     {
         const uint64_t dims[4] = {H, nh, L, (uint64_t)g.batch};
         const uint64_t strides[3] = {H * 2, nh * H * 2, L * nh * H * 2};
         const uint32_t box[4] = {64, 1, 128, 1};
         if (!make_tmap_bf16(&tm_x, a.x, 4, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_tmap_bf16(&tm_y, a.y, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
         const uint64_t dims[4] = {S, G, L, (uint64_t)g.batch};
@@ -639,7 +657,7 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
                                          (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.head_blocks * (p.T / 128)), (unsigned)g.nchunks, (unsigned)g.batch);
-    k_chunk_out_tc<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, tm_c, tm_h, p);
+    k_chunk_out_tc<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, tm_c, tm_h, tm_y, p);
     return cudaGetLastError();
 }
 
