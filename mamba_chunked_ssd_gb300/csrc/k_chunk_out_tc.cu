@@ -122,36 +122,27 @@ __device__ __forceinline__ float exact_weight(float gi, float gj, float dtj) {
     return w > kWMax ? kWMax : w;
 }
 
-// Scales, in place, the 16-byte bf16 chunks [c_begin, c_begin + n) of one
-// 128-byte-swizzled row (chunk index = physical position, rotated by the row
-// to spread banks) by f, rounded once to bf16 per element (bf16x2 multiplies
-// by f rounded to bf16).  Boxes of 64 columns sit box_stride bytes apart.
-__device__ __forceinline__ void scale_row_chunks(uint8_t* base, uint32_t box_stride, int row, int c_begin, int n,
-                                                 float f) {
+// Scales, in place, four consecutive 16-byte bf16 chunks [c_begin, c_begin + 4)
+// of one 128-byte-swizzled row by f, rounded once to bf16 per element (bf16x2
+// multiplies by f rounded to bf16).  c_begin is a multiple of 4, so the four
+// chunks lie in one box of 64 columns; boxes sit box_stride bytes apart.  The
+// chunks are visited in physical order, rotated by the row to spread banks.
+__device__ __forceinline__ void scale_row4(uint8_t* base, uint32_t box_stride, int row, int c_begin, float f) {
     const uint32_t f2 = tc::pack_bf16x2(f, f);
+    uint8_t* rowp = base + (c_begin >> 3) * box_stride + row * 128;
+    const int c0 = (c_begin & 7) + row;
+    uint4 v[4];
 #pragma unroll
-    for (int t0 = 0; t0 < 4; t0 += 2) {  // two chunks in flight
-        uint4 v[2];
+    for (int t = 0; t < 4; ++t) v[t] = *reinterpret_cast<const uint4*>(rowp + (((c0 + t) & 7) << 4));
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (t0 + t >= n) break;
-            const int c = c_begin + t0 + t;
-            const int pc = ((c & 7) + row) & 7;
-            v[t] = *reinterpret_cast<const uint4*>(base + (c >> 3) * box_stride + row * 128 + pc * 16);
-        }
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (t0 + t >= n) break;
-            const int c = c_begin + t0 + t;
-            const int pc = ((c & 7) + row) & 7;
-            uint4 w = v[t];
-            w.x = tc::mul_bf16x2(w.x, f2);
-            w.y = tc::mul_bf16x2(w.y, f2);
-            w.z = tc::mul_bf16x2(w.z, f2);
-            w.w = tc::mul_bf16x2(w.w, f2);
-            *reinterpret_cast<uint4*>(base + (c >> 3) * box_stride + row * 128 + pc * 16) = w;
-        }
+    for (int t = 0; t < 4; ++t) {
+        v[t].x = tc::mul_bf16x2(v[t].x, f2);
+        v[t].y = tc::mul_bf16x2(v[t].y, f2);
+        v[t].z = tc::mul_bf16x2(v[t].z, f2);
+        v[t].w = tc::mul_bf16x2(v[t].w, f2);
     }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) *reinterpret_cast<uint4*>(rowp + (((c0 + t) & 7) << 4)) = v[t];
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -335,7 +326,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         const int part = (e % wps) >> 2;        // column part handled by this warp
         const int gpw = 4 / nparts;             // 32-column groups of P per warp
         const int ncoly = H / nparts;           // output columns per thread (32)
-        const int cpt = 8 * (H / 64) / nparts;  // 16-byte chunks per row per thread in the folds
+        // the folds give each thread 8 (H/64) / nparts = 4 chunks of 16 bytes per row
         const int il = q * 32 + lane;           // row inside the block = TMEM lane
         const int i = 128 * I + il;             // row inside the chunk
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
@@ -430,9 +421,9 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 uint8_t* sH = sX + p.off_h_in_stage;
                 const float g127 = vG[127];
                 const float a = exp2f(g127);
-                for (int r = il; r < S; r += 128) scale_row_chunks(sH, S * 128, r, part * cpt, cpt, a);
+                for (int r = il; r < S; r += 128) scale_row4(sH, S * 128, r, part * 4, a);
                 const float vj = exp2f(g127 - vG[il]) * vDt[il];
-                scale_row_chunks(sX, Tj * 128, il, part * cpt, cpt, vj);
+                scale_row4(sX, Tj * 128, il, part * 4, vj);
                 tc::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&bars[kBarOpsReady + sid]);
