@@ -145,6 +145,9 @@ __device__ __forceinline__ void scale_row4(uint8_t* base, uint32_t box_stride, i
     for (int t = 0; t < 4; ++t) *reinterpret_cast<uint4*>(rowp + (((c0 + t) & 7) << 4)) = v[t];
 }
 
+// H (head dim) and T (chunk) are compile-time, so the stream / part / box
+// counts and most swizzle offsets fold into constants.
+template <int H, int T>
 __global__ void __launch_bounds__(kThreads, 1)
 k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_h,
@@ -158,14 +161,14 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const int I = blockIdx.x / p.head_blocks;  // row block inside the chunk
     const int64_t c = blockIdx.y;
     const int64_t b = blockIdx.z;
-    const int64_t t0 = c * g.chunk;
-    const int tc = (int)imin64(g.chunk, g.seqlen - t0);  // valid tokens of the chunk
+    const int64_t t0 = (int64_t)c * T;
+    const int tc = (int)imin64(T, g.seqlen - t0);  // valid tokens of the chunk
     if (128 * I >= tc) return;                           // ragged tail: no valid row here
     const int h0 = hb * p.nhb;
     const int grp = (int)(h0 / g.heads_per_group);
     const int Tj = 128 * (I + 1);  // columns j that rows of block I can see
-    const int S = (int)g.dstate, H = (int)g.headdim;
-    const int nstr = p.nstr;
+    const int S = (int)g.dstate;
+    constexpr int nstr = (H == 64) ? 2 : 1;
     const int wps = kEpiWarps / nstr;  // warps per stream
 
     uint8_t* sC = smem + p.off_C;
@@ -236,7 +239,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             uint8_t* sX = sStage + st * p.stage_bytes;
             uint8_t* sH = sX + p.off_h_in_stage;
             float* vG = reinterpret_cast<float*>(sX + p.off_vec_in_stage);  // G[T], dt[T], D
-            float* vDt = vG + p.T;
+            float* vDt = vG + T;
             uint64_t* full = &bars[kBarFull + k % p.nfill];
             const int h = h0 + k;
             if (lane == 0) {
@@ -257,7 +260,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc::cp_async4(vG + j, Gh + jv, 4);
                 tc::cp_async4(vDt + j, dth + (int64_t)jv * g.nheads, j < tc ? 4u : 0u);
             }
-            if (lane == 0) tc::cp_async4(vDt + p.T, p.D ? p.D + h : p.dt, p.D ? 4u : 0u);
+            if (lane == 0) tc::cp_async4(vDt + T, p.D ? p.D + h : p.dt, p.D ? 4u : 0u);
             tc::cp_async_mbar_arrive_noinc(full);
         }
         if (!ok && lane == 0) set_abort(ctl, p.status);
@@ -393,7 +396,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             uint8_t* sX = sStage + st * p.stage_bytes;
           if (ok) {
             const float* vG = reinterpret_cast<const float*>(sX + p.off_vec_in_stage);
-            const float* vDt = vG + p.T;
+            const float* vDt = vG + T;
             const float grow = vG[i];
             const float gref = rq < 0 ? 0.f : vG[rq];
 
@@ -493,7 +496,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             // 16-byte pieces it reads; Y2, the last reader of X_I, is done)
             const float si = exp2f(grow - (I == 1 ? vG[127] : 0.f));
             const float ui = mild ? exp2f(grow - gref) : 1.f;
-            const float dh = vDt[p.T];
+            const float dh = vDt[T];
             const float2 si2 = make_float2(si, si), ui2 = make_float2(ui, ui), d2 = make_float2(dh, dh);
             uint8_t* xrow = sX + i * 128;
             ok = tc::mbar_wait(&bars[kBarYDone + sid], n & 1, abort_flag);
@@ -644,11 +647,12 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
         const uint32_t box[2] = {64, (uint32_t)S};
         if (!make_tmap_bf16(&tm_h, a.chunk_states, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(k_chunk_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)p.smem_bytes);
+    auto kern = (g.headdim == 64) ? (p.T == 256 ? k_chunk_out_tc<64, 256> : k_chunk_out_tc<64, 128>)
+                                  : (p.T == 256 ? k_chunk_out_tc<128, 256> : k_chunk_out_tc<128, 128>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.head_blocks * (p.T / 128)), (unsigned)g.nchunks, (unsigned)g.batch);
-    k_chunk_out_tc<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, tm_c, tm_h, tm_y, p);
+    kern<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, tm_c, tm_h, tm_y, p);
     return cudaGetLastError();
 }
 
