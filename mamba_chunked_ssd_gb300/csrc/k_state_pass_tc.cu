@@ -68,6 +68,9 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
     if (status) atomicExch(status, kStatusTimeout);
 }
 
+// H (head dim) and T (chunk) are compile-time, so the sub-block count and the
+// box and chunk offsets fold into constants.
+template <int H, int T>
 __global__ void __launch_bounds__(kThreads, 2)
 k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_cs, const SpTcParams p) {
@@ -80,8 +83,9 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int64_t b = blockIdx.z;
     const int64_t bh = b * g.nheads + h;
     const int grp = (int)(h / g.heads_per_group);
-    const int S = (int)g.dstate, H = (int)g.headdim;
-    const int nsub = (int)g.nchunks * p.nsb;  // total sub-blocks
+    const int S = (int)g.dstate;
+    constexpr int nsb = T / kKb;              // sub-blocks per chunk
+    const int nsub = (int)g.nchunks * nsb;  // total sub-blocks
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + p.off_bar + kNumBars * 8);
@@ -127,9 +131,9 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], ((u / p.nst) - 1) & 1, abort_flag);
                 if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) { ok = false; break; }
             }
-            const int c = u / p.nsb, sb = u % p.nsb;
-            const int64_t t0 = c * g.chunk;
-            const int tc = (int)imin64(g.chunk, g.seqlen - t0);
+            const int c = u / nsb, sb = u % nsb;
+            const int64_t t0 = (int64_t)c * T;
+            const int tc = (int)imin64(T, g.seqlen - t0);
             const int tok = (int)(t0 + sb * kKb);
             uint8_t* sB = smem + st * p.stage_bytes;
             uint8_t* sX = sB + p.off_x_in_stage;
@@ -166,7 +170,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // B = w . X_c (rows tokens = K, columns head dim = N): both MN-major.
             const uint32_t idesc = tc::idesc_bf16(128, H, true, true);
             for (int u = 0; u < nsub; ++u) {
-                const int st = u % p.nst, c = u / p.nsb, sb = u % p.nsb, ub = c & 1;
+                const int st = u % p.nst, c = u / nsb, sb = u % nsb, ub = c & 1;
                 if (sb == 0 && c >= 2 && !tc::mbar_wait(&bars[kBarUFree + ub], ((c >> 1) - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -184,7 +188,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     tc::mma_bf16_ss(tm_u0 + ub * H, da, db, idesc, (sb > 0 || k16 > 0) ? 1u : 0u);
                 }
                 tc::mma_commit(&bars[kBarSlotFree + st]);
-                if (sb == p.nsb - 1) tc::mma_commit(&bars[kBarUDone + ub]);
+                if (sb == nsb - 1) tc::mma_commit(&bars[kBarUDone + ub]);
             }
             if (!ok) set_abort(ctl, p.status);
         }
@@ -237,10 +241,11 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
             const float* Gbh = p.G + bh * g.seqlen;
             auto glast_of = [&](int c) -> float {
-                const int64_t t0 = (int64_t)c * g.chunk;
-                return Gbh[t0 + imin64(g.chunk, g.seqlen - t0) - 1];
+                const int64_t t0 = (int64_t)c * T;
+                return Gbh[t0 + imin64(T, g.seqlen - t0) - 1];
             };
             // h <- initial state (or zeros)
+#pragma unroll 1
             for (int m = 0; m < H / 16; ++m) {
                 uint32_t r[16];
 #pragma unroll
@@ -270,6 +275,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 for (int half = 0; half < 2; ++half) {
                     if (mt * 128 + 64 * half >= S) break;  // dstate = 64: one half only
                     if (ok && (q >> 1) == half) {
+#pragma unroll 1
                         for (int m = 0; m < H / 16; ++m) {
                             uint32_t hv[16], uv[16];
                             tc::tmem_ld16_nowait(tm_h + lane_base + 16 * m, hv);
@@ -309,6 +315,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             }
             if (leader) tc::bulk_wait_all();
             if (ok && p.final_state && valid) {
+#pragma unroll 1
                 for (int m = 0; m < H / 16; ++m) {
                     uint32_t hv[16];
                     tc::tmem_ld16(tm_h + lane_base + 16 * m, hv);
@@ -395,12 +402,16 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
         const uint32_t box[2] = {64, 64};
         if (!make_tmap_bf16(&tm_cs, a.chunk_states, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(k_state_pass_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)p.smem_bytes);
+    auto kern = (g.headdim == 64)
+                    ? (g.chunk == 256 ? k_state_pass_tc<64, 256>
+                                      : (g.chunk == 128 ? k_state_pass_tc<64, 128> : k_state_pass_tc<64, 64>))
+                    : (g.chunk == 256 ? k_state_pass_tc<128, 256>
+                                      : (g.chunk == 128 ? k_state_pass_tc<128, 128> : k_state_pass_tc<128, 64>));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     const int mtiles = (int)((g.dstate + 127) / 128);
     dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)g.batch);
-    k_state_pass_tc<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, tm_cs, p);
+    kern<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, tm_cs, p);
     return cudaGetLastError();
 }
 
