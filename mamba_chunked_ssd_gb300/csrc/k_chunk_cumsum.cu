@@ -7,10 +7,11 @@
 // stages read one head's decays as one contiguous run.
 //
 // GB300 mapping: one CTA per (chunk, block of 32 heads, batch).  dt rows of 32
-// heads (128 B) are read coalesced into shared memory, each warp scans whole
-// heads (per-lane serial prefix + warp-shuffle scan of the lane totals), and
-// the tile is written back transposed, coalesced along t.  Pure streaming:
-// every thread issues all of its loads before it stores any of them.
+// heads (128 B) are read coalesced into shared memory, each warp scans a
+// 32-token segment of all 32 heads (one head per lane), segment offsets are
+// added in order, and the tile is written back transposed, coalesced along t.
+// Pure streaming: every thread issues all of its loads before it stores any of
+// them.
 #include "common.cuh"
 
 namespace m2 {
@@ -24,6 +25,7 @@ __global__ void __launch_bounds__(kThreads)
 k_chunk_cumsum(const float* __restrict__ dt, const float* __restrict__ A, float* __restrict__ G,
                Geom g) {
     __shared__ float tile[kMaxChunk][kHeadsPerCta + 1];
+    __shared__ float seg_total[kThreads / 32][kHeadsPerCta];
     const int64_t c = blockIdx.x;
     const int64_t h0 = (int64_t)blockIdx.y * kHeadsPerCta;
     const int64_t b = blockIdx.z;
@@ -33,7 +35,8 @@ k_chunk_cumsum(const float* __restrict__ dt, const float* __restrict__ A, float*
 
     // a_t = A[h] * dt[b, t, h], coalesced over heads.  Thread (r, hh) owns
     // head column hh and rows r, r + 8, ...: all of its loads are issued
-    // before the first store, so their latencies overlap.
+    // before the first store, so their latencies overlap.  Rows past the
+    // chunk's valid tokens are zero.
     constexpr int kRowsPerPass = kThreads / kHeadsPerCta;       // 8
     constexpr int kPasses = kMaxChunk / kRowsPerPass;           // 32
     const int hh = threadIdx.x % kHeadsPerCta, r = threadIdx.x / kHeadsPerCta;
@@ -47,49 +50,27 @@ k_chunk_cumsum(const float* __restrict__ dt, const float* __restrict__ A, float*
         v[k] = (hv && t < tc) ? dcol[(int64_t)t * g.nheads] : 0.f;
     }
 #pragma unroll
-    for (int k = 0; k < kPasses; ++k) {
-        const int t = r + kRowsPerPass * k;
-        if (t < tc) tile[t][hh] = a * v[k];
-    }
+    for (int k = 0; k < kPasses; ++k) tile[r + kRowsPerPass * k][hh] = a * v[k];
     __syncthreads();
 
-    // Inclusive scan along t.  Warp w scans heads w, w + 8, w + 16, w + 24
-    // together: per lane a serial prefix over its run of tokens, then a
-    // warp-shuffle scan of the lane totals.
+    // Inclusive scan along t.  Warp w scans rows [32 w, 32 w + 32) with one
+    // head per lane (conflict-free: a row's 32 heads sit in 32 banks); the
+    // segment offsets are then summed from lower segments only, in a fixed
+    // order, so G_t never depends on tokens after t.
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    constexpr int kHeadsPerWarp = kHeadsPerCta / (kThreads / 32);  // 4
-    const int per_lane = (tc + 31) / 32;
-    const int lo = lane * per_lane;
-    const int hi = min(lo + per_lane, tc);
-    float run[kHeadsPerWarp];
-#pragma unroll
-    for (int u = 0; u < kHeadsPerWarp; ++u) run[u] = 0.f;
-    for (int t = lo; t < hi; ++t) {
-#pragma unroll
-        for (int u = 0; u < kHeadsPerWarp; ++u) {
-            run[u] += tile[t][warp + 8 * u];
-            tile[t][warp + 8 * u] = run[u];
-        }
+    const int seg0 = 32 * warp;
+    float run = 0.f;
+#pragma unroll 8
+    for (int t = seg0; t < seg0 + 32; ++t) {
+        run += tile[t][lane];
+        tile[t][lane] = run;
     }
-    // exclusive prefix of the lane totals, formed from lower lanes only
-    // (never as inclusive - own), so G_t cannot depend on tokens after t
-    float excl[kHeadsPerWarp];
-#pragma unroll
-    for (int u = 0; u < kHeadsPerWarp; ++u) {
-        float incl = run[u];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float n = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += n;
-        }
-        excl[u] = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) excl[u] = 0.f;
-    }
-    for (int t = lo; t < hi; ++t) {
-#pragma unroll
-        for (int u = 0; u < kHeadsPerWarp; ++u)
-            tile[t][warp + 8 * u] = (tile[t][warp + 8 * u] + excl[u]) * kLog2e;
-    }
+    seg_total[warp][lane] = run;
+    __syncthreads();
+    float off = 0.f;
+    for (int w = 0; w < warp; ++w) off += seg_total[w][lane];
+#pragma unroll 8
+    for (int t = seg0; t < seg0 + 32; ++t) tile[t][lane] = (tile[t][lane] + off) * kLog2e;
     __syncthreads();
 
     // G[b, h, t0 + t], coalesced along t.
