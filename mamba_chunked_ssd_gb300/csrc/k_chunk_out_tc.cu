@@ -48,14 +48,14 @@ namespace {
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kSmemLimit = 232448;
-constexpr int kMaxStages = 3;
+constexpr int kMaxStages = 5;
 constexpr int kMaxStreams = 2;
 // Fill barriers of the stages.  Head k fills stage k % nst and is read by
 // stream k % nstr; its fill is signalled on barrier k % nfill with
 // nfill = lcm(nst, nstr), so that each barrier's fills all go to one stage and
 // one stream and every waiter sees each phase of it in order (a waiter that
 // skipped a phase would take the next-but-one phase parity for its own).
-constexpr int kMaxFill = 6;  // lcm(3, 2)
+constexpr int kMaxFill = 10;  // lcm(5, 2)
 // Arrivals that complete a fill: the producer's expect-tx, then one per lane
 // when that lane's cp.async gathers have landed.
 constexpr int kFillArrivals = 1 + 32;
@@ -67,18 +67,23 @@ constexpr uint32_t kColCB = 0;
 __host__ __device__ constexpr uint32_t col_p(int s) { return 128u + 64u * (uint32_t)s; }
 __host__ __device__ constexpr uint32_t col_z(int s, int H) { return 256u + 2u * (uint32_t)H * (uint32_t)s; }
 
+// Shared-memory layout of a CTA of row block I: C_I, (I = 1) CB_10, then the
+// stages; a stage holds X [128 (I + 1) rows x H] | h_c [S x H] | G[T] dt[T] D.
+// Block 0 needs neither X_1 nor CB_10, so it fits more stages.
+struct CoLayout {
+    int nst;    // pipeline stages
+    int nfill;  // stage-fill barriers, lcm(nst, nstr)
+    uint32_t off_stage, stage_bytes, off_h_in_stage, off_vec_in_stage, off_small, off_bar, smem_bytes;
+};
+
 struct CoTcParams {
     Geom g;
     int T;            // chunk size (128 or 256)
     int nhb;          // heads per CTA (all in one group)
-    int nst;          // pipeline stages
     int nstr;         // epilogue head streams (2 for H = 64, 1 for H = 128)
-    int nfill;        // stage-fill barriers, lcm(nst, nstr)
     int head_blocks;  // nheads / nhb
-    // shared-memory layout: C, CB_10, then the stages; a stage holds
-    // X [T rows x H] | h_c [S x H] | G[T] dt[T] D
-    uint32_t off_C, off_CB10, off_stage, stage_bytes, off_h_in_stage, off_vec_in_stage, off_small, off_bar,
-        smem_bytes;
+    uint32_t off_C, off_CB10, smem_bytes;
+    CoLayout lay[2];  // by row block I
     const float* dt;
     const float* G;
     const float* D;
@@ -173,10 +178,11 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
     uint8_t* sC = smem + p.off_C;
     uint8_t* sCB10 = smem + p.off_CB10;
-    uint8_t* sStage = smem + p.off_stage;
+    const CoLayout lay = I ? p.lay[1] : p.lay[0];
+    uint8_t* sStage = smem + lay.off_stage;
     uint8_t* sB = sCB10;  // B overlays CB_10 and the stages until the CB products are done
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + p.off_bar + kNumBars * 8);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.off_bar);
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + lay.off_bar + kNumBars * 8);
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&bars[kBarCbFull], 1);
@@ -227,20 +233,20 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         if (lane == 0) ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
         ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
         for (int k = 0; ok && k < p.nhb; ++k) {
-            const int st = k % p.nst;
-            if (k >= p.nst) {
+            const int st = k % lay.nst;
+            if (k >= lay.nst) {
                 bool w_ok = true;
-                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], ((k / p.nst) - 1) & 1, abort_flag);
+                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], ((k / lay.nst) - 1) & 1, abort_flag);
                 if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) {
                     ok = false;
                     break;
                 }
             }
-            uint8_t* sX = sStage + st * p.stage_bytes;
-            uint8_t* sH = sX + p.off_h_in_stage;
-            float* vG = reinterpret_cast<float*>(sX + p.off_vec_in_stage);  // G[T], dt[T], D
+            uint8_t* sX = sStage + st * lay.stage_bytes;
+            uint8_t* sH = sX + lay.off_h_in_stage;
+            float* vG = reinterpret_cast<float*>(sX + lay.off_vec_in_stage);  // G[T], dt[T], D
             float* vDt = vG + T;
-            uint64_t* full = &bars[kBarFull + k % p.nfill];
+            uint64_t* full = &bars[kBarFull + k % lay.nfill];
             const int h = h0 + k;
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(full, x_bytes + h_bytes);
@@ -285,11 +291,11 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const uint32_t id_y = tc::idesc_bf16(128, H, false, true);
             const uint32_t aCB10 = tc::smem_u32(sCB10);
             for (int k = 0; ok && k < p.nhb; ++k) {
-                const int st = k % p.nst, s = k % nstr, n = k / nstr;
-                uint8_t* sX = sStage + st * p.stage_bytes;
-                const uint32_t aX = tc::smem_u32(sX), aH = tc::smem_u32(sX + p.off_h_in_stage);
+                const int st = k % lay.nst, s = k % nstr, n = k / nstr;
+                uint8_t* sX = sStage + st * lay.stage_bytes;
+                const uint32_t aX = tc::smem_u32(sX), aH = tc::smem_u32(sX + lay.off_h_in_stage);
                 const uint32_t tz = tmem + col_z(s, H), ty2 = tz + H;
-                if (!tc::mbar_wait(&bars[kBarFull + k % p.nfill], (k / p.nfill) & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarFull + k % lay.nfill], (k / lay.nfill) & 1, abort_flag)) { ok = false; break; }
                 if (n >= 1 && !tc::mbar_wait(&bars[kBarYFree + s], (n - 1) & 1, abort_flag)) { ok = false; break; }
                 if (I == 1 && !tc::mbar_wait(&bars[kBarOpsReady + s], n & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
@@ -334,7 +340,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         const int i = 128 * I + il;             // row inside the chunk
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t tz = tmem + col_z(sid, H), ty2 = tz + H, tp = tmem + col_p(sid);
-        float* wv = reinterpret_cast<float*>(smem + p.off_small) + e * 64;  // per warp: w of 2 column groups
+        float* wv = reinterpret_cast<float*>(smem + lay.off_small) + e * 64;  // per warp: w of 2 column groups
         const int rq = 128 * I + 32 * q - 1;   // the column before this quadrant (-1: before the chunk)
 
         bool ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
@@ -391,11 +397,11 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // left at the barrier; after a failed wait a warp only skips the work.
         const bool stream_leader = (e % wps == 0) && lane == 0;
         for (int k = sid; k < p.nhb; k += nstr) {
-            const int st = k % p.nst, n = k / nstr;
-            if (ok) ok = tc::mbar_wait(&bars[kBarFull + k % p.nfill], (k / p.nfill) & 1, abort_flag);
-            uint8_t* sX = sStage + st * p.stage_bytes;
+            const int st = k % lay.nst, n = k / nstr;
+            if (ok) ok = tc::mbar_wait(&bars[kBarFull + k % lay.nfill], (k / lay.nfill) & 1, abort_flag);
+            uint8_t* sX = sStage + st * lay.stage_bytes;
           if (ok) {
-            const float* vG = reinterpret_cast<const float*>(sX + p.off_vec_in_stage);
+            const float* vG = reinterpret_cast<const float*>(sX + lay.off_vec_in_stage);
             const float* vDt = vG + T;
             const float grow = vG[i];
             const float gref = rq < 0 ? 0.f : vG[rq];
@@ -421,7 +427,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
             if (I == 1) {
                 // a h_c and v . X_0, in place in the stage
-                uint8_t* sH = sX + p.off_h_in_stage;
+                uint8_t* sH = sX + lay.off_h_in_stage;
                 const float g127 = vG[127];
                 const float a = exp2f(g127);
                 for (int r = il; r < S; r += 128) scale_row4(sH, S * 128, r, part * 4, a);
@@ -570,34 +576,44 @@ int lcm_small(int a, int b) {
     return m;
 }
 
-bool plan_smem(const Geom& g, CoTcParams& p) {
-    const int T = (int)g.chunk, S = (int)g.dstate, H = (int)g.headdim;
-    p.nstr = (H == 64) ? 2 : 1;
-    p.off_C = 0;
-    p.off_CB10 = p.off_C + 128 * S * 2;
-    p.off_stage = p.off_CB10 + (T == 256 ? 32768 : 0);
-    p.off_h_in_stage = T * H * 2;
-    p.off_vec_in_stage = p.off_h_in_stage + S * H * 2;
+bool plan_layout(const Geom& g, int I, int nstr, uint32_t off_CB10, CoLayout& L) {
+    const int T = (int)g.chunk, S = (int)g.dstate, H = (int)g.headdim, Tj = 128 * (I + 1);
+    L.off_stage = off_CB10 + (I == 1 ? 32768u : 0u);
+    L.off_h_in_stage = (uint32_t)(Tj * H * 2);
+    L.off_vec_in_stage = L.off_h_in_stage + (uint32_t)(S * H * 2);
     const uint32_t vec_bytes = (uint32_t)(2 * T + 4) * 4;
-    p.stage_bytes = (p.off_vec_in_stage + vec_bytes + 1023) / 1024 * 1024;  // swizzled tiles: 1024-aligned
+    L.stage_bytes = (L.off_vec_in_stage + vec_bytes + 1023) / 1024 * 1024;  // swizzled tiles: 1024-aligned
     for (int nst = kMaxStages; nst >= 1; --nst) {
         // B (for the CB products) overlays CB_10, the stages and, if it is
         // longer, the per-warp area: all are written only after CB is done.
-        const uint32_t stages_end = p.off_stage + nst * p.stage_bytes;
-        const uint32_t b_end = p.off_CB10 + (uint32_t)(T * S * 2);
+        const uint32_t stages_end = L.off_stage + nst * L.stage_bytes;
+        const uint32_t b_end = off_CB10 + (uint32_t)(Tj * S * 2);
         const uint32_t off_small = stages_end > b_end ? stages_end : b_end;
         const uint32_t off_bar = off_small + kEpiWarps * 64 * 4;
         const uint32_t total = off_bar + kNumBars * 8 + 64 + 1024;  // + ctl + alignment slack
         if (total <= (uint32_t)kSmemLimit) {
-            p.nst = nst;
-            p.nfill = lcm_small(nst, p.nstr);
-            p.off_small = off_small;
-            p.off_bar = off_bar;
-            p.smem_bytes = total;
-            return p.nfill <= kMaxFill;
+            L.nst = nst;
+            L.nfill = lcm_small(nst, nstr);
+            L.off_small = off_small;
+            L.off_bar = off_bar;
+            L.smem_bytes = total;
+            return L.nfill <= kMaxFill;
         }
     }
     return false;
+}
+
+bool plan_smem(const Geom& g, CoTcParams& p) {
+    p.nstr = (g.headdim == 64) ? 2 : 1;
+    p.off_C = 0;
+    p.off_CB10 = p.off_C + 128 * (uint32_t)g.dstate * 2;
+    p.smem_bytes = 0;
+    for (int I = 0; I < (int)(g.chunk / 128); ++I) {
+        if (!plan_layout(g, I, p.nstr, p.off_CB10, p.lay[I])) return false;
+        if (p.lay[I].smem_bytes > p.smem_bytes) p.smem_bytes = p.lay[I].smem_bytes;
+    }
+    if (g.chunk == 128) p.lay[1] = p.lay[0];  // unused
+    return true;
 }
 
 }  // namespace
