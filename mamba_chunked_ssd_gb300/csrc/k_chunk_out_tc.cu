@@ -439,54 +439,61 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             }
 
             // ---- P on the diagonal block -> TMEM as bf16 (CB is masked already),
-            // 16 columns at a time
+            // one 32-column group at a time: both 16-column halves are loaded
+            // under one wait
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (t >= gpw) break;
                 const int gi = part * gpw + t;  // 32-column group 0..3 of the diagonal block
+                if (gi > q) {
+                    uint32_t z[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) z[x] = 0u;
+                    tc::tmem_st8(tp + lane_base + 16 * gi, z);
+                    tc::tmem_st8(tp + lane_base + 16 * gi + 8, z);
+                    continue;
+                }
+                uint32_t r[2][16];
+                tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi, r[0]);
+                tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi + 16, r[1]);
+                tc::tmem_wait_ld16(r[0]);
+                tc::tmem_tie16(r[1]);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const uint32_t col = 32 * gi + 16 * hh;  // first column of this piece
                     const float* w = wv + 32 * t + 16 * hh;
                     const float* gj = vG + 128 * I + col;
                     const float* dj = vDt + 128 * I + col;
+                    const uint32_t* rr = r[hh];
                     uint32_t pk[8];
-                    if (gi > q) {
+                    if (all_mild) {
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) pk[x] = 0u;
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const float4 v4 = *reinterpret_cast<const float4*>(w + 4 * e4);
+                            const int o = 4 * e4;
+                            const float2 p0 = tc::mul_f32x2(
+                                make_float2(__uint_as_float(rr[o]), __uint_as_float(rr[o + 1])), make_float2(v4.x, v4.y));
+                            const float2 p1 = tc::mul_f32x2(
+                                make_float2(__uint_as_float(rr[o + 2]), __uint_as_float(rr[o + 3])), make_float2(v4.z, v4.w));
+                            pk[2 * e4] = tc::pack_bf16x2(p0.x, p0.y);
+                            pk[2 * e4 + 1] = tc::pack_bf16x2(p1.x, p1.y);
+                        }
                     } else {
-                        uint32_t r[16];
-                        tc::tmem_ld16_nowait(tmem + kColCB + lane_base + col, r);
-                        tc::tmem_wait_ld16(r);
-                        if (all_mild) {
+                        // per row: the split weight (mild rows, the same products
+                        // as above) or the direct one
 #pragma unroll
-                            for (int e4 = 0; e4 < 4; ++e4) {
-                                const float4 v4 = *reinterpret_cast<const float4*>(w + 4 * e4);
-                                const int o = 4 * e4;
-                                const float2 p0 = tc::mul_f32x2(
-                                    make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1])), make_float2(v4.x, v4.y));
-                                const float2 p1 = tc::mul_f32x2(
-                                    make_float2(__uint_as_float(r[o + 2]), __uint_as_float(r[o + 3])), make_float2(v4.z, v4.w));
-                                pk[2 * e4] = tc::pack_bf16x2(p0.x, p0.y);
-                                pk[2 * e4 + 1] = tc::pack_bf16x2(p1.x, p1.y);
-                            }
-                        } else {
-                            // per row: the split weight (mild rows, the same products
-                            // as above) or the direct one
-#pragma unroll
-                            for (int e4 = 0; e4 < 4; ++e4) {
-                                const float4 v4 = *reinterpret_cast<const float4*>(w + 4 * e4);
-                                const float4 g4 = *reinterpret_cast<const float4*>(gj + 4 * e4);
-                                const float4 d4 = *reinterpret_cast<const float4*>(dj + 4 * e4);
-                                const int o = 4 * e4;
-                                const float f0 = mild ? v4.x : exact_weight(grow, g4.x, d4.x);
-                                const float f1 = mild ? v4.y : exact_weight(grow, g4.y, d4.y);
-                                const float f2 = mild ? v4.z : exact_weight(grow, g4.z, d4.z);
-                                const float f3 = mild ? v4.w : exact_weight(grow, g4.w, d4.w);
-                                pk[2 * e4] = tc::pack_bf16x2(__uint_as_float(r[o]) * f0, __uint_as_float(r[o + 1]) * f1);
-                                pk[2 * e4 + 1] =
-                                    tc::pack_bf16x2(__uint_as_float(r[o + 2]) * f2, __uint_as_float(r[o + 3]) * f3);
-                            }
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const float4 v4 = *reinterpret_cast<const float4*>(w + 4 * e4);
+                            const float4 g4 = *reinterpret_cast<const float4*>(gj + 4 * e4);
+                            const float4 d4 = *reinterpret_cast<const float4*>(dj + 4 * e4);
+                            const int o = 4 * e4;
+                            const float f0 = mild ? v4.x : exact_weight(grow, g4.x, d4.x);
+                            const float f1 = mild ? v4.y : exact_weight(grow, g4.y, d4.y);
+                            const float f2 = mild ? v4.z : exact_weight(grow, g4.z, d4.z);
+                            const float f3 = mild ? v4.w : exact_weight(grow, g4.w, d4.w);
+                            pk[2 * e4] = tc::pack_bf16x2(__uint_as_float(rr[o]) * f0, __uint_as_float(rr[o + 1]) * f1);
+                            pk[2 * e4 + 1] =
+                                tc::pack_bf16x2(__uint_as_float(rr[o + 2]) * f2, __uint_as_float(rr[o + 3]) * f3);
                         }
                     }
                     tc::tmem_st8(tp + lane_base + col / 2, pk);
@@ -508,31 +515,43 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             ok = tc::mbar_wait(&bars[kBarYDone + sid], n & 1, abort_flag);
             tc::tc_fence_after();
             if (ok) {
+                // two 8-column slices of Z and Y2 (and their x chunks) per wait
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    if (m >= ncoly / 8) break;
-                    const int kk = part * ncoly + 8 * m;
-                    uint32_t za[8], yb[8];
-                    tc::tmem_ld8_nowait(tz + lane_base + kk, za);
-                    tc::tmem_ld8_nowait(ty2 + lane_base + kk, yb);
-                    uint4* px = reinterpret_cast<uint4*>(xrow + (kk >> 6) * (Tj * 128) +
+                for (int mp = 0; mp < 2; ++mp) {
+                    if (mp >= ncoly / 16) break;
+                    uint32_t za[2][8], yb[2][8];
+                    uint4* px[2];
+                    uint4 xv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int kk = part * ncoly + 16 * mp + 8 * u;
+                        tc::tmem_ld8_nowait(tz + lane_base + kk, za[u]);
+                        tc::tmem_ld8_nowait(ty2 + lane_base + kk, yb[u]);
+                        px[u] = reinterpret_cast<uint4*>(xrow + (kk >> 6) * (Tj * 128) +
                                                          ((((kk & 63) >> 3) ^ (i & 7)) << 4));
-                    const uint4 xv = *px;
-                    tc::tmem_wait_ld8(za);
-                    tc::tmem_wait_ld8(yb);
-                    // y = si Z + ui Y2 + D x, in fp32, rounded once to bf16
-                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                    uint32_t yw[4];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const float2 t2 = tc::fma_f32x2(d2, make_float2(tc::bf16_lo(xw[x]), tc::bf16_hi(xw[x])),
-                                                        tc::mul_f32x2(ui2, make_float2(__uint_as_float(yb[2 * x]),
-                                                                                       __uint_as_float(yb[2 * x + 1]))));
-                        const float2 a2 = tc::fma_f32x2(
-                            si2, make_float2(__uint_as_float(za[2 * x]), __uint_as_float(za[2 * x + 1])), t2);
-                        yw[x] = tc::pack_bf16x2(a2.x, a2.y);
                     }
-                    *px = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+                    xv[0] = *px[0];
+                    xv[1] = *px[1];
+                    tc::tmem_wait_ld8(za[0]);
+                    tc::tmem_tie8(yb[0]);
+                    tc::tmem_tie8(za[1]);
+                    tc::tmem_tie8(yb[1]);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        // y = si Z + ui Y2 + D x, in fp32, rounded once to bf16
+                        const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+                        uint32_t yw[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const float2 t2 = tc::fma_f32x2(
+                                d2, make_float2(tc::bf16_lo(xw[x]), tc::bf16_hi(xw[x])),
+                                tc::mul_f32x2(ui2, make_float2(__uint_as_float(yb[u][2 * x]), __uint_as_float(yb[u][2 * x + 1]))));
+                            const float2 a2 = tc::fma_f32x2(
+                                si2, make_float2(__uint_as_float(za[u][2 * x]), __uint_as_float(za[u][2 * x + 1])), t2);
+                            yw[x] = tc::pack_bf16x2(a2.x, a2.y);
+                        }
+                        *px[u] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+                    }
                 }
             }
           }
