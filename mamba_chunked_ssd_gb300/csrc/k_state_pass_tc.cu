@@ -169,26 +169,41 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // A = B_c^T (rows of the box are tokens = K, columns are states = M),
             // B = w . X_c (rows tokens = K, columns head dim = N): both MN-major.
             const uint32_t idesc = tc::idesc_bf16(128, H, true, true);
+            // This one thread paces the kernel, so its loop is kept short: the
+            // stage index and phase are counters, and the descriptors of a
+            // stage are the first stage's advanced by whole stages (the 14-bit
+            // address field, in 16-byte units, cannot carry: shared memory is
+            // below 256 KB) and by 2 KB (128 units) per 16 tokens.
+            const uint64_t desc0 = tc::sdesc_sw128(tc::smem_u32(smem), x_box_bytes, 1024);
+            const uint64_t stage_step = p.stage_bytes >> 4, x_step = p.off_x_in_stage >> 4;
+            uint64_t dstage = desc0;
+            int st = 0;
+            uint32_t phase = 0;
             for (int u = 0; u < nsub; ++u) {
-                const int st = u % p.nst, c = u / nsb, sb = u % nsb, ub = c & 1;
+                const int c = u / nsb, sb = u % nsb, ub = c & 1;
                 if (sb == 0 && c >= 2 && !tc::mbar_wait(&bars[kBarUFree + ub], ((c >> 1) - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                if (!tc::mbar_wait(&bars[kBarXform + st], (u / p.nst) & 1, abort_flag)) {
+                if (!tc::mbar_wait(&bars[kBarXform + st], phase, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc::tc_fence_after();
-                const uint32_t aB = tc::smem_u32(smem + st * p.stage_bytes);
-                const uint32_t aX = aB + p.off_x_in_stage;
-                for (int k16 = 0; k16 < kKb / 16; ++k16) {
-                    const uint64_t da = tc::sdesc_sw128(aB + k16 * 2048, x_box_bytes, 1024);
-                    const uint64_t db = tc::sdesc_sw128(aX + k16 * 2048, x_box_bytes, 1024);
-                    tc::mma_bf16_ss(tm_u0 + ub * H, da, db, idesc, (sb > 0 || k16 > 0) ? 1u : 0u);
-                }
+                const uint32_t tu = tm_u0 + ub * H;
+#pragma unroll
+                for (int k16 = 0; k16 < kKb / 16; ++k16)
+                    tc::mma_bf16_ss(tu, dstage + 128 * k16, dstage + x_step + 128 * k16, idesc,
+                                    (sb > 0 || k16 > 0) ? 1u : 0u);
                 tc::mma_commit(&bars[kBarSlotFree + st]);
                 if (sb == nsb - 1) tc::mma_commit(&bars[kBarUDone + ub]);
+                if (++st == p.nst) {
+                    st = 0;
+                    phase ^= 1u;
+                    dstage = desc0;
+                } else {
+                    dstage += stage_step;
+                }
             }
             if (!ok) set_abort(ctl, p.status);
         }
