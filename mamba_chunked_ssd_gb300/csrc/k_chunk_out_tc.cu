@@ -289,40 +289,57 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 if (I == 1) ok = tc::mbar_wait(&bars[kBarCb10Ready], 0, abort_flag);
             }
             const uint32_t id_y = tc::idesc_bf16(128, H, false, true);
-            const uint32_t aCB10 = tc::smem_u32(sCB10);
+            // This one thread serves both head streams, so its loop is kept
+            // short: stage and fill-barrier indices and phases are counters, and
+            // every descriptor is a base built once plus a constant offset in
+            // its 14-bit address field (16-byte units; shared memory is below
+            // 256 KB, so the field cannot carry).  K-major A tiles (C_I, CB_10)
+            // advance 32 bytes per 16 columns inside a 64-column box and 16 KB
+            // per box; MN-major B tiles (h_c, X) advance 2 KB per 16 rows.
+            const uint64_t dC0 = tc::sdesc_sw128(aC, 16, 1024);
+            const uint64_t dCB10 = tc::sdesc_sw128(tc::smem_u32(sCB10), 16, 1024);
+            const uint64_t dH0 = tc::sdesc_sw128(tc::smem_u32(sStage + lay.off_h_in_stage), S * 128, 1024);
+            const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(sStage), Tj * 128, 1024);
+            const uint64_t stage_step = lay.stage_bytes >> 4;
+            uint64_t dstage = 0;  // stage offset, in descriptor units
+            int st = 0, fill = 0;
+            uint32_t fill_phase = 0;
             for (int k = 0; ok && k < p.nhb; ++k) {
-                const int st = k % lay.nst, s = k % nstr, n = k / nstr;
-                uint8_t* sX = sStage + st * lay.stage_bytes;
-                const uint32_t aX = tc::smem_u32(sX), aH = tc::smem_u32(sX + lay.off_h_in_stage);
+                const int s = k % nstr, n = k / nstr;
                 const uint32_t tz = tmem + col_z(s, H), ty2 = tz + H;
-                if (!tc::mbar_wait(&bars[kBarFull + k % lay.nfill], (k / lay.nfill) & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarFull + fill], fill_phase, abort_flag)) { ok = false; break; }
                 if (n >= 1 && !tc::mbar_wait(&bars[kBarYFree + s], (n - 1) & 1, abort_flag)) { ok = false; break; }
                 if (I == 1 && !tc::mbar_wait(&bars[kBarOpsReady + s], n & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
+                const uint64_t dH = dH0 + dstage, dX = dX0 + dstage;
                 // Z = C_I (a h_c)   (B operand: rows s = K, columns H = N, MN-major)
-                for (int k16 = 0; k16 < S / 16; ++k16) {
-                    const uint64_t da = tc::sdesc_sw128(aC + (k16 >> 2) * 16384 + (k16 & 3) * 32, 16, 1024);
-                    const uint64_t db = tc::sdesc_sw128(aH + k16 * 2048, S * 128, 1024);
-                    tc::mma_bf16_ss(tz, da, db, id_y, k16 > 0);
-                }
+                for (int k16 = 0; k16 < S / 16; ++k16)
+                    tc::mma_bf16_ss(tz, dC0 + (k16 >> 2) * 1024 + (k16 & 3) * 2, dH + 128 * k16, id_y, k16 > 0);
                 if (I == 1) {
                     // Z += CB_10 (v . X_0)   (A: CB_10 bf16, K-major over j; B: rows 0..127 of
                     // the stage's X, scaled in place, MN-major)
-                    for (int k16 = 0; k16 < 8; ++k16) {
-                        const uint64_t da = tc::sdesc_sw128(aCB10 + (k16 >> 2) * 16384 + (k16 & 3) * 32, 16, 1024);
-                        const uint64_t db = tc::sdesc_sw128(aX + k16 * 2048, Tj * 128, 1024);
-                        tc::mma_bf16_ss(tz, da, db, id_y, 1);
-                    }
+#pragma unroll
+                    for (int k16 = 0; k16 < 8; ++k16)
+                        tc::mma_bf16_ss(tz, dCB10 + (k16 >> 2) * 1024 + (k16 & 3) * 2, dX + 128 * k16, id_y, 1);
                 }
                 // Y2 = P X_I   (A: P in TMEM; B: rows 128I.. of X, MN-major)
                 if (!tc::mbar_wait(&bars[kBarPReady + s], n & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
-                for (int k16 = 0; k16 < 8; ++k16) {
-                    const uint64_t db = tc::sdesc_sw128(aX + I * 16384 + k16 * 2048, Tj * 128, 1024);
-                    tc::mma_bf16_ts(ty2, tmem + col_p(s) + k16 * 8, db, id_y, k16 > 0);
-                }
+#pragma unroll
+                for (int k16 = 0; k16 < 8; ++k16)
+                    tc::mma_bf16_ts(ty2, tmem + col_p(s) + k16 * 8, dX + I * 1024 + 128 * k16, id_y, k16 > 0);
                 tc::mma_commit(&bars[kBarYDone + s]);
                 tc::mma_commit(&bars[kBarSlotFree + st]);
+                if (++st == lay.nst) {
+                    st = 0;
+                    dstage = 0;
+                } else {
+                    dstage += stage_step;
+                }
+                if (++fill == lay.nfill) {
+                    fill = 0;
+                    fill_phase ^= 1u;
+                }
             }
             if (!ok) set_abort(ctl, p.status);
         }
