@@ -46,7 +46,8 @@ namespace m2 {
 namespace {
 
 constexpr int kEpiWarps = 16;
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kIssuer2 = 2 + kEpiWarps;  // warp 18: MMA issuer of head stream 1 (two streams)
+constexpr int kThreads = (kIssuer2 + 1) * 32;
 constexpr int kSmemLimit = 232448;
 constexpr int kMaxStages = 5;
 constexpr int kMaxStreams = 2;
@@ -270,12 +271,18 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::cp_async_mbar_arrive_noinc(full);
         }
         if (!ok && lane == 0) set_abort(ctl, p.status);
-    } else if (warp == 1) {
-        // ============================ MMA issuer ============================
+    } else if (warp == 1 || (nstr == 2 && warp == kIssuer2)) {
+        // ========================= MMA issuers (one per stream) =========================
+        // Warp 1 issues the C B^T products and the per-head products of stream
+        // 0, warp 18 those of stream 1, so neither stream waits behind the other.
         if (lane == 0) {
+            const int sid0 = (warp == 1) ? 0 : 1;
             bool ok = tc::mbar_wait(&bars[kBarCbFull], 0, abort_flag);
             const uint32_t aC = tc::smem_u32(sC), aB = tc::smem_u32(sB);
-            if (ok) {
+            if (ok && sid0 == 1) {
+                // stream 1 reads C_I (and for I = 1 the bf16 CB_10) from shared memory
+                if (I == 1) ok = tc::mbar_wait(&bars[kBarCb10Ready], 0, abort_flag);
+            } else if (ok) {
                 tc::tc_fence_after();
                 // CB_II = C_I B_I^T (both K-major over S); for I = 1 also CB_10 = C_1 B_0^T.
                 const uint32_t id_cb = tc::idesc_bf16(128, 128, false, false);
@@ -289,8 +296,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 if (I == 1) ok = tc::mbar_wait(&bars[kBarCb10Ready], 0, abort_flag);
             }
             const uint32_t id_y = tc::idesc_bf16(128, H, false, true);
-            // This one thread serves both head streams, so its loop is kept
-            // short: stage and fill-barrier indices and phases are counters, and
+            // Each issuing thread paces its stream, so its loop is kept short: stage and fill-barrier indices and phases are counters, and
             // every descriptor is a base built once plus a constant offset in
             // its 14-bit address field (16-byte units; shared memory is below
             // 256 KB, so the field cannot carry).  K-major A tiles (C_I, CB_10)
@@ -301,10 +307,10 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const uint64_t dH0 = tc::sdesc_sw128(tc::smem_u32(sStage + lay.off_h_in_stage), S * 128, 1024);
             const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(sStage), Tj * 128, 1024);
             const uint64_t stage_step = lay.stage_bytes >> 4;
-            uint64_t dstage = 0;  // stage offset, in descriptor units
-            int st = 0, fill = 0;
-            uint32_t fill_phase = 0;
-            for (int k = 0; ok && k < p.nhb; ++k) {
+            int st = sid0 % lay.nst, fill = sid0 % lay.nfill;
+            uint32_t fill_phase = (sid0 / lay.nfill) & 1;
+            uint64_t dstage = st * stage_step;  // stage offset, in descriptor units
+            for (int k = sid0; ok && k < p.nhb; k += nstr) {
                 const int s = k % nstr, n = k / nstr;
                 const uint32_t tz = tmem + col_z(s, H), ty2 = tz + H;
                 if (!tc::mbar_wait(&bars[kBarFull + fill], fill_phase, abort_flag)) { ok = false; break; }
@@ -330,20 +336,23 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tc::mma_bf16_ts(ty2, tmem + col_p(s) + k16 * 8, dX + I * 1024 + 128 * k16, id_y, k16 > 0);
                 tc::mma_commit(&bars[kBarYDone + s]);
                 tc::mma_commit(&bars[kBarSlotFree + st]);
-                if (++st == lay.nst) {
-                    st = 0;
-                    dstage = 0;
-                } else {
-                    dstage += stage_step;
-                }
-                if (++fill == lay.nfill) {
-                    fill = 0;
-                    fill_phase ^= 1u;
+#pragma unroll
+                for (int i = 0; i < nstr; ++i) {
+                    if (++st == lay.nst) {
+                        st = 0;
+                        dstage = 0;
+                    } else {
+                        dstage += stage_step;
+                    }
+                    if (++fill == lay.nfill) {
+                        fill = 0;
+                        fill_phase ^= 1u;
+                    }
                 }
             }
             if (!ok) set_abort(ctl, p.status);
         }
-    } else {
+    } else if (warp < kIssuer2) {
         // ============================== epilogue ==============================
         const int e = warp - 2;                 // 0..15
         const int sid = e / wps;                // head stream of this warp
