@@ -233,11 +233,13 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         bool ok = true;
         if (lane == 0) ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
         ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+        // stage, its reuse phase and the fill barrier as counters (no divisions)
+        int st = 0, fill = 0;
+        uint32_t slot_phase = 1;  // phase of the previous use of the stage
         for (int k = 0; ok && k < p.nhb; ++k) {
-            const int st = k % lay.nst;
             if (k >= lay.nst) {
                 bool w_ok = true;
-                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], ((k / lay.nst) - 1) & 1, abort_flag);
+                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], slot_phase, abort_flag);
                 if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) {
                     ok = false;
                     break;
@@ -247,7 +249,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             uint8_t* sH = sX + lay.off_h_in_stage;
             float* vG = reinterpret_cast<float*>(sX + lay.off_vec_in_stage);  // G[T], dt[T], D
             float* vDt = vG + T;
-            uint64_t* full = &bars[kBarFull + k % lay.nfill];
+            uint64_t* full = &bars[kBarFull + fill];
             const int h = h0 + k;
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(full, x_bytes + h_bytes);
@@ -269,6 +271,11 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             }
             if (lane == 0) tc::cp_async4(vDt + T, p.D ? p.D + h : p.dt, p.D ? 4u : 0u);
             tc::cp_async_mbar_arrive_noinc(full);
+            if (++st == lay.nst) {
+                st = 0;
+                slot_phase ^= 1u;
+            }
+            if (++fill == lay.nfill) fill = 0;
         }
         if (!ok && lane == 0) set_abort(ctl, p.status);
     } else if (warp == 1 || (nstr == 2 && warp == kIssuer2)) {
@@ -422,9 +429,12 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // named barrier below, whatever its own waits return, so no warp is
         // left at the barrier; after a failed wait a warp only skips the work.
         const bool stream_leader = (e % wps == 0) && lane == 0;
+        // stage and fill barrier of head k as counters, advanced by nstr heads
+        int st = sid % lay.nst, fill = sid % lay.nfill;
+        uint32_t fill_phase = (sid / lay.nfill) & 1;
         for (int k = sid; k < p.nhb; k += nstr) {
-            const int st = k % lay.nst, n = k / nstr;
-            if (ok) ok = tc::mbar_wait(&bars[kBarFull + k % lay.nfill], (k / lay.nfill) & 1, abort_flag);
+            const int n = k / nstr;
+            if (ok) ok = tc::mbar_wait(&bars[kBarFull + fill], fill_phase, abort_flag);
             uint8_t* sX = sStage + st * lay.stage_bytes;
           if (ok) {
             const float* vG = reinterpret_cast<const float*>(sX + lay.off_vec_in_stage);
@@ -595,6 +605,14 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc::mbar_arrive(&bars[kBarSlotFree + st]);
             }
             if (ok && lane == 0) tc::mbar_arrive(&bars[kBarYFree + sid]);
+#pragma unroll
+            for (int i = 0; i < nstr; ++i) {
+                if (++st == lay.nst) st = 0;
+                if (++fill == lay.nfill) {
+                    fill = 0;
+                    fill_phase ^= 1u;
+                }
+            }
         }
         if (stream_leader) tc::bulk_wait_all();
         if (!ok) set_abort(ctl, p.status);

@@ -124,11 +124,12 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
         const float* Gbh = p.G + bh * g.seqlen;
         bool ok = true;
-        for (int u = 0; u < nsub; ++u) {
-            const int st = u % p.nst;
+        int st = 0;
+        uint32_t slot_phase = 1;  // phase of the previous use of the stage (counters, no divisions)
+        for (int u = 0; u < nsub; ++u, st = (st + 1 == p.nst) ? (slot_phase ^= 1u, 0) : st + 1) {
             if (u >= p.nst) {
                 bool w_ok = true;
-                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], ((u / p.nst) - 1) & 1, abort_flag);
+                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], slot_phase, abort_flag);
                 if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) { ok = false; break; }
             }
             const int c = u / nsb, sb = u % nsb;
@@ -216,9 +217,10 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const int ft = (warp - 2) * 32 + lane;  // 0..127
             const int frow = ft >> 1, fh = ft & 1;
             const int per = 4 * (H / 64);           // chunks per thread (4 or 8)
-            for (int u = 0; ok && u < nsub; ++u) {
-                const int st = u % p.nst;
-                if (!tc::mbar_wait(&bars[kBarFull + st], (u / p.nst) & 1, abort_flag)) { ok = false; break; }
+            int st = 0;
+            uint32_t full_phase = 0;
+            for (int u = 0; ok && u < nsub; ++u, st = (st + 1 == p.nst) ? (full_phase ^= 1u, 0) : st + 1) {
+                if (!tc::mbar_wait(&bars[kBarFull + st], full_phase, abort_flag)) { ok = false; break; }
                 const float* sV = reinterpret_cast<const float*>(smem + st * p.stage_bytes + p.off_w_in_stage);
                 const float w = sV[64 + frow] * exp2f(sV[128] - sV[frow]);  // w_t = dt_t exp2(G_last - G_t)
                 uint8_t* rowp = smem + st * p.stage_bytes + p.off_x_in_stage + frow * 128;
