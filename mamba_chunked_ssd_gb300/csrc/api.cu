@@ -203,9 +203,13 @@ mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const flo
     void* cs = ws + round_up(z.G, 256);
     const Geom g = make_geom(*shape);
     if ((rc = from_cuda(launch_chunk_cumsum(g, dt, A, G, st))) != MAMBA2_OK) return rc;
-    const StatePassArgs sp{x, dt, B, G, initial_state, cs, final_state};
+    // stages 2 and 3 may start while the stage before them runs (programmatic
+    // dependent launch); they wait for it before reading its output
+    StatePassArgs sp{x, dt, B, G, initial_state, cs, final_state};
+    sp.pdl = true;
     if ((rc = run_state_pass(*shape, sp, st)) != MAMBA2_OK) return rc;
-    const ChunkOutArgs co{x, dt, B, C, D, G, cs, y};
+    ChunkOutArgs co{x, dt, B, C, D, G, cs, y};
+    co.pdl = true;
     return run_chunk_out(*shape, co, st);
 }
 

@@ -63,6 +63,9 @@ struct StatePassArgs {
     const float* init;  // may be null
     void* chunk_states;
     float* final_state;  // may be null
+    // Launch with programmatic stream serialization (the forward pass: the
+    // kernel may start while stage 1 runs and waits for it before reading G).
+    bool pdl = false;
 };
 
 struct ChunkOutArgs {
@@ -74,6 +77,8 @@ struct ChunkOutArgs {
     const float* G;
     const void* chunk_states;
     void* y;
+    // As StatePassArgs::pdl: may start while stage 2 runs.
+    bool pdl = false;
 };
 
 struct SsdStepArgs {

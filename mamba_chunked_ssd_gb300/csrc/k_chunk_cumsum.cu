@@ -24,6 +24,9 @@ constexpr int kMaxChunk = 256;
 __global__ void __launch_bounds__(kThreads)
 k_chunk_cumsum(const float* __restrict__ dt, const float* __restrict__ A, float* __restrict__ G,
                Geom g) {
+    // The state pass, launched after this kernel with programmatic stream
+    // serialization, may start now; it waits for this grid before reading G.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ float tile[kMaxChunk][kHeadsPerCta + 1];
     __shared__ float seg_total[kThreads / 32][kHeadsPerCta];
     const int64_t c = blockIdx.x;

@@ -229,6 +229,8 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                                     (int)(t0 + 128 * rb), (int)b);
             }
         }
+        // h_c and G come from the previous kernels
+        tc::griddep_wait();
         // the B area is reused by the stages
         bool ok = true;
         if (lane == 0) ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
@@ -731,8 +733,17 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.head_blocks * (p.T / 128)), (unsigned)g.nchunks, (unsigned)g.batch);
-    kern<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, tm_c, tm_h, tm_y, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_b, tm_c, tm_h, tm_y, p);
 }
 
 }  // namespace m2

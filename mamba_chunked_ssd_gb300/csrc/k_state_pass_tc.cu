@@ -116,12 +116,14 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     volatile int* abort_flag = &ctl->abort;
     const uint32_t x_box_bytes = kKb * 128;
 
+    tc::griddep_launch_dependents();  // stage 3 may start; it waits for this grid
     if (warp == 0) {
         // ===================== TMA producer + weight gather =====================
         if (lane == 0) {
             tc::tma_prefetch_desc(&tm_x);
             tc::tma_prefetch_desc(&tm_b);
         }
+        tc::griddep_wait();  // G comes from the previous kernel
         const float* Gbh = p.G + bh * g.seqlen;
         bool ok = true;
         int st = 0;
@@ -278,6 +280,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             uint8_t* stg = smem + p.off_stg;
             const int hrow = (q & 1) * 32 + lane;  // row inside the 64-row tile
             const bool leader = (q == 0 && lane == 0);
+            tc::griddep_wait();  // G comes from the previous kernel
             float gl_next = glast_of(0);
             // Every scan warp runs every iteration and every named barrier below,
             // whatever its own waits return, so no warp is left at a barrier;
@@ -428,8 +431,17 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     if (e != cudaSuccess) return e;
     const int mtiles = (int)((g.dstate + 127) / 128);
     dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)g.batch);
-    kern<<<grid, kThreads, p.smem_bytes, st>>>(tm_x, tm_b, tm_cs, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_b, tm_cs, p);
 }
 
 }  // namespace m2

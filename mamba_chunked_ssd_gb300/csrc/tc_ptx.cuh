@@ -94,6 +94,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start before the previous kernel on its stream has
+// finished; griddep_wait() returns once that kernel has completed and its
+// writes are visible (at once when there is no such kernel), so every thread
+// that reads the previous kernel's output calls it first.
+// griddep_launch_dependents() lets the next such kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
