@@ -12,11 +12,14 @@
 //                blocks 0 .. I) and h_c into a ring of stages; its 32 lanes
 //                gather the head's G, dt and D into the same stage with
 //                cp.async, so the epilogue never waits on a global load;
-//   warp 1       TMEM allocator and single-thread tcgen05.mma issuer;
+//   warp 1       TMEM allocator; one thread issues the C B^T products and
+//                the tcgen05.mma of head stream 0;
 //   warps 2..17  epilogue, split into head streams (two when H = 64, one when
 //                H = 128) that take alternate heads, each stream with its own
 //                TMEM accumulators so one stream's arithmetic overlaps the
-//                other's tensor-core work.
+//                other's tensor-core work;
+//   warp 18      one thread issues the tcgen05.mma of head stream 1 (idle with
+//                one stream).
 // Once per CTA (per group, shared by every head):
 //   CB_II = C_I B_I^T -> TMEM, causally masked in place;  for I = 1 also
 //   CB_10 = C_1 B_0^T, converted to bf16 into shared memory as an MMA operand.
