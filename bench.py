@@ -50,6 +50,26 @@ def parse_args():
     return p.parse_args()
 
 
+# ----------------------------------------------------------------- ranks
+def max_over_ranks(value, device="cuda"):
+    """The largest `value` over all ranks of the default process group (the
+    job's time is its slowest rank's); `value` itself with one process.  The
+    only collective of the benchmark: the replicas exchange no data."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms_per_step):
+    """Whole-job throughput: the tokens all ranks processed in one step over
+    the step time of the slowest rank."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 # --------------------------------------------------------------------- work
 def work_counts(w):
     """Algorithmic FLOPs and bytes of one forward pass.
@@ -337,11 +357,7 @@ def run_gpu(args, w, rank, world):
     clock_info = clocks.stop()
     bd.mamba2_check_device_status()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms))
 
     # ---- per-kernel durations: the same launches through the per-stage entry points
     kev = {k: [] for k in ("chunk_cumsum", "state_pass", "chunk_out")}
@@ -420,11 +436,7 @@ def run_gpu(args, w, rank, world):
     barrier()
     e2e_ms = [pipelined(args.steps)]
     bd.mamba2_check_device_status()
-    e2e_total = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
+    e2e_total = max_over_ranks(sum(e2e_ms))
     return {"total_ms": total_ms, "step_ms": step_ms, "kernel_ms": kernel_ms, "clocks": clock_info,
             "e2e_ms": e2e_total, "h2d": h2d, "d2h": d2h, "inp": inp}
 
@@ -447,7 +459,7 @@ def main():
     peaks = load_peaks()
     ms = r["total_ms"] / args.steps
     tokens = w.tokens * world
-    value = tokens / (ms * 1e-3)
+    value = job_tokens_per_s(w.tokens, world, ms)
     kb = kernel_bytes(w)
     top = max(r["kernel_ms"], key=r["kernel_ms"].get)
     achieved = kb[top] / (r["kernel_ms"][top] * 1e-3) / 1e9
