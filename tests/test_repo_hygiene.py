@@ -1,0 +1,54 @@
+"""Repository rules that a reader can check mechanically, on the CPU:
+
+- no committed file refers to the scratch folder `_work/` (scratch tools and
+  experiments stay out of the product, and nothing committed may use them);
+- `profiles/` holds short text summaries only, each giving the full command
+  that produced it, which runs a committed file (`bench.py`).
+
+Skipped when the tree is not a git checkout.
+"""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _tracked():
+    try:
+        out = subprocess.run(["git", "ls-files"], cwd=ROOT, capture_output=True, text=True, timeout=60)
+    except (OSError, subprocess.SubprocessError):
+        pytest.skip("git is not available")
+    if out.returncode != 0:
+        pytest.skip("not a git checkout")
+    return [f for f in out.stdout.splitlines() if f]
+
+
+def test_nothing_committed_uses_the_scratch_folder():
+    pattern = re.compile(r"(^|[^A-Za-z0-9_])_work/")
+    offenders = []
+    for f in _tracked():
+        if f == ".gitignore":
+            continue
+        path = os.path.join(ROOT, f)
+        try:
+            text = open(path, encoding="utf-8").read()
+        except (UnicodeDecodeError, OSError):
+            continue
+        if pattern.search(text):
+            offenders.append(f)
+    assert offenders == []
+
+
+def test_profiles_are_text_summaries_with_their_command():
+    files = [f for f in _tracked() if f.startswith("profiles/")]
+    assert files, "no committed profile summaries"
+    for f in files:
+        assert f.endswith((".md", ".txt")), f
+        path = os.path.join(ROOT, f)
+        assert os.path.getsize(path) < 16 * 1024, f
+        text = open(path, encoding="utf-8").read()
+        assert "Command" in text and "python bench.py" in text, f
+        assert "--clock-control none" in text, f
