@@ -47,6 +47,9 @@ def parse_args():
     p.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     p.add_argument("--cpu-pairs", type=int, default=256,
                    help="(batch, head) pairs the oracle runs for the CPU baseline sample")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the extra workloads (the other configurations and the sweep)")
+    p.add_argument("--extra-steps", type=int, default=10, help="timed steps per extra workload")
     return p.parse_args()
 
 
@@ -206,10 +209,11 @@ def oracle_sample_problem(w, inp, npairs):
     import torch
     pairs = _pick_pairs(w.batch, w.nheads, npairs)
     r = w.nheads // w.ngroups
-    bi = torch.tensor([b for b, _ in pairs])
-    hi = torch.tensor([h for _, h in pairs])
+    dev = inp["x"].device
+    bi = torch.tensor([b for b, _ in pairs], device=dev)
+    hi = torch.tensor([h for _, h in pairs], device=dev)
     gi = hi // r
-    f64 = lambda t: np.ascontiguousarray(t.to(torch.float64).numpy())
+    f64 = lambda t: np.ascontiguousarray(t.cpu().to(torch.float64).numpy())  # noqa: E731
     prob = {
         "x": f64(inp["x"][bi, :, hi].permute(1, 0, 2).unsqueeze(0)),
         "dt": f64(inp["dt"][bi, :, hi].permute(1, 0).unsqueeze(0)),
@@ -359,6 +363,19 @@ def run_gpu(args, w, rank, world):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(sum(step_ms))
 
+    # ---- host time of one call: the public call enqueues the whole pass and
+    # returns; timed on the host clock, without synchronising, over a burst of
+    # calls (the GPU runs behind them)
+    host_us = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(20):
+            step()
+        host_us.append((time.perf_counter() - t0) / 20 * 1e6)
+    torch.cuda.synchronize()
+    host_us_per_call = min(host_us)
+
     # ---- per-kernel durations: the same launches through the per-stage entry points
     kev = {k: [] for k in ("chunk_cumsum", "state_pass", "chunk_out")}
     G = ws[: 4 * w.batch * w.nheads * w.seqlen].view(torch.float32).view(w.batch, w.nheads, w.seqlen)
@@ -383,7 +400,7 @@ def run_gpu(args, w, rank, world):
 
     if args.no_e2e:
         return {"total_ms": total_ms, "step_ms": step_ms, "kernel_ms": kernel_ms, "clocks": clock_info,
-                "e2e_ms": None, "h2d": 0, "d2h": 0, "inp": inp}
+                "e2e_ms": None, "h2d": 0, "d2h": 0, "inp": inp, "host_us": host_us_per_call}
 
     # ---- end to end through the public API with host buffers, pipelined as a
     # server runs it: two sets of device buffers; step i's inputs are copied in
@@ -438,7 +455,60 @@ def run_gpu(args, w, rank, world):
     bd.mamba2_check_device_status()
     e2e_total = max_over_ranks(sum(e2e_ms))
     return {"total_ms": total_ms, "step_ms": step_ms, "kernel_ms": kernel_ms, "clocks": clock_info,
-            "e2e_ms": e2e_total, "h2d": h2d, "d2h": d2h, "inp": inp}
+            "e2e_ms": e2e_total, "h2d": h2d, "d2h": d2h, "inp": inp, "host_us": host_us_per_call}
+
+
+EXTRA_WORKLOADS = ("mamba2_1p3b_layer", "large_state", "blog_example")
+
+
+def run_extra(args, w, peaks, cpu_pairs):
+    """One more workload, measured like the headline one (inputs resident,
+    256 MiB L2 flush before every timed step, CUDA events on the launching
+    stream), with the oracle timed on a small sample of it.  Inputs are drawn
+    on the GPU (different values than the CPU generator, same distributions)."""
+    import torch
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+
+    d = make_inputs(w, device="cuda")
+    shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
+    ws = torch.empty(max(bd.mamba2_ssd_fwd_workspace_size(shape), 1), device="cuda", dtype=torch.uint8)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty(w.batch, w.nheads, w.dstate, w.headdim, device="cuda", dtype=torch.float32)
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size, D=d["D"],
+                          initial_state=d["initial_state"], y=y, final_state=fin, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    ev = []
+    for _ in range(args.extra_steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    bd.mamba2_check_device_status()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    flop, flop_dense, bytes_min = work_counts(w)
+    out = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+           "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk_size": w.chunk_size,
+           "seed": w.seed, "tokens_per_s": w.tokens / (ms * 1e-3), "ms_per_step": ms,
+           "tflops": flop / (ms * 1e-3) / 1e12,
+           "hbm_frac": bytes_min / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+           "tensor_frac": flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], "bytes_min": bytes_min}
+    if cpu_pairs:
+        cb = run_oracle_sample(w, d, min(cpu_pairs, w.batch * w.nheads))
+        out["oracle_tokens_per_s"] = cb["value"]
+        out["oracle_sample"] = f"{min(cpu_pairs, w.batch * w.nheads)} (batch, head) sequences, {cb['cores']} cores"
+    del d, ws, y, fin, flush
+    return out
 
 
 def main():
@@ -482,6 +552,7 @@ def main():
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": load_traffic(top, w.name), "algorithmic_bytes": kb[top]},
         "kernel_ms": r["kernel_ms"],
+        "host_us_per_call": r["host_us"],
         "gpu_launches": 3 * args.steps,
         "e2e": None if r["e2e_ms"] is None else {
             "value": tokens / (r["e2e_ms"] / args.steps * 1e-3), "unit": "tokens/s",
@@ -493,6 +564,12 @@ def main():
     }
     if not args.no_decode and w.seqlen > 1:
         out["decode_step"] = run_decode(args, WORKLOADS["decode_b256"], peaks)
+    if not args.no_extra:
+        from mamba_chunked_ssd_gb300.synthetic import sweep_workloads
+        pairs = 0 if args.no_cpu_baseline else 8
+        out["other_workloads"] = [run_extra(args, WORKLOADS[n], peaks, pairs)
+                                  for n in EXTRA_WORKLOADS if n != w.name]
+        out["sweep"] = [run_extra(args, sw, peaks, 0) for sw in sweep_workloads(seeds=(0,))]
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = run_oracle_sample(w, r["inp"], args.cpu_pairs)
         out["cpu_baseline"].pop("seconds", None)

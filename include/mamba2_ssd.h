@@ -144,9 +144,11 @@ MAMBA2_API mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x
  * process exits), so no workspace is passed and nothing is allocated.
  *  - Problems with mamba2_ssd_fwd_workspace_size(shape) > 32 MiB return
  *    MAMBA2_ERR_UNSUPPORTED with nothing enqueued.
- *  - The first call on a device looks up the array's device address (a
- *    runtime query, no allocation) and caches it; make that first call before
- *    any stream capture on that device.
+ *  - Every call looks up the array's device address on the current device (a
+ *    runtime query, no allocation), so the address is never stale after a
+ *    device reset.  The first call on a device may also load the library's
+ *    device code there; make that first call before any stream capture on
+ *    that device.
  *  - All calls share the one array: calls that overlap on the GPU race on it
  *    and must be ordered by the caller (one stream, or explicit events).  The
  *    array's previous contents never affect a result. */
@@ -181,6 +183,18 @@ MAMBA2_API mamba2_status mamba2_ssd_step(const mamba2_shape* shape, const void* 
                                          const float* A, const void* B, const void* C, const float* D,
                                          const float* state_in, float* state_out, void* y,
                                          struct CUstream_st* stream);
+
+/* Self-test of the bounded device waits (a diagnostic of this library's own
+ * failure handling; the blog has no counterpart).  Enqueues one small kernel
+ * that holds tensor memory and waits on a barrier that nothing ever completes,
+ * with a wall-clock limit of `limit_ns` (1e3 .. 1e8 ns, else
+ * MAMBA2_ERR_INVALID_ARG): the wait runs out, the kernel records
+ * MAMBA2_ERR_TIMEOUT in the current device's status word, a second waiter in
+ * the same kernel leaves through the kernel's abort flag, the tensor memory is
+ * freed and the kernel returns.  The next mamba2_check_device_status therefore
+ * returns MAMBA2_ERR_TIMEOUT (and clears the word); the context stays usable.
+ * Allocates nothing; does not synchronise. */
+MAMBA2_API mamba2_status mamba2_selftest_wait_timeout(int64_t limit_ns, struct CUstream_st* stream);
 
 /* Reads (and clears) the current device's status word.  SYNCHRONISES `stream`.
  * Returns MAMBA2_ERR_TIMEOUT if a kernel's bounded wait ran out since the

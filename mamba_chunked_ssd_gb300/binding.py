@@ -60,6 +60,7 @@ def load_library(path: str = LIB_PATH):
         "mamba2_ssd_fwd": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]),
         "mamba2_ssd_fwd_noalloc": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P]),
         "mamba2_ssd_step": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P]),
+        "mamba2_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, P]),
         "mamba2_check_device_status": (ctypes.c_int, [P]),
         "mamba2_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "mamba2_version": (ctypes.c_int, []),
@@ -222,6 +223,13 @@ def mamba2_ssd_step(x, dt, A, B, C, state_in=None, D=None, state_out=None, y=Non
         ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
         _ptr(state_in), _ptr(state_out), _ptr(y), _stream(stream)))
     return y, state_out
+
+
+def mamba2_selftest_wait_timeout(limit_ns: int, stream=None):
+    """Enqueue the bounded-wait self-test kernel (see the header); the next
+    mamba2_check_device_status then raises with MAMBA2_ERR_TIMEOUT."""
+    _check("mamba2_selftest_wait_timeout",
+           load_library().mamba2_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def mamba2_check_device_status(stream=None):

@@ -3,6 +3,10 @@
 // the forward pass runs in the kernels of the other translation units.
 #include <string.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "common.cuh"
 
 namespace m2 {
@@ -29,6 +33,7 @@ mamba2_status check_shape(const mamba2_shape* s) {
     if (s->headdim > 256 || s->dstate > 256 || s->chunk_size > 256) return MAMBA2_ERR_UNSUPPORTED;
     // grid-dimension and index-range limits of the kernels
     if (s->batch > 65535 || s->nheads > 65535) return MAMBA2_ERR_UNSUPPORTED;
+    if (s->batch * s->nheads >= ((int64_t)1 << 31)) return MAMBA2_ERR_UNSUPPORTED;
     const int64_t lim = (int64_t)1 << 40;
     if (s->seqlen > lim / 1024 || s->batch * s->seqlen > lim / (s->nheads * s->headdim) ||
         s->batch * s->seqlen > lim / (s->ngroups * s->dstate))
@@ -106,6 +111,20 @@ mamba2_status empty_sequence_state(const mamba2_shape& s, const float* init, flo
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace
+
+cudaError_t ensure_max_dynamic_smem(const void* func, int bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> done;  // (device, kernel) -> bytes set
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find({dev, func});
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[{dev, func}] = bytes;
+    return e;
+}
 
 unsigned int* device_status_word() {
     void* p = nullptr;

@@ -114,4 +114,10 @@ cudaError_t launch_chunk_out(const Geom& g, bool bf16, const ChunkOutArgs& a, cu
 // Device address of the current device's status word (api.cu).
 unsigned int* device_status_word();
 
+// Raises `func`'s dynamic shared-memory limit to at least `bytes` on the
+// current device.  The driver call is made once per (device, kernel) and again
+// only when a launch needs more than was set before, so launches do no
+// attribute work on the host (api.cu).
+cudaError_t ensure_max_dynamic_smem(const void* func, int bytes);
+
 }  // namespace m2

@@ -166,10 +166,13 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const Geom& g = p.g;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    const int hb = blockIdx.x % p.head_blocks;
-    const int I = blockIdx.x / p.head_blocks;  // row block inside the chunk
-    const int64_t c = blockIdx.y;
-    const int64_t b = blockIdx.z;
+    // blockIdx.x = hb + head_blocks (I + (T / 128) c): the chunk index rides in
+    // x, whose range (2^31 - 1) covers every chunk count the library accepts
+    const int hb = (int)(blockIdx.x % (unsigned)p.head_blocks);
+    const unsigned rest = blockIdx.x / (unsigned)p.head_blocks;
+    const int I = (int)(rest % (unsigned)(T / 128));  // row block inside the chunk
+    const int64_t c = rest / (unsigned)(T / 128);
+    const int64_t b = blockIdx.y;
     const int64_t t0 = (int64_t)c * T;
     const int tc = (int)imin64(T, g.seqlen - t0);  // valid tokens of the chunk
     if (128 * I >= tc) return;                           // ragged tail: no valid row here
@@ -693,6 +696,8 @@ bool chunk_out_tc_fits(const Geom& g) {
     if (g.dstate != 64 && g.dstate != 128 && g.dstate != 256) return false;
     if (g.batch * g.nheads * g.nchunks * g.dstate >= (int64_t(1) << 31)) return false;
     if (g.batch * g.seqlen >= (int64_t(1) << 31)) return false;
+    // grid.x = head blocks x row blocks x chunks (at most nheads * 2 * nchunks)
+    if (g.nheads * (g.chunk / 128) * g.nchunks >= (int64_t(1) << 31)) return false;
     CoTcParams p;
     return plan_smem(g, p);
 }
@@ -733,9 +738,9 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
     }
     auto kern = (g.headdim == 64) ? (p.T == 256 ? k_chunk_out_tc<64, 256> : k_chunk_out_tc<64, 128>)
                                   : (p.T == 256 ? k_chunk_out_tc<128, 256> : k_chunk_out_tc<128, 128>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
+    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(p.head_blocks * (p.T / 128)), (unsigned)g.nchunks, (unsigned)g.batch);
+    dim3 grid((unsigned)((int64_t)p.head_blocks * (p.T / 128) * g.nchunks), (unsigned)g.batch);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);

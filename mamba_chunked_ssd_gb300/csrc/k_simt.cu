@@ -294,15 +294,13 @@ cudaError_t launch_chunk_out_simt(const Geom& g, bool bf16, const ChunkOutArgs& 
     const size_t smem = sizeof(CoSmem);
     cudaError_t e;
     if (bf16) {
-        e = cudaFuncSetAttribute(k_chunk_out_simt<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(k_chunk_out_simt<__nv_bfloat16>), (int)smem);
         if (e != cudaSuccess) return e;
         k_chunk_out_simt<__nv_bfloat16><<<grid, kThreads, smem, st>>>(
             (const __nv_bfloat16*)a.x, a.dt, (const __nv_bfloat16*)a.B, (const __nv_bfloat16*)a.C,
             a.D, a.G, (const __nv_bfloat16*)a.chunk_states, (__nv_bfloat16*)a.y, g);
     } else {
-        e = cudaFuncSetAttribute(k_chunk_out_simt<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+        e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(k_chunk_out_simt<float>), (int)smem);
         if (e != cudaSuccess) return e;
         k_chunk_out_simt<float><<<grid, kThreads, smem, st>>>(
             (const float*)a.x, a.dt, (const float*)a.B, (const float*)a.C, a.D, a.G,

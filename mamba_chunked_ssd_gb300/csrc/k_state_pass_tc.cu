@@ -427,7 +427,7 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
                                       : (g.chunk == 128 ? k_state_pass_tc<64, 128> : k_state_pass_tc<64, 64>))
                     : (g.chunk == 256 ? k_state_pass_tc<128, 256>
                                       : (g.chunk == 128 ? k_state_pass_tc<128, 128> : k_state_pass_tc<128, 64>));
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
+    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     const int mtiles = (int)((g.dstate + 127) / 128);
     dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)g.batch);

@@ -14,33 +14,22 @@
 // All calls share the one array, so calls that overlap on the GPU (different
 // streams, or different host threads without ordering) race on it.  Nothing in
 // the array needs to start at zero: every byte the pass reads it wrote first.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace {
 
 constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of the array, per device
-
 // The name g_noalloc_scratch is only a host-side stand-in; the array's device
-// address is looked up once per device, with that device current, and cached.
+// address is looked up on every call, with the caller's device current (a
+// runtime query, no allocation), so it is never stale after a cudaDeviceReset
+// or a switch of the current device or context.
 mamba2_status scratch_address(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MAMBA2_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return MAMBA2_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MAMBA2_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MAMBA2_ERR_CUDA;
+    *out = p;
     return MAMBA2_OK;
 }
 

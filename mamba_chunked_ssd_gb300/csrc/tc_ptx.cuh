@@ -80,16 +80,19 @@ constexpr uint64_t kWaitLimitNs = 500000000ull;        // 0.5 s of wall clock
 constexpr long long kWaitLimitCycles = 4000000000ll;   // ~2 s of SM clock, a backstop
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// gives up) once the wait has lasted kWaitLimitNs (or kWaitLimitCycles SM
-// cycles, whichever comes first) or `abort` became non-zero.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// gives up) once the wait has lasted limit_ns of wall clock (kWaitLimitNs
+// unless a caller passes a shorter limit), or kWaitLimitCycles SM cycles,
+// whichever comes first, or once `abort` became non-zero.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t hint = limit_ns < 100000u ? (uint32_t)limit_ns : 100000u;  // at most 0.1 ms per try
     const uint64_t t0 = globaltimer_ns();
     const long long c0 = clock64();
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;  // sleep up to 0.1 ms per try
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
         if (clock64() - c0 > kWaitLimitCycles) return false;
     }
 }

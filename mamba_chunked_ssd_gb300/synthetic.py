@@ -12,7 +12,10 @@ Distributions (per workload description):
   D ~ N(0, 1) per head, fp32;
   initial_state ~ N(0, 0.1) fp32 when the workload carries a state, else None.
 Draws come from one ``torch.Generator`` seeded per call, in the fixed order
-x, dt, A, B, C, D, initial_state.
+x, dt, A, B, C, D, initial_state.  By default the generator runs on the CPU
+(the same values on every machine); ``device="cuda"`` draws on the GPU instead,
+which is much faster for the large sweep shapes (different values for the same
+seed, but still one seeded draw that both sides of a comparison share).
 """
 from __future__ import annotations
 
@@ -60,6 +63,9 @@ WORKLOADS = {
     # one decode step (seqlen 1) for 256 sequences of the same layer, each
     # carrying a state: the inference use of the carried final state
     "decode_b256": Workload("decode_b256", 256, 1, 64, 64, 128, 1, 1, init_state=True),
+    # the example problem the blog's usage snippet times: batch 4, 16384
+    # tokens, one group, 8 heads, state 128, head dim 64, chunk 128
+    "blog_example": Workload("blog_example", 4, 16384, 8, 64, 128, 1, 128),
 }
 
 
@@ -79,20 +85,21 @@ def sweep_workloads(seeds=(0, 1, 2)):
 TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 
 
-def make_inputs(w: Workload, seed: int | None = None) -> dict:
-    """Draw the inputs of workload ``w`` on the CPU.
+def make_inputs(w: Workload, seed: int | None = None, device: str = "cpu") -> dict:
+    """Draw the inputs of workload ``w`` on ``device`` (CPU by default).
 
-    Returns a dict of CPU tensors: x [b,L,nh,H], dt [b,L,nh], A [nh],
-    B, C [b,L,G,S], D [nh], initial_state [b,nh,S,H] or None."""
-    g = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    Returns a dict of tensors on that device: x [b,L,nh,H], dt [b,L,nh],
+    A [nh], B, C [b,L,G,S], D [nh], initial_state [b,nh,S,H] or None."""
+    g = torch.Generator(device=device).manual_seed(w.seed if seed is None else seed)
     dt_ = TORCH_DTYPES[w.dtype]
     b, L, nh, H, S, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
-    x = torch.randn(b, L, nh, H, generator=g).to(dt_)
-    dt = torch.nn.functional.softplus(torch.randn(b, L, nh, generator=g) + w.dt_mu)
+    kw = {"generator": g, "device": device}
+    x = torch.randn(b, L, nh, H, **kw).to(dt_)
+    dt = torch.nn.functional.softplus(torch.randn(b, L, nh, **kw) + w.dt_mu)
     dt = dt.clamp_(1e-3, 0.1).float()
-    A = -torch.exp(torch.rand(nh, generator=g) * math.log(16.0)).float()
-    B = torch.randn(b, L, G, S, generator=g).to(dt_)
-    C = torch.randn(b, L, G, S, generator=g).to(dt_)
-    D = torch.randn(nh, generator=g).float()
-    init = (torch.randn(b, nh, S, H, generator=g) * 0.1).float() if w.init_state else None
+    A = -torch.exp(torch.rand(nh, **kw) * math.log(16.0)).float()
+    B = torch.randn(b, L, G, S, **kw).to(dt_)
+    C = torch.randn(b, L, G, S, **kw).to(dt_)
+    D = torch.randn(nh, **kw).float()
+    init = (torch.randn(b, nh, S, H, **kw) * 0.1).float() if w.init_state else None
     return {"x": x, "dt": dt, "A": A, "B": B, "C": C, "D": D, "initial_state": init}

@@ -19,7 +19,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = bd.header_functions()
-    assert len(names) == 10
+    assert len(names) == 11
     for n in names:
         assert hasattr(lib, n), f"{n} declared in the header but not exported"
 
@@ -142,3 +142,9 @@ def test_step_rejects_y_over_state(lib):
 
 def test_step_rejects_misaligned(lib):
     assert _step(lib, _shape(seqlen=1), x=FAKE + 8) == INVALID
+
+
+@pytest.mark.parametrize("limit", [0, 999, 100000001, -5])
+def test_selftest_rejects_out_of_range_limits(lib, limit):
+    """Checked on the host: nothing is launched for a bad limit."""
+    assert lib.mamba2_selftest_wait_timeout(limit, None) == INVALID

@@ -71,11 +71,19 @@ def test_kernel_bytes_bench_workload():
 
 @pytest.mark.parametrize("kernel", ["chunk_out", "state_pass", "chunk_cumsum"])
 def test_traffic_link_follows_the_committed_summary(kernel):
+    """The recorded DRAM bytes while the kernel source still has the hash the
+    summary names; None (no traffic claim) once the source has changed."""
+    import hashlib
     t = bench.load_traffic(kernel, "long_seq_carried_state")
-    assert t is not None and t > 0
     path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_long_seq_carried_state.md")
-    recorded = [ln for ln in open(path) if ln.startswith("traffic_bytes_per_launch:")]
-    assert float(recorded[0].split(":")[1]) == t
+    fields = dict(ln.split(":", 1) for ln in open(path)
+                  if ln.startswith(("traffic_bytes_per_launch:", "source:", "source_sha256_16:")))
+    src = os.path.join(ROOT, fields["source"].strip())
+    same = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == fields["source_sha256_16"].strip()
+    if same:
+        assert t == float(fields["traffic_bytes_per_launch"])
+    else:
+        assert t is None
 
 
 def test_traffic_link_drops_when_the_source_changes(tmp_path, monkeypatch):
@@ -83,10 +91,14 @@ def test_traffic_link_drops_when_the_source_changes(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
     src_dir = tmp_path / "mamba_chunked_ssd_gb300" / "csrc"
     src_dir.mkdir(parents=True)
-    summary = os.path.join(ROOT, "profiles", "ncu_chunk_out_long_seq_carried_state.md")
-    shutil.copy(summary, tmp_path / "profiles")
+    import hashlib
     src = os.path.join(ROOT, "mamba_chunked_ssd_gb300", "csrc", "k_chunk_out_tc.cu")
     shutil.copy(src, src_dir)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    with open(tmp_path / "profiles" / "ncu_chunk_out_long_seq_carried_state.md", "w") as f:
+        f.write("# summary\n\ntraffic_bytes_per_launch: 12345\n"
+                "source: mamba_chunked_ssd_gb300/csrc/k_chunk_out_tc.cu\n"
+                f"source_sha256_16: {sha}\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.load_traffic("chunk_out", "long_seq_carried_state") is not None
     with open(src_dir / "k_chunk_out_tc.cu", "a") as f:

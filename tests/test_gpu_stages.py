@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, np64, rel_err, to_dev
+from gpu_helpers import TOL, np64, rel_err, strong_decay, to_dev
 from mamba_chunked_ssd_gb300 import binding as bd
 from mamba_chunked_ssd_gb300.synthetic import Workload, make_inputs
 
@@ -52,10 +52,12 @@ def test_chunk_cumsum_matches_oracle(spec):
     assert err.max() <= 1e-5, err.max()
 
 
-def test_chunk_cumsum_bit_exact_layout():
+@pytest.mark.parametrize("nh", [37, 36, 64])
+def test_chunk_cumsum_bit_exact_layout(nh):
     """With A a power of two and dt on a 2^-12 grid every partial sum is exact
-    in fp32, so G = fl(sum * log2e) exactly: any indexing or layout slip shows."""
-    b, L, nh, T = 2, 300, 37, 64
+    in fp32, so G = fl(sum * log2e) exactly: any indexing or layout slip shows.
+    A head count divisible by 4 takes the 16-byte load path, 37 the scalar one."""
+    b, L, T = 2, 300, 64
     g = torch.Generator().manual_seed(5)
     dt = (torch.randint(1, 64, (b, L, nh), generator=g).float() / 4096.0)
     A = torch.tensor([-(2.0 ** (k % 3)) for k in range(nh)], dtype=torch.float32)
@@ -159,3 +161,36 @@ def test_chunk_out_single_term(spec, term):
     y_ref = oracle.chunk_out(inp["x"], inp["dt"], inp["B"], inp["C"], G32, cs_dev.cpu(), w.chunk_size,
                              D=inp["D"])
     assert rel_err(np64(y), y_ref) <= TOL[w.dtype]
+
+
+# Tensor-core shapes of stages 2 and 3 (both row blocks of a 256-token chunk,
+# both head-dim variants) fed decay rates far beyond the split-decay range.
+STRONG = [
+    ("strong_t256", 2, 512, 6, 64, 128, 1, 256, "bf16", True),
+    ("strong_t128_h128", 1, 384, 6, 128, 256, 2, 128, "bf16", True),
+    ("strong_t256_ragged", 1, 600, 6, 64, 64, 3, 256, "bf16", False),
+]
+
+
+@pytest.mark.parametrize("spec", STRONG, ids=[s[0] for s in STRONG])
+def test_stages_under_strong_decay(spec):
+    """Stage 2 and stage 3 each against the oracle (stage 3 given the oracle's
+    states) with decays that leave the split-decay range: the direct-weight
+    rows, mixed warps, the weight clamp and underflowing decays all run."""
+    w = _w(*spec)
+    inp = strong_decay(make_inputs(w))
+    d = to_dev(inp)
+    G32, cs_ref, fin_ref = _oracle_stage_inputs(inp, w)
+    Gd = torch.from_numpy(G32).cuda()
+    cs, fin = bd.mamba2_state_pass(d["x"], d["dt"], d["B"], Gd, w.chunk_size, initial_state=d["initial_state"])
+    bd.mamba2_check_device_status()
+    assert rel_err(np64(cs), cs_ref) <= TOL[w.dtype]
+    assert rel_err(np64(fin), fin_ref) <= TOL[w.dtype]
+    cs_dev = torch.from_numpy(cs_ref).to(d["x"].dtype).cuda()
+    y = bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], Gd, cs_dev, w.chunk_size, D=d["D"])
+    bd.mamba2_check_device_status()
+    y_ref = oracle.chunk_out(inp["x"], inp["dt"], inp["B"], inp["C"], G32, cs_dev.cpu(), w.chunk_size,
+                             D=inp["D"])
+    assert torch.isfinite(y.float()).all()
+    for h in range(w.nheads):
+        assert rel_err(np64(y[:, :, h]), y_ref[:, :, h]) <= TOL[w.dtype], h
