@@ -41,6 +41,8 @@
 // entries are zero in CB before any weight multiplies them.  The T x T matrix
 // never reaches global memory.
 // Every wait is bounded; a timeout sets the status word and the CTA unwinds.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap_host.cuh"
@@ -154,9 +156,14 @@ __device__ __forceinline__ void scale_row4(uint8_t* base, uint32_t box_stride, i
     for (int t = 0; t < 4; ++t) *reinterpret_cast<uint4*>(rowp + (((c0 + t) & 7) << 4)) = v[t];
 }
 
-// H (head dim) and T (chunk) are compile-time, so the stream / part / box
-// counts and most swizzle offsets fold into constants.
-template <int H, int T>
+// H (the head width one MMA covers) and T (chunk) are compile-time, so the
+// stream / part / box counts and most swizzle offsets fold into constants.
+// VS = 2 splits every head of width 2 H into two virtual heads of width H that
+// share the head's decays (its P is formed once per virtual head): the stages
+// then hold half of the head's X and h_c, which lets a head of 128 columns
+// with a 256-wide state and a 256-token chunk fit, and gives such heads two
+// streams.  VS = 1: virtual and real heads coincide.
+template <int H, int T, int VS>
 __global__ void __launch_bounds__(kThreads, 1)
 k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_h,
@@ -177,6 +184,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const int tc = (int)imin64(T, g.seqlen - t0);  // valid tokens of the chunk
     if (128 * I >= tc) return;                           // ragged tail: no valid row here
     const int h0 = hb * p.nhb;
+    const int nvh = p.nhb * VS;  // virtual heads of this CTA
     const int grp = (int)(h0 / g.heads_per_group);
     const int Tj = 128 * (I + 1);  // columns j that rows of block I can see
     const int S = (int)g.dstate;
@@ -244,7 +252,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // stage, its reuse phase and the fill barrier as counters (no divisions)
         int st = 0, fill = 0;
         uint32_t slot_phase = 1;  // phase of the previous use of the stage
-        for (int k = 0; ok && k < p.nhb; ++k) {
+        for (int k = 0; ok && k < nvh; ++k) {
             if (k >= lay.nst) {
                 bool w_ok = true;
                 if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], slot_phase, abort_flag);
@@ -258,14 +266,15 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             float* vG = reinterpret_cast<float*>(sX + lay.off_vec_in_stage);  // G[T], dt[T], D
             float* vDt = vG + T;
             uint64_t* full = &bars[kBarFull + fill];
-            const int h = h0 + k;
+            const int h = h0 + k / VS;          // real head
+            const int col0 = (k % VS) * H;      // its first column in this virtual head
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(full, x_bytes + h_bytes);
                 for (int cb = 0; cb < H / 64; ++cb) {
                     for (int rb = 0; rb < Tj / 128; ++rb)
-                        tc::tma_load_4d(sX + cb * (Tj * 128) + rb * 16384, &tm_x, full, cb * 64, h,
+                        tc::tma_load_4d(sX + cb * (Tj * 128) + rb * 16384, &tm_x, full, col0 + cb * 64, h,
                                         (int)(t0 + 128 * rb), (int)b);
-                    tc::tma_load_2d(sH + cb * (S * 128), &tm_h, full, cb * 64,
+                    tc::tma_load_2d(sH + cb * (S * 128), &tm_h, full, col0 + cb * 64,
                                     (int)(((b * g.nheads + h) * g.nchunks + c) * S));
                 }
             }
@@ -325,7 +334,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             int st = sid0 % lay.nst, fill = sid0 % lay.nfill;
             uint32_t fill_phase = (sid0 / lay.nfill) & 1;
             uint64_t dstage = st * stage_step;  // stage offset, in descriptor units
-            for (int k = sid0; ok && k < p.nhb; k += nstr) {
+            for (int k = sid0; ok && k < nvh; k += nstr) {
                 const int s = k % nstr, n = k / nstr;
                 const uint32_t tz = tmem + col_z(s, H), ty2 = tz + H;
                 if (!tc::mbar_wait(&bars[kBarFull + fill], fill_phase, abort_flag)) { ok = false; break; }
@@ -440,7 +449,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // stage and fill barrier of head k as counters, advanced by nstr heads
         int st = sid % lay.nst, fill = sid % lay.nfill;
         uint32_t fill_phase = (sid / lay.nfill) & 1;
-        for (int k = sid; k < p.nhb; k += nstr) {
+        for (int k = sid; k < nvh; k += nstr) {
             const int n = k / nstr;
             if (ok) ok = tc::mbar_wait(&bars[kBarFull + fill], fill_phase, abort_flag);
             uint8_t* sX = sStage + st * lay.stage_bytes;
@@ -606,7 +615,8 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             asm volatile("bar.sync %0, %1;" ::"r"(2 + sid), "r"(wps * 32) : "memory");
             if (stream_leader && ok) {
                 for (int cb = 0; cb < H / 64; ++cb)
-                    tc::tma_store_4d(&tm_y, sX + cb * (Tj * 128) + I * 16384, cb * 64, h0 + k, (int)(t0 + 128 * I),
+                    tc::tma_store_4d(&tm_y, sX + cb * (Tj * 128) + I * 16384, (k % VS) * H + cb * 64, h0 + k / VS,
+                                     (int)(t0 + 128 * I),
                                      (int)b);
                 tc::bulk_commit();
                 tc::bulk_wait_read_all();
@@ -634,9 +644,11 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     }
 }
 
-int pick_heads_per_cta(const Geom& g) {
+// Real heads per CTA: the largest divisor of the heads per group with at most
+// 16 virtual heads.
+int pick_heads_per_cta(const Geom& g, int vs) {
     const int r = (int)g.heads_per_group;
-    for (int n = 16; n >= 1; --n)
+    for (int n = 16 / vs; n >= 1; --n)
         if (r % n == 0) return n;
     return 1;
 }
@@ -647,8 +659,8 @@ int lcm_small(int a, int b) {
     return m;
 }
 
-bool plan_layout(const Geom& g, int I, int nstr, uint32_t off_CB10, CoLayout& L) {
-    const int T = (int)g.chunk, S = (int)g.dstate, H = (int)g.headdim, Tj = 128 * (I + 1);
+bool plan_layout(const Geom& g, int I, int vs, int nstr, uint32_t off_CB10, CoLayout& L) {
+    const int T = (int)g.chunk, S = (int)g.dstate, H = (int)g.headdim / vs, Tj = 128 * (I + 1);
     L.off_stage = off_CB10 + (I == 1 ? 32768u : 0u);
     L.off_h_in_stage = (uint32_t)(Tj * H * 2);
     L.off_vec_in_stage = L.off_h_in_stage + (uint32_t)(S * H * 2);
@@ -674,17 +686,44 @@ bool plan_layout(const Geom& g, int I, int nstr, uint32_t off_CB10, CoLayout& L)
     return false;
 }
 
-bool plan_smem(const Geom& g, CoTcParams& p) {
-    p.nstr = (g.headdim == 64) ? 2 : 1;
+// Shared-memory plan for virtual-head split vs (1, or 2 for 128-wide heads).
+bool plan_smem(const Geom& g, int vs, CoTcParams& p) {
+    if (vs != 1 && !(vs == 2 && g.headdim == 128)) return false;
+    p.nstr = (g.headdim / vs == 64) ? 2 : 1;
     p.off_C = 0;
     p.off_CB10 = p.off_C + 128 * (uint32_t)g.dstate * 2;
     p.smem_bytes = 0;
     for (int I = 0; I < (int)(g.chunk / 128); ++I) {
-        if (!plan_layout(g, I, p.nstr, p.off_CB10, p.lay[I])) return false;
+        if (!plan_layout(g, I, vs, p.nstr, p.off_CB10, p.lay[I])) return false;
         if (p.lay[I].smem_bytes > p.smem_bytes) p.smem_bytes = p.lay[I].smem_bytes;
     }
     if (g.chunk == 128) p.lay[1] = p.lay[0];  // unused
     return true;
+}
+
+// The virtual-head split used for a shape (0: none fits).  Heads stay whole
+// when every row block gets at least two pipeline stages; otherwise a head of
+// 128 columns is split in two (which halves a stage), and only if that does not
+// fit either do whole heads run with one stage.  Measured on GB300 (stage-3
+// time, whole vs split, µs): state 64: 522 vs 575 (chunk 128), 604 vs 658
+// (chunk 256); state 128: 563 vs 600 (128), 855 vs 722 (256, one stage whole);
+// state 256: 962 vs 737 (128, one stage whole), split only at chunk 256.
+// MAMBA2_CHUNK_OUT_HEAD_SPLIT=1 or =2 forces that variant, for timing both on
+// one shape; where the forced variant does not fit, stage 3 runs on the
+// CUDA-core kernel.
+int pick_vs(const Geom& g) {
+    CoTcParams p;
+    const char* env = getenv("MAMBA2_CHUNK_OUT_HEAD_SPLIT");
+    if (env && (env[0] == '1' || env[0] == '2') && env[1] == 0) {
+        const int want = env[0] - '0';
+        return plan_smem(g, want, p) ? want : 0;
+    }
+    const bool whole = plan_smem(g, 1, p);
+    bool deep = whole;
+    for (int I = 0; whole && I < (int)(g.chunk / 128); ++I) deep = deep && p.lay[I].nst >= 2;
+    if (deep) return 1;
+    if (plan_smem(g, 2, p)) return 2;
+    return whole ? 1 : 0;
 }
 
 }  // namespace
@@ -698,16 +737,16 @@ bool chunk_out_tc_fits(const Geom& g) {
     if (g.batch * g.seqlen >= (int64_t(1) << 31)) return false;
     // grid.x = head blocks x row blocks x chunks (at most nheads * 2 * nchunks)
     if (g.nheads * (g.chunk / 128) * g.nchunks >= (int64_t(1) << 31)) return false;
-    CoTcParams p;
-    return plan_smem(g, p);
+    return pick_vs(g) != 0;
 }
 
 cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream_t st) {
     CoTcParams p{};
     p.g = g;
     p.T = (int)g.chunk;
-    if (!plan_smem(g, p)) return cudaErrorInvalidConfiguration;
-    p.nhb = pick_heads_per_cta(g);
+    const int vs = pick_vs(g);
+    if (vs == 0 || !plan_smem(g, vs, p)) return cudaErrorInvalidConfiguration;
+    p.nhb = pick_heads_per_cta(g, vs);
     p.head_blocks = (int)(g.nheads / p.nhb);
     p.dt = a.dt;
     p.G = a.G;
@@ -736,8 +775,10 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
         const uint32_t box[2] = {64, (uint32_t)S};
         if (!make_tmap_bf16(&tm_h, a.chunk_states, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    auto kern = (g.headdim == 64) ? (p.T == 256 ? k_chunk_out_tc<64, 256> : k_chunk_out_tc<64, 128>)
-                                  : (p.T == 256 ? k_chunk_out_tc<128, 256> : k_chunk_out_tc<128, 128>);
+    auto kern = (g.headdim == 64)
+                    ? (p.T == 256 ? k_chunk_out_tc<64, 256, 1> : k_chunk_out_tc<64, 128, 1>)
+                    : (vs == 2 ? (p.T == 256 ? k_chunk_out_tc<64, 256, 2> : k_chunk_out_tc<64, 128, 2>)
+                               : (p.T == 256 ? k_chunk_out_tc<128, 256, 1> : k_chunk_out_tc<128, 128, 1>));
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((int64_t)p.head_blocks * (p.T / 128) * g.nchunks), (unsigned)g.batch);

@@ -1,0 +1,111 @@
+"""Times the alternatives behind the library's per-shape kernel choices.
+
+The library picks, per problem shape, among kernels that all compute the same
+result (host dispatch in csrc/dispatch.cu and the launchers).  Where a choice
+has more than one candidate that fits, an environment override forces one of
+them, and this tool times each candidate on the GPU so the dispatch rule can
+be checked against measurements:
+
+  MAMBA2_CHUNK_OUT_HEAD_SPLIT = 1 | 2   stage 3 with heads of 128 columns
+      whole (one 128-wide MMA per head) or split into two 64-wide virtual
+      heads sharing the head's decays; a forced variant that does not fit
+      runs stage 3 on the CUDA-core kernel instead (its time is shown).
+
+Usage (one GPU):  python -m mamba_chunked_ssd_gb300.tune [--steps K] [--json]
+Each line: workload, candidate, mean stage time in microseconds (CUDA events
+on the launching stream, a 256 MiB L2 flush before every timed launch), and
+the candidate the default rule picks.  Inputs are seeded synthetic tensors
+drawn on the GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FLUSH_BYTES = 256 << 20
+HEAD_SPLIT_ENV = "MAMBA2_CHUNK_OUT_HEAD_SPLIT"
+
+
+def _time(fn, steps, warmup, flush, stream):
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    ev = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+
+
+def head_split_rows(workloads, steps=10, warmup=3):
+    """Stage-3 time of every candidate head split, per workload with 128-wide
+    heads (others have one candidate)."""
+    import torch
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+
+    bd.load_library()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    rows = []
+    saved = os.environ.pop(HEAD_SPLIT_ENV, None)
+    try:
+        for w in workloads:
+            if w.headdim != 128 or w.dtype != "bf16":
+                continue
+            d = make_inputs(w, device="cuda")
+            G = bd.mamba2_chunk_cumsum(d["dt"], d["A"], w.chunk_size)
+            cs, _ = bd.mamba2_state_pass(d["x"], d["dt"], d["B"], G, w.chunk_size,
+                                         initial_state=d["initial_state"], want_final_state=False)
+            y = torch.empty_like(d["x"])
+            fn = lambda: bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], G, cs, w.chunk_size,  # noqa: E731
+                                             D=d["D"], y=y)
+            times = {}
+            for cand in ("1", "2"):
+                os.environ[HEAD_SPLIT_ENV] = cand
+                times[cand] = _time(fn, steps, warmup, flush, stream)
+            os.environ.pop(HEAD_SPLIT_ENV, None)
+            default_us = _time(fn, steps, warmup, flush, stream)
+            bd.mamba2_check_device_status()
+            rows.append({"workload": w.name, "seqlen": w.seqlen, "dstate": w.dstate, "headdim": w.headdim,
+                         "chunk_size": w.chunk_size, "whole_us": times["1"], "split_us": times["2"],
+                         "default_us": default_us})
+            del d, G, cs, y
+    finally:
+        if saved is not None:
+            os.environ[HEAD_SPLIT_ENV] = saved
+    return rows
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--json", action="store_true")
+    args = ap.parse_args()
+    from mamba_chunked_ssd_gb300.synthetic import WORKLOADS, sweep_workloads
+    ws = [WORKLOADS["large_state"]] + sweep_workloads(seeds=(0,))
+    rows = head_split_rows(ws, steps=args.steps)
+    if args.json:
+        print(json.dumps(rows))
+        return
+    print("| workload | whole heads (µs) | split heads (µs) | default (µs) |")
+    print("|---|---|---|---|")
+    for r in rows:
+        print(f"| {r['workload']} | {r['whole_us']:.1f} | {r['split_us']:.1f} | {r['default_us']:.1f} |")
+
+
+if __name__ == "__main__":
+    main()

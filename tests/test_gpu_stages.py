@@ -194,3 +194,34 @@ def test_stages_under_strong_decay(spec):
     assert torch.isfinite(y.float()).all()
     for h in range(w.nheads):
         assert rel_err(np64(y[:, :, h]), y_ref[:, :, h]) <= TOL[w.dtype], h
+
+
+# Heads of 128 columns in stage 3: whole (one 128-wide MMA per head) or split
+# into two 64-wide virtual heads; the override selects the variant where it
+# fits, and both must match the oracle.  State 256 with chunk 256 fits only
+# split.
+SPLIT = [
+    ("h128_t128_s256", 1, 384, 4, 128, 256, 2, 128, "bf16", True),
+    ("h128_t256_s128", 2, 512, 2, 128, 128, 1, 256, "bf16", False),
+    ("h128_t256_s256_ragged", 1, 700, 3, 128, 256, 1, 256, "bf16", True),
+    ("h128_t128_s64_groups", 2, 300, 8, 128, 64, 2, 128, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("variant", ["1", "2"])
+@pytest.mark.parametrize("spec", SPLIT, ids=[s[0] for s in SPLIT])
+def test_chunk_out_head_split_variants(spec, variant, monkeypatch):
+    monkeypatch.setenv("MAMBA2_CHUNK_OUT_HEAD_SPLIT", variant)
+    w = _w(*spec)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    G32, cs_ref, _ = _oracle_stage_inputs(inp, w)
+    cs_dev = torch.from_numpy(cs_ref).to(d["x"].dtype).cuda()
+    y = bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], torch.from_numpy(G32).cuda(), cs_dev,
+                            w.chunk_size, D=d["D"])
+    bd.mamba2_check_device_status()
+    y_ref = oracle.chunk_out(inp["x"], inp["dt"], inp["B"], inp["C"], G32, cs_dev.cpu(), w.chunk_size,
+                             D=inp["D"])
+    assert rel_err(np64(y), y_ref) <= TOL[w.dtype]
+    for h in range(w.nheads):
+        assert rel_err(np64(y[:, :, h]), y_ref[:, :, h]) <= TOL[w.dtype], h
