@@ -222,6 +222,12 @@ mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const flo
     void* cs = ws + round_up(z.G, 256);
     const Geom g = make_geom(*shape);
     if ((rc = from_cuda(launch_chunk_cumsum(g, dt, A, G, st))) != MAMBA2_OK) return rc;
+    if (use_fused_forward(g, shape->dtype == MAMBA2_BF16)) {
+        // stages 2 and 3 in one kernel: the carried states stay on the chip
+        FusedArgs fa{x, dt, B, C, D, G, initial_state, y, final_state};
+        fa.pdl = true;
+        return from_cuda(launch_ssd_fused(g, fa, st));
+    }
     // stages 2 and 3 may start while the stage before them runs (programmatic
     // dependent launch); they wait for it before reading its output
     StatePassArgs sp{x, dt, B, G, initial_state, cs, final_state};

@@ -93,6 +93,21 @@ struct SsdStepArgs {
     void* y;
 };
 
+// The fused state pass + chunk output (k_ssd_fused_tc.cu): y and the final
+// state straight from x, dt, B, C, D, G and the initial state.
+struct FusedArgs {
+    const void* x;
+    const float* dt;
+    const void* B;
+    const void* C;
+    const float* D;     // may be null
+    const float* G;
+    const float* init;  // may be null
+    void* y;
+    float* final_state;  // may be null
+    bool pdl = false;    // may start while stage 1 runs
+};
+
 cudaError_t launch_chunk_cumsum(const Geom& g, const float* dt, const float* A, float* G,
                                 cudaStream_t st);
 cudaError_t launch_state_pass_simt(const Geom& g, bool bf16, const StatePassArgs& a, cudaStream_t st);
@@ -106,10 +121,16 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
 bool state_pass_tc_fits(const Geom& g);
 cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStream_t st);
 
+bool ssd_fused_fits(const Geom& g);
+cudaError_t launch_ssd_fused(const Geom& g, const FusedArgs& a, cudaStream_t st);
+
 // Dispatchers: pick the tensor-core kernel when the shape has one, else the
 // CUDA-core kernel (dispatch.cu).
 cudaError_t launch_state_pass(const Geom& g, bool bf16, const StatePassArgs& a, cudaStream_t st);
 cudaError_t launch_chunk_out(const Geom& g, bool bf16, const ChunkOutArgs& a, cudaStream_t st);
+// Whether mamba2_ssd_fwd runs the fused kernel after stage 1 for this shape
+// (else stages 2 and 3 separately).
+bool use_fused_forward(const Geom& g, bool bf16);
 
 // Device address of the current device's status word (api.cu).
 unsigned int* device_status_word();

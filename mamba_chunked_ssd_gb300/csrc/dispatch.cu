@@ -1,4 +1,7 @@
 // dispatch.cu — chooses the kernel that runs each stage for a given shape.
+#include <stdlib.h>
+#include <string.h>
+
 #include "common.cuh"
 
 namespace m2 {
@@ -11,6 +14,18 @@ cudaError_t launch_state_pass(const Geom& g, bool bf16, const StatePassArgs& a, 
 cudaError_t launch_chunk_out(const Geom& g, bool bf16, const ChunkOutArgs& a, cudaStream_t st) {
     if (bf16 && chunk_out_tc_fits(g)) return launch_chunk_out_tc(g, a, st);
     return launch_chunk_out_simt(g, bf16, a, st);
+}
+
+// The fused kernel keeps one CTA per pair of heads of a batch row on the chip
+// for the whole sequence.  Measured on GB300 it is still slower than the
+// separate stages (long-sequence workload: 0.42 ms against 0.31 ms per pass),
+// so the separate stages stay the default.  MAMBA2_FWD_PATH=fused or =staged
+// forces a path (fused only where it fits), for testing and for timing both on
+// one shape.
+bool use_fused_forward(const Geom& g, bool bf16) {
+    if (!bf16 || !ssd_fused_fits(g)) return false;
+    const char* env = getenv("MAMBA2_FWD_PATH");
+    return env && strcmp(env, "fused") == 0;
 }
 
 }  // namespace m2
