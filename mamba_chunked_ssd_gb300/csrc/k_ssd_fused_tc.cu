@@ -18,30 +18,32 @@
 // token.  Per block, with the pair's two heads a and b side by side as N:
 //   CB  = C B^T                        tcgen05, 128 x 128, K = state
 //   Z   = C [h_a | h_b]                tcgen05, N = 128; h in bf16 from the scan
-//   Z  <- exp2(G_i - G_s) Z            epilogue warps, in TMEM
-//   P'  = CB . u_i w_j (causal)        P warps, to TMEM as bf16, per head
-//   Y   = Z + P' X                     tcgen05 accumulating onto Z, A from TMEM
-//   y   = Y + D x                      epilogue
+//   Z  <- f_i Z                        epilogue warps, in TMEM
+//   P   = CB . w (causal)              P warps, to TMEM as bf16, per head
+//   Y   = Z + P X                      tcgen05 accumulating onto Z, A from TMEM
+//   y   = u_i Y + D x                  epilogue
 //   h  <- exp2(G_l - G_s) h + B^T [w_a . X_a | w_b . X_b]    scan, then tcgen05
 // The decay of each P row is split at the column r before its 32-row quadrant:
 // exp2(G_i - G_j) dt_j = u_i w_j, u_i = exp2(G_i - G_r) <= 1, w_j =
-// exp2(G_r - G_j) dt_j; rows whose u_i would fall below 2^-96 take
-// exp2(G_i - G_j) dt_j per entry.  Because P' carries its whole row factor and
-// Z is rescaled in place, the output needs one accumulator, so the C B^T
-// product of the next block can start as soon as this block's P' is formed.
-// Roles (21 warps):
+// exp2(G_r - G_j) dt_j, and exp2(G_i - G_s) = u_i exp2(G_r - G_s); so for such
+// rows f_i = exp2(G_r - G_s) <= 1 and u_i Y = exp2(G_i - G_s) Z + (exact P) X.
+// Rows whose u_i would fall below 2^-96 take exp2(G_i - G_j) dt_j per entry,
+// f_i = exp2(G_i - G_s) and u_i = 1.  With Z rescaled in place the output needs
+// one accumulator, so the C B^T product of the next block can start as soon as
+// this block's P warps have read CB.  Roles (30 warps):
 //   warp 0      X producer: TMA of both heads' X block into a double buffer;
-//               its lanes gather G, dt, D and G_s of both heads by cp.async
-//   warp 1      TMEM allocator; issues CB and head a's P' X
+//               its lanes gather G, dt, D and G_s of both heads by cp.async;
+//               before refilling a buffer it stores the y the epilogue wrote
+//               over that buffer's X (TMA store)
+//   warp 1      TMEM allocator; issues CB and the TMA loads of C (one buffer)
+//               and B (two buffers)
 //   warp 2      issues Z and the state update (the state chain)
-//   warp 3      C producer (one buffer) and B producer (two buffers), TMA
-//   warps 4-11  P' formation: head a (4-7) and head b (8-11), one TMEM lane
-//               quadrant each
-//   warps 12-15 epilogue: Z rescaling, then y written over X in shared memory
-//               and stored with TMA
-//   warps 16-19 scan, then fold: h -> bf16 tile for Z and h <- exp2(G_l - G_s) h
+//   warp 3      issues P X of head a, then of head b
+//   warps 4-19  P formation: (head, column half, TMEM lane quadrant); the
+//               first half covers column groups 0-1, the second groups 2-3
+//   warps 20-23 epilogue: Z rescaling, then y written over X in shared memory
+//   warps 24-27 scan, then fold: h -> bf16 tile for Z and h <- exp2(G_l - G_s) h
 //               in TMEM; once Z has read that tile, w . X into the same buffer
-//   warp 20     issues head b's P' X
 // Tensor memory (512 columns): CB fp32 [0,128), Z / Y [128,256) (head a |
 // head b), P' bf16 [256,384), h fp32 [384,512).  Every wait is bounded; a
 // timeout sets the status word and the CTA unwinds.
@@ -55,7 +57,8 @@ namespace {
 constexpr int kBlk = 128;  // tokens per block
 constexpr int kS = 128;    // state rows
 constexpr int kH = 64;     // head dim
-constexpr int kThreads = 21 * 32;
+constexpr int kThreads = 28 * 32;
+constexpr int kWarpP0 = 4, kWarpEpi0 = 20, kWarpScan0 = 24;
 constexpr int kSmemLimit = 232448;
 
 constexpr uint32_t kColCB = 0, kColZ = 128, kColP = 256, kColH = 384;
@@ -69,8 +72,8 @@ constexpr uint32_t kOffX = 6 * kBox;       // X double buffer: [2][head a | head
 constexpr uint32_t kOffHW = 10 * kBox;     // h in bf16 (rows = states), then w . X (rows = tokens): head a | b
 constexpr uint32_t kOffVec = 12 * kBox;    // per X buffer: G[2][128], dt[2][128], misc[16]
 constexpr uint32_t kVecBytes = 2304;
-constexpr uint32_t kOffWv = kOffVec + 2 * kVecBytes;  // P warps' column weights [8][128]
-constexpr uint32_t kOffBar = kOffWv + 8 * 128 * 4;
+constexpr uint32_t kOffWv = kOffVec + 2 * kVecBytes;  // P warps' column weights [16][64]
+constexpr uint32_t kOffBar = kOffWv + 16 * 64 * 4;
 // misc: D_a, D_b, G_s of a, b
 constexpr int kMiscD = 0, kMiscGs = 2;
 
@@ -88,13 +91,14 @@ enum : int {
     kBarDrainA,
     kBarDrainB,
     kBarDrainC,
+    kBarCbRead,                 // the P warps have read CB
     kBarPReady,                 // [2] per head
     kBarBFull = kBarPReady + 2, // [2]
     kBarBFree = kBarBFull + 2,  // [2]
     kBarXFull = kBarBFree + 2,  // [2] X buffer filled (TMA + gathers)
     kBarXRead = kBarXFull + 2,  // [2] the fold warps have read the buffer's X
-    kBarXFree = kBarXRead + 2,  // [2] y (written over X) has been stored
-    kNumBars = kBarXFree + 2
+    kBarYReady = kBarXRead + 2, // [2] the epilogue has written y over the buffer's X
+    kNumBars = kBarYReady + 2
 };
 constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + ctl + alignment slack
 static_assert(kSmemBytes <= (uint32_t)kSmemLimit, "shared-memory plan too large");
@@ -135,7 +139,7 @@ struct Vec {  // one X buffer's gathered per-token values
 };
 static_assert(sizeof(Vec) <= kVecBytes, "per-buffer vector area too small");
 
-// Issues Y += P'_hh X_hh for one head (A: P' in TMEM; B: the head's X box,
+// Issues Y += P_hh X_hh for one head (A: P in TMEM; B: the head's X box,
 // MN-major); the accumulator already holds the rescaled Z.
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint64_t dXhead, int hh) {
     const uint32_t id_y = tc::idesc_bf16(128, kH, false, true);
@@ -168,7 +172,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         tc::mbar_init(&bars[kBarCbDone], 1);
         tc::mbar_init(&bars[kBarZDone], 1);
         tc::mbar_init(&bars[kBarZScaled], 4);
-        tc::mbar_init(&bars[kBarY2Done], 2);    // heads a and b
+        tc::mbar_init(&bars[kBarY2Done], 1);
         tc::mbar_init(&bars[kBarEpiDone], 4);
         tc::mbar_init(&bars[kBarHReady], 4);
         tc::mbar_init(&bars[kBarWxReady], 4);
@@ -176,13 +180,14 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         tc::mbar_init(&bars[kBarDrainA], 1);
         tc::mbar_init(&bars[kBarDrainB], 1);
         tc::mbar_init(&bars[kBarDrainC], 1);
+        tc::mbar_init(&bars[kBarCbRead], 16);
         for (int u = 0; u < 2; ++u) {
-            tc::mbar_init(&bars[kBarPReady + u], 4);
+            tc::mbar_init(&bars[kBarPReady + u], 8);
             tc::mbar_init(&bars[kBarBFull + u], 1);
             tc::mbar_init(&bars[kBarBFree + u], 2);  // after the CB product and the state update
             tc::mbar_init(&bars[kBarXFull + u], 1 + 32);  // expect-tx + one cp.async arrival per lane
             tc::mbar_init(&bars[kBarXRead + u], 4);       // the fold warps
-            tc::mbar_init(&bars[kBarXFree + u], 1);       // the epilogue's store
+            tc::mbar_init(&bars[kBarYReady + u], 4);      // the epilogue warps
         }
         ctl->abort = 0;
         ctl->never = 0;
@@ -201,15 +206,28 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
     if (warp == 0) {
         // ===================== X producer + per-token gathers =====================
-        if (lane == 0) tc::tma_prefetch_desc(&tm_x);
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tm_x);
+            tc::tma_prefetch_desc(&tm_y);
+        }
         tc::griddep_wait();  // G comes from stage 1
         bool ok = true;
-        int fills[2] = {0, 0};
+        int fills0 = 0, fills1 = 0;  // fills issued per buffer
         for (int k = 0; ok && k < nblk; ++k) {
             const int u = k & 1, v = k >> 1;
             if (k >= 2) {
+                // y of block k - 2 sits over this buffer's X: store it, then refill
                 bool w_ok = true;
-                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarXFree + u], (v - 1) & 1, abort_flag);
+                if (lane == 0) {
+                    w_ok = tc::mbar_wait(&bars[kBarYReady + u], (v - 1) & 1, abort_flag);
+                    if (w_ok) {
+                        for (int hh = 0; hh < 2; ++hh)
+                            tc::tma_store_4d(&tm_y, smem + kOffX + u * 2 * kBox + hh * kBox, 0, h0 + hh,
+                                             (k - 2) * kBlk, (int)b);
+                        tc::bulk_commit();
+                        tc::bulk_wait_read_all();
+                    }
+                }
                 if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) {
                     ok = false;
                     break;
@@ -247,55 +265,61 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc::cp_async4(&vec->misc[kMiscGs + hh], gs, pos ? 4u : 0u);
             }
             tc::cp_async_mbar_arrive_noinc(full);
-            ++fills[u];
+            if (u) ++fills1; else ++fills0;
+        }
+        // the last (up to) two blocks' y
+        for (int k = nblk - 2 < 0 ? 0 : nblk - 2; ok && k < nblk; ++k) {
+            if (lane == 0) {
+                const int u = k & 1, v = k >> 1;
+                ok = tc::mbar_wait(&bars[kBarYReady + u], v & 1, abort_flag);
+                if (ok) {
+                    for (int hh = 0; hh < 2; ++hh)
+                        tc::tma_store_4d(&tm_y, smem + kOffX + u * 2 * kBox + hh * kBox, 0, h0 + hh, k * kBlk, (int)b);
+                    tc::bulk_commit();
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
         }
         if (!ok && lane == 0) set_abort(ctl, p.status);
-        // no copy of this warp may still be landing when the CTA exits
-        if (lane == 0)
-            for (int u = 0; u < 2; ++u)
-                if (fills[u] > 0) (void)tc::mbar_wait(&bars[kBarXFull + u], (fills[u] - 1) & 1, never);
-    } else if (warp == 3) {
-        // ============================ B, C producer ============================
+        // no copy of this warp may still be landing or reading when the CTA exits
+        if (lane == 0) {
+            tc::bulk_wait_all();
+            if (fills0 > 0) (void)tc::mbar_wait(&bars[kBarXFull + 0], (fills0 - 1) & 1, never);
+            if (fills1 > 0) (void)tc::mbar_wait(&bars[kBarXFull + 1], (fills1 - 1) & 1, never);
+        }
+    } else if (warp == 1) {
+        // ============== issuer of CB, and the C and B loads (TMA) ==============
         if (lane == 0) {
             tc::tma_prefetch_desc(&tm_b);
             tc::tma_prefetch_desc(&tm_c);
             bool ok = true;
-            int cfills = 0, bfills[2] = {0, 0};
-            for (int k = 0; ok && k < nblk; ++k) {
-                const int u = k & 1, v = k >> 1;
-                const int t0 = k * kBlk;
-                // B of block k into its buffer once block k - 2's CB and state update read it
-                if (k >= 2 && !tc::mbar_wait(&bars[kBarBFree + u], (v - 1) & 1, abort_flag)) { ok = false; break; }
+            int cfills = 0, bfills0 = 0, bfills1 = 0;
+            auto load_b = [&](int k) {
+                const int u = k & 1;
                 tc::mbar_arrive_expect_tx(&bars[kBarBFull + u], 2 * kBox);
                 for (int kb = 0; kb < 2; ++kb)
                     tc::tma_load_4d(smem + kOffB + u * 2 * kBox + kb * kBox, &tm_b, &bars[kBarBFull + u], kb * 64,
-                                    grp, t0, (int)b);
-                ++bfills[u];
-                // C of block k once block k - 1's CB and Z products read it
-                if (k >= 1 && !tc::mbar_wait(&bars[kBarCFree], (k - 1) & 1, abort_flag)) { ok = false; break; }
+                                    grp, k * kBlk, (int)b);
+                if (u) ++bfills1; else ++bfills0;
+            };
+            auto load_c = [&](int k) {
                 tc::mbar_arrive_expect_tx(&bars[kBarCFull], 2 * kBox);
                 for (int kb = 0; kb < 2; ++kb)
-                    tc::tma_load_4d(smem + kOffC + kb * kBox, &tm_c, &bars[kBarCFull], kb * 64, grp, t0, (int)b);
+                    tc::tma_load_4d(smem + kOffC + kb * kBox, &tm_c, &bars[kBarCFull], kb * 64, grp, k * kBlk, (int)b);
                 ++cfills;
+            };
+            if (nblk > 0) {
+                load_b(0);
+                load_c(0);
             }
-            if (!ok) set_abort(ctl, p.status);
-            if (cfills > 0) (void)tc::mbar_wait(&bars[kBarCFull], (cfills - 1) & 1, never);
-            for (int u = 0; u < 2; ++u)
-                if (bfills[u] > 0) (void)tc::mbar_wait(&bars[kBarBFull + u], (bfills[u] - 1) & 1, never);
-        }
-    } else if (warp == 1) {
-        // =========== issuer: CB, then head a's P' X onto the rescaled Z ===========
-        if (lane == 0) {
-            bool ok = true;
             const uint32_t aC = tc::smem_u32(smem + kOffC), aB0 = tc::smem_u32(smem + kOffB);
             const uint32_t id_cb = tc::idesc_bf16(128, 128, false, false);
-            const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffX), kBox, 1024);
             for (int k = 0; ok && k < nblk; ++k) {
                 const int u = k & 1, v = k >> 1;
                 if (!tc::mbar_wait(&bars[kBarCFull], k & 1, abort_flag)) { ok = false; break; }
                 if (!tc::mbar_wait(&bars[kBarBFull + u], v & 1, abort_flag)) { ok = false; break; }
-                // CB of block k - 1 has been read by both heads' P' warps
-                if (k >= 1 && !tc::mbar_wait(&bars[kBarPReady + 1], (k - 1) & 1, abort_flag)) { ok = false; break; }
+                // CB of block k - 1 has been read by every P warp
+                if (k >= 1 && !tc::mbar_wait(&bars[kBarCbRead], (k - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 // CB = C B^T: both K-major over the state (two boxes of 64)
                 const uint32_t aB = aB0 + u * 2 * kBox;
@@ -308,31 +332,42 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc::mma_commit(&bars[kBarCbDone]);
                 tc::mma_commit(&bars[kBarCFree]);
                 tc::mma_commit(&bars[kBarBFree + u]);
-                if (!tc::mbar_wait(&bars[kBarPReady + 0], k & 1, abort_flag)) { ok = false; break; }
-                if (!tc::mbar_wait(&bars[kBarZScaled], k & 1, abort_flag)) { ok = false; break; }
-                if (!tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag)) { ok = false; break; }
-                tc::tc_fence_after();
-                issue_pv(tmem, dX0 + (uint64_t)u * ((2 * kBox) >> 4), 0);
-                tc::mma_commit(&bars[kBarY2Done]);
+                if (k + 1 < nblk) {
+                    // B of block k + 1 into the buffer block k - 1's CB and state update read
+                    if (k >= 1 && !tc::mbar_wait(&bars[kBarBFree + (u ^ 1)], ((k - 1) >> 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    load_b(k + 1);
+                    // C of block k + 1 once block k's CB and Z products read it
+                    if (!tc::mbar_wait(&bars[kBarCFree], k & 1, abort_flag)) { ok = false; break; }
+                    load_c(k + 1);
+                }
             }
-            // every MMA this thread issued has completed before TMEM is freed
+            // every MMA this thread issued has completed, and no copy is still
+            // landing, before TMEM is freed and the CTA exits
             tc::mma_commit(&bars[kBarDrainA]);
             (void)tc::mbar_wait(&bars[kBarDrainA], 0, never);
+            if (cfills > 0) (void)tc::mbar_wait(&bars[kBarCFull], (cfills - 1) & 1, never);
+            if (bfills0 > 0) (void)tc::mbar_wait(&bars[kBarBFull + 0], (bfills0 - 1) & 1, never);
+            if (bfills1 > 0) (void)tc::mbar_wait(&bars[kBarBFull + 1], (bfills1 - 1) & 1, never);
             if (!ok) set_abort(ctl, p.status);
         }
-    } else if (warp == 20) {
-        // ================= issuer: head b's P' X onto the rescaled Z =================
+    } else if (warp == 3) {
+        // ============ issuer of P X onto the rescaled Z, head a then head b ============
         if (lane == 0) {
             bool ok = true;
             const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffX), kBox, 1024);
             for (int k = 0; ok && k < nblk; ++k) {
                 const int u = k & 1, v = k >> 1;
-                if (!tc::mbar_wait(&bars[kBarPReady + 1], k & 1, abort_flag)) { ok = false; break; }
                 if (!tc::mbar_wait(&bars[kBarZScaled], k & 1, abort_flag)) { ok = false; break; }
                 if (!tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag)) { ok = false; break; }
-                tc::tc_fence_after();
-                issue_pv(tmem, dX0 + (uint64_t)u * ((2 * kBox) >> 4) + (kBox >> 4), 1);
-                tc::mma_commit(&bars[kBarY2Done]);
+                for (int hh = 0; hh < 2 && ok; ++hh) {
+                    if (!tc::mbar_wait(&bars[kBarPReady + hh], k & 1, abort_flag)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    issue_pv(tmem, dX0 + (uint64_t)u * ((2 * kBox) >> 4) + (uint64_t)hh * (kBox >> 4), hh);
+                }
+                if (ok) tc::mma_commit(&bars[kBarY2Done]);
             }
             tc::mma_commit(&bars[kBarDrainC]);
             (void)tc::mbar_wait(&bars[kBarDrainC], 0, never);
@@ -380,20 +415,22 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             (void)tc::mbar_wait(&bars[kBarDrainB], 0, never);
             if (!ok) set_abort(ctl, p.status);
         }
-    } else if (warp < 12) {
-        // ============== P' formation (warps 4-7 head a, 8-11 head b) ==============
+    } else if (warp < kWarpEpi0) {
+        // ======== P formation (warps 4-19: head, column half, lane quadrant) ========
         const int q = warp & 3;
-        const int hh = (warp - 4) >> 2;
+        const int role = (warp - kWarpP0) >> 2;  // 0..3
+        const int hh = role & 1, part = role >> 1;
         const int i = 32 * q + lane;  // row of the block = TMEM lane
+        const int g_lo = 2 * part, g_hi = imin64(2 * part + 1, q);  // column groups with entries
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         const uint32_t tp = tmem + kColP + hh * 64 + lane_base;
-        float* wv = reinterpret_cast<float*>(smem + kOffWv) + (warp - 4) * kBlk;
+        float* wv = reinterpret_cast<float*>(smem + kOffWv) + (warp - kWarpP0) * 64;  // w of groups g_lo, g_lo + 1
         bool ok = true;
         for (int k = 0; k < nblk; ++k) {
             const int u = k & 1, v = k >> 1;
             if (ok) ok = tc::mbar_wait(&bars[kBarCbDone], k & 1, abort_flag);
             if (ok) ok = tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag);
-            if (ok && k >= 1) ok = tc::mbar_wait(&bars[kBarY2Done], (k - 1) & 1, abort_flag);  // P' free
+            if (ok && k >= 1) ok = tc::mbar_wait(&bars[kBarY2Done], (k - 1) & 1, abort_flag);  // P free
             if (!ok) break;
             tc::tc_fence_after();
             const Vec* vec = vecs + u;
@@ -401,17 +438,16 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const float gref = q == 0 ? vec->misc[kMiscGs + hh] : vec->G[hh][32 * q - 1];
             const bool mild = gref - grow <= kMildSpan;  // false for NaN
             const bool all_mild = __all_sync(0xffffffffu, mild);
-            const float ui = mild ? exp2f(grow - gref) : 1.f;
-            for (int gi = 0; gi <= q; ++gi) {
+            for (int gi = g_lo; gi <= g_hi; ++gi) {
                 const int j = 32 * gi + lane;
                 const float wj = exp2f(fminf(gref - vec->G[hh][j], kMildSpan)) * vec->dt[hh][j];
-                wv[j] = wj > kWMax ? kWMax : wj;
+                wv[32 * (gi - g_lo) + lane] = wj > kWMax ? kWMax : wj;
             }
             __syncwarp();
-            const float2 u2 = make_float2(ui, ui);
 #pragma unroll
-            for (int gi = 0; gi < 4; ++gi) {
-                if (gi > q) {
+            for (int t = 0; t < 2; ++t) {
+                const int gi = g_lo + t;
+                if (gi > g_hi) {
                     uint32_t z[8];
 #pragma unroll
                     for (int x = 0; x < 8; ++x) z[x] = 0u;
@@ -424,6 +460,12 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi + 16, r[1]);
                 tc::tmem_wait_ld16(r[0]);
                 tc::tmem_tie16(r[1]);
+                if (gi == g_hi) {
+                    // this warp's last read of CB: the next block's CB may be written
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&bars[kBarCbRead]);
+                }
                 if (gi == q) {  // causal mask inside the diagonal 32 x 32 group
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
@@ -434,7 +476,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int col = 32 * gi + 16 * half;
-                    const float* w = wv + col;
+                    const float* w = wv + 32 * t + 16 * half;
                     const uint32_t* rr = r[half];
                     uint32_t pk[8];
                     if (all_mild) {
@@ -442,18 +484,16 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         for (int e4 = 0; e4 < 4; ++e4) {
                             const float4 v4 = *reinterpret_cast<const float4*>(w + 4 * e4);
                             const int o = 4 * e4;
-                            const float2 f0 = tc::mul_f32x2(make_float2(v4.x, v4.y), u2);
-                            const float2 f1 = tc::mul_f32x2(make_float2(v4.z, v4.w), u2);
                             const float2 p0 = tc::mul_f32x2(
-                                make_float2(__uint_as_float(rr[o]), __uint_as_float(rr[o + 1])), f0);
+                                make_float2(__uint_as_float(rr[o]), __uint_as_float(rr[o + 1])), make_float2(v4.x, v4.y));
                             const float2 p1 = tc::mul_f32x2(
-                                make_float2(__uint_as_float(rr[o + 2]), __uint_as_float(rr[o + 3])), f1);
+                                make_float2(__uint_as_float(rr[o + 2]), __uint_as_float(rr[o + 3])), make_float2(v4.z, v4.w));
                             pk[2 * e4] = tc::pack_bf16x2(p0.x, p0.y);
                             pk[2 * e4 + 1] = tc::pack_bf16x2(p1.x, p1.y);
                         }
                     } else {
-                        // per row: the split weight times u_i (mild rows, the
-                        // same products as above) or the direct one
+                        // per row: the split weight (mild rows, the same products
+                        // as above) or the direct one
                         const float* gj = &vec->G[hh][col];
                         const float* dj = &vec->dt[hh][col];
 #pragma unroll
@@ -462,10 +502,10 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             const float4 g4 = *reinterpret_cast<const float4*>(gj + 4 * e4);
                             const float4 d4 = *reinterpret_cast<const float4*>(dj + 4 * e4);
                             const int o = 4 * e4;
-                            const float f0 = mild ? v4.x * ui : exact_weight(grow, g4.x, d4.x);
-                            const float f1 = mild ? v4.y * ui : exact_weight(grow, g4.y, d4.y);
-                            const float f2 = mild ? v4.z * ui : exact_weight(grow, g4.z, d4.z);
-                            const float f3 = mild ? v4.w * ui : exact_weight(grow, g4.w, d4.w);
+                            const float f0 = mild ? v4.x : exact_weight(grow, g4.x, d4.x);
+                            const float f1 = mild ? v4.y : exact_weight(grow, g4.y, d4.y);
+                            const float f2 = mild ? v4.z : exact_weight(grow, g4.z, d4.z);
+                            const float f3 = mild ? v4.w : exact_weight(grow, g4.w, d4.w);
                             pk[2 * e4] = tc::pack_bf16x2(__uint_as_float(rr[o]) * f0, __uint_as_float(rr[o + 1]) * f1);
                             pk[2 * e4 + 1] =
                                 tc::pack_bf16x2(__uint_as_float(rr[o + 2]) * f2, __uint_as_float(rr[o + 3]) * f3);
@@ -474,32 +514,46 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tc::tmem_st8(tp + col / 2, pk);
                 }
             }
+            if (g_hi < g_lo) {
+                // no column group of this warp has entries (second half, quadrants 0-1)
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[kBarCbRead]);
+            }
             tc::tmem_wait_st();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[kBarPReady + hh]);
         }
         if (!ok) set_abort(ctl, p.status);
-    } else if (warp < 16) {
-        // ========================= epilogue (warps 12-15) =========================
+    } else if (warp < kWarpScan0) {
+        // ========================= epilogue (warps 20-23) =========================
         const int q = warp & 3;
         const int i = 32 * q + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        const bool leader = (warp == 12 && lane == 0);
         bool ok = true;
-        // Every epilogue warp runs every block and the named barrier below,
-        // whatever its own waits return, so none is left at the barrier.
-        for (int k = 0; k < nblk; ++k) {
+        for (int k = 0; ok && k < nblk; ++k) {
             const int u = k & 1, v = k >> 1;
             const Vec* vec = vecs + u;
-            // ---- Z <- exp2(G_i - G_s) Z, in place
+            // row factors of both heads: Z <- f_i Z now, y = u_i Y + D x later
+            float fz[2] = {0.f, 0.f}, fu[2] = {1.f, 1.f};
             if (ok) ok = tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag);
+            if (ok) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const float grow = vec->G[hh][i];
+                    const float gs = vec->misc[kMiscGs + hh];
+                    const float gref = q == 0 ? gs : vec->G[hh][32 * q - 1];
+                    const bool mild = gref - grow <= kMildSpan;
+                    fz[hh] = mild ? exp2f(gref - gs) : exp2f(grow - gs);
+                    fu[hh] = mild ? exp2f(grow - gref) : 1.f;
+                }
+            }
             if (ok) ok = tc::mbar_wait(&bars[kBarZDone], k & 1, abort_flag);
             tc::tc_fence_after();
             if (ok) {
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const float si = exp2f(vec->G[hh][i] - vec->misc[kMiscGs + hh]);
 #pragma unroll
                     for (int m = 0; m < kH / 32; ++m) {
                         uint32_t za[2][16];
@@ -511,7 +565,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
                         for (int t = 0; t < 2; ++t)
 #pragma unroll
-                            for (int x = 0; x < 16; ++x) za[t][x] = __float_as_uint(si * __uint_as_float(za[t][x]));
+                            for (int x = 0; x < 16; ++x) za[t][x] = __float_as_uint(fz[hh] * __uint_as_float(za[t][x]));
                         tc::tmem_st16(ta, za[0]);
                         tc::tmem_st16(ta + 16, za[1]);
                     }
@@ -521,7 +575,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::tc_fence_before();
             __syncwarp();
             if (ok && lane == 0) tc::mbar_arrive(&bars[kBarZScaled]);
-            // ---- y = Y + D x, written over x in the stage
+            // ---- y = u_i Y + D x, written over x in the stage
             if (ok) ok = tc::mbar_wait(&bars[kBarY2Done], k & 1, abort_flag);
             if (ok) ok = tc::mbar_wait(&bars[kBarXRead + u], v & 1, abort_flag);  // y goes over X
             tc::tc_fence_after();
@@ -530,32 +584,36 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const float dh = vec->misc[kMiscD + hh];
-                    const float2 d2 = make_float2(dh, dh);
+                    const float2 d2 = make_float2(dh, dh), u2 = make_float2(fu[hh], fu[hh]);
                     uint8_t* xrow = sX + hh * kBox + i * 128;
 #pragma unroll
-                    for (int m = 0; m < kH / 16; ++m) {
-                        uint32_t ya[2][8];
-                        uint4* px[2];
-                        uint4 xv[2];
+                    for (int m = 0; m < kH / 32; ++m) {
+                        // 32 columns of Y and the four 16-byte x chunks under one wait
+                        uint32_t ya[4][8];
+                        uint4* px[4];
+                        uint4 xv[4];
 #pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            const int kk = 16 * m + 8 * t;
+                        for (int t = 0; t < 4; ++t) {
+                            const int kk = 32 * m + 8 * t;
                             tc::tmem_ld8_nowait(tmem + kColZ + hh * kH + lane_base + kk, ya[t]);
                             px[t] = reinterpret_cast<uint4*>(xrow + (((kk >> 3) ^ (i & 7)) << 4));
                         }
-                        xv[0] = *px[0];
-                        xv[1] = *px[1];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) xv[t] = *px[t];
                         tc::tmem_wait_ld8(ya[0]);
                         tc::tmem_tie8(ya[1]);
+                        tc::tmem_tie8(ya[2]);
+                        tc::tmem_tie8(ya[3]);
 #pragma unroll
-                        for (int t = 0; t < 2; ++t) {
+                        for (int t = 0; t < 4; ++t) {
                             const uint32_t xw[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
                             uint32_t yw[4];
 #pragma unroll
                             for (int x = 0; x < 4; ++x) {
                                 const float2 a2 = tc::fma_f32x2(
                                     d2, make_float2(tc::bf16_lo(xw[x]), tc::bf16_hi(xw[x])),
-                                    make_float2(__uint_as_float(ya[t][2 * x]), __uint_as_float(ya[t][2 * x + 1])));
+                                    tc::mul_f32x2(u2, make_float2(__uint_as_float(ya[t][2 * x]),
+                                                                  __uint_as_float(ya[t][2 * x + 1]))));
                                 yw[x] = tc::pack_bf16x2(a2.x, a2.y);
                             }
                             *px[t] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
@@ -563,27 +621,22 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     }
                 }
             }
-            // Y has been read: Z of the next block may be written
+            // Y has been read: Z of the next block may be written.  y is in
+            // shared memory for the X producer's TMA store.
             tc::tc_fence_before();
-            __syncwarp();
-            if (ok && lane == 0) tc::mbar_arrive(&bars[kBarEpiDone]);
             tc::fence_proxy_async_smem();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (leader && ok) {
-                for (int hh = 0; hh < 2; ++hh)
-                    tc::tma_store_4d(&tm_y, sX + hh * kBox, 0, h0 + hh, k * kBlk, (int)b);
-                tc::bulk_commit();
-                tc::bulk_wait_read_all();
-                tc::mbar_arrive(&bars[kBarXFree + u]);
+            __syncwarp();
+            if (ok && lane == 0) {
+                tc::mbar_arrive(&bars[kBarEpiDone]);
+                tc::mbar_arrive(&bars[kBarYReady + u]);
             }
         }
-        if (leader) tc::bulk_wait_all();
         if (!ok) set_abort(ctl, p.status);
     } else {
         // ==================== scan, then fold (warps 16-19) ====================
         const int q = warp & 3;
         const int s = 32 * q + lane;       // scan: state row = TMEM lane
-        const int t = (warp - 16) * 32 + lane;  // fold: token row of the block
+        const int t = (warp - kWarpScan0) * 32 + lane;  // fold: token row of the block
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         // h <- initial state (or zeros)
 #pragma unroll 1

@@ -10,6 +10,9 @@ be checked against measurements:
       whole (one 128-wide MMA per head) or split into two 64-wide virtual
       heads sharing the head's decays; a forced variant that does not fit
       runs stage 3 on the CUDA-core kernel instead (its time is shown).
+  MAMBA2_FWD_PATH = staged | fused      the whole forward pass as separate
+      stages or with the fused state-pass + output kernel (where it fits:
+      bf16, head dim 64 in pairs of one group, state 128, chunk 128 or 256).
 
 Usage (one GPU):  python -m mamba_chunked_ssd_gb300.tune [--steps K] [--json]
 Each line: workload, candidate, mean stage time in microseconds (CUDA events
@@ -31,6 +34,7 @@ if ROOT not in sys.path:
 
 FLUSH_BYTES = 256 << 20
 HEAD_SPLIT_ENV = "MAMBA2_CHUNK_OUT_HEAD_SPLIT"
+FWD_PATH_ENV = "MAMBA2_FWD_PATH"
 
 
 def _time(fn, steps, warmup, flush, stream):
@@ -90,21 +94,75 @@ def head_split_rows(workloads, steps=10, warmup=3):
     return rows
 
 
+def fused_fits(w):
+    """The fused kernel's shape range (mirrors ssd_fused_fits in the library)."""
+    return (w.dtype == "bf16" and w.headdim == 64 and w.dstate == 128 and w.chunk_size in (128, 256)
+            and w.nheads % 2 == 0 and (w.nheads // w.ngroups) % 2 == 0)
+
+
+def fwd_path_rows(workloads, steps=10, warmup=3):
+    """Whole-pass time (mamba2_ssd_fwd) on the separate stages and on the fused
+    kernel, per workload the fused kernel covers."""
+    import torch
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+
+    bd.load_library()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    rows = []
+    saved = os.environ.pop(FWD_PATH_ENV, None)
+    try:
+        for w in workloads:
+            if not fused_fits(w):
+                continue
+            d = make_inputs(w, device="cuda")
+            shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
+            ws = torch.empty(max(bd.mamba2_ssd_fwd_workspace_size(shape), 1), device="cuda", dtype=torch.uint8)
+            y = torch.empty_like(d["x"])
+            fin = torch.empty(w.batch, w.nheads, w.dstate, w.headdim, device="cuda", dtype=torch.float32)
+            fn = lambda: bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size,  # noqa: E731
+                                           D=d["D"], initial_state=d["initial_state"], y=y, final_state=fin,
+                                           workspace=ws)
+            times = {}
+            for cand in ("staged", "fused"):
+                os.environ[FWD_PATH_ENV] = cand
+                times[cand] = _time(fn, steps, warmup, flush, stream)
+            os.environ.pop(FWD_PATH_ENV, None)
+            bd.mamba2_check_device_status()
+            rows.append({"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                         "chunk_size": w.chunk_size, "staged_us": times["staged"], "fused_us": times["fused"]})
+            del d, ws, y, fin
+    finally:
+        if saved is not None:
+            os.environ[FWD_PATH_ENV] = saved
+    return rows
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--json", action="store_true")
     args = ap.parse_args()
     from mamba_chunked_ssd_gb300.synthetic import WORKLOADS, sweep_workloads
-    ws = [WORKLOADS["large_state"]] + sweep_workloads(seeds=(0,))
+    ws = [WORKLOADS["large_state"], WORKLOADS["long_seq_carried_state"], WORKLOADS["mamba2_1p3b_layer"],
+          WORKLOADS["blog_example"]] + sweep_workloads(seeds=(0,))
     rows = head_split_rows(ws, steps=args.steps)
+    paths = fwd_path_rows(ws, steps=args.steps)
     if args.json:
-        print(json.dumps(rows))
+        print(json.dumps({"head_split": rows, "fwd_path": paths}))
         return
+    print("Stage 3, heads of 128 columns:")
     print("| workload | whole heads (µs) | split heads (µs) | default (µs) |")
     print("|---|---|---|---|")
     for r in rows:
         print(f"| {r['workload']} | {r['whole_us']:.1f} | {r['split_us']:.1f} | {r['default_us']:.1f} |")
+    print()
+    print("Whole forward pass where the fused kernel fits:")
+    print("| workload | separate stages (µs) | fused (µs) |")
+    print("|---|---|---|")
+    for r in paths:
+        print(f"| {r['workload']} | {r['staged_us']:.1f} | {r['fused_us']:.1f} |")
 
 
 if __name__ == "__main__":
