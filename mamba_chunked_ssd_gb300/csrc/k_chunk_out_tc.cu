@@ -12,6 +12,9 @@
 //                blocks 0 .. I) and h_c into a ring of stages; its 32 lanes
 //                gather the head's G, dt and D into the same stage with
 //                cp.async, so the epilogue never waits on a global load;
+//                before refilling a stage it stores (TMA) the y that the
+//                epilogue wrote over the stage's X, so no epilogue warp waits
+//                on a store;
 //   warp 1       TMEM allocator; one thread issues the C B^T products and
 //                the tcgen05.mma of head stream 0;
 //   warps 2..17  epilogue, split into head streams (two when H = 64, one when
@@ -105,8 +108,9 @@ enum : int {
     kBarYDone = kBarPReady + kMaxStreams,      // [kMaxStreams]
     kBarYFree = kBarYDone + kMaxStreams,       // [kMaxStreams]
     kBarFull = kBarYFree + kMaxStreams,        // [kMaxFill]
-    kBarSlotFree = kBarFull + kMaxFill,        // [kMaxStages]
-    kNumBars = kBarSlotFree + kMaxStages
+    kBarSlotFree = kBarFull + kMaxFill,        // [kMaxStages] the MMAs have read the stage
+    kBarYReady = kBarSlotFree + kMaxStages,    // [kMaxStages] y is written over the stage's X
+    kNumBars = kBarYReady + kMaxStages
 };
 
 struct SharedCtl {
@@ -210,9 +214,12 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::mbar_init(&bars[kBarYFree + i], wps);
         }
         for (int i = 0; i < kMaxFill; ++i) tc::mbar_init(&bars[kBarFull + i], kFillArrivals);
-        // a stage is free once the MMAs have read it and the TMA store of y
-        // (written over X_I in the stage) has read it
-        for (int i = 0; i < kMaxStages; ++i) tc::mbar_init(&bars[kBarSlotFree + i], 2);
+        // a stage is refilled once the MMAs have read it and the producer has
+        // stored the y the epilogue wrote over X_I in it
+        for (int i = 0; i < kMaxStages; ++i) {
+            tc::mbar_init(&bars[kBarSlotFree + i], 1);
+            tc::mbar_init(&bars[kBarYReady + i], wps);
+        }
         ctl->abort = 0;
         tc::fence_barrier_init();
     }
@@ -252,10 +259,25 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // stage, its reuse phase and the fill barrier as counters (no divisions)
         int st = 0, fill = 0;
         uint32_t slot_phase = 1;  // phase of the previous use of the stage
+        // y of virtual head kp leaves stage st (its previous use: phase `ph`)
+        // through TMA stores; rows past the sequence end are clipped
+        auto store_y = [&](int kp, int st_kp, uint32_t ph) -> bool {
+            if (!tc::mbar_wait(&bars[kBarYReady + st_kp], ph, abort_flag)) return false;
+            const uint8_t* sY = sStage + st_kp * lay.stage_bytes;
+            for (int cb = 0; cb < H / 64; ++cb)
+                tc::tma_store_4d(&tm_y, sY + cb * (Tj * 128) + I * 16384, (kp % VS) * H + cb * 64, h0 + kp / VS,
+                                 (int)(t0 + 128 * I), (int)b);
+            tc::bulk_commit();
+            return true;
+        };
         for (int k = 0; ok && k < nvh; ++k) {
             if (k >= lay.nst) {
                 bool w_ok = true;
-                if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], slot_phase, abort_flag);
+                if (lane == 0) {
+                    w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], slot_phase, abort_flag) &&
+                           store_y(k - lay.nst, st, slot_phase);
+                    tc::bulk_wait_read_all();  // the stage may be overwritten
+                }
                 if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) {
                     ok = false;
                     break;
@@ -293,6 +315,12 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 slot_phase ^= 1u;
             }
             if (++fill == lay.nfill) fill = 0;
+        }
+        // the y of the last heads still sits in the stages
+        if (lane == 0) {
+            for (int kp = nvh > lay.nst ? nvh - lay.nst : 0; ok && kp < nvh; ++kp)
+                ok = store_y(kp, kp % lay.nst, (uint32_t)(kp / lay.nst) & 1u);
+            tc::bulk_wait_all();
         }
         if (!ok && lane == 0) set_abort(ctl, p.status);
     } else if (warp == 1 || (nstr == 2 && warp == kIssuer2)) {
@@ -442,14 +470,10 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
         tc::tc_fence_after();
 
-        // Every warp of a stream runs every head of the stream and the stream's
-        // named barrier below, whatever its own waits return, so no warp is
-        // left at the barrier; after a failed wait a warp only skips the work.
-        const bool stream_leader = (e % wps == 0) && lane == 0;
         // stage and fill barrier of head k as counters, advanced by nstr heads
         int st = sid % lay.nst, fill = sid % lay.nfill;
         uint32_t fill_phase = (sid / lay.nfill) & 1;
-        for (int k = sid; k < nvh; k += nstr) {
+        for (int k = sid; ok && k < nvh; k += nstr) {
             const int n = k / nstr;
             if (ok) ok = tc::mbar_wait(&bars[kBarFull + fill], fill_phase, abort_flag);
             uint8_t* sX = sStage + st * lay.stage_bytes;
@@ -608,21 +632,15 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 }
             }
           }
-            // y leaves the stage through TMA stores (rows past the sequence end
-            // are clipped by the tensor bounds)
-            tc::fence_proxy_async_smem();
+            // Z and Y2 have been read (the stream's accumulators may be
+            // rewritten), and y is in the stage for the producer's TMA store
             tc::tc_fence_before();
-            asm volatile("bar.sync %0, %1;" ::"r"(2 + sid), "r"(wps * 32) : "memory");
-            if (stream_leader && ok) {
-                for (int cb = 0; cb < H / 64; ++cb)
-                    tc::tma_store_4d(&tm_y, sX + cb * (Tj * 128) + I * 16384, (k % VS) * H + cb * 64, h0 + k / VS,
-                                     (int)(t0 + 128 * I),
-                                     (int)b);
-                tc::bulk_commit();
-                tc::bulk_wait_read_all();
-                tc::mbar_arrive(&bars[kBarSlotFree + st]);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (ok && lane == 0) {
+                tc::mbar_arrive(&bars[kBarYFree + sid]);
+                tc::mbar_arrive(&bars[kBarYReady + st]);
             }
-            if (ok && lane == 0) tc::mbar_arrive(&bars[kBarYFree + sid]);
 #pragma unroll
             for (int i = 0; i < nstr; ++i) {
                 if (++st == lay.nst) st = 0;
@@ -632,7 +650,6 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 }
             }
         }
-        if (stream_leader) tc::bulk_wait_all();
         if (!ok) set_abort(ctl, p.status);
     }
 
