@@ -43,6 +43,14 @@
 // row's arithmetic depends only on its own and earlier tokens.  Masked
 // entries are zero in CB before any weight multiplies them.  The T x T matrix
 // never reaches global memory.
+// Chunks of 64 tokens run in pairs: a CTA's 128 rows are chunks 2c' and
+// 2c' + 1, each with its own cumsum and its own state.  The state term takes
+// both states in one product over K = 2S,
+//   Z = [C_top | C_bot] [h_2c' ; h_2c'+1],
+// where C_top is C with the rows of the second chunk zeroed and C_bot with
+// those of the first (both built once per CTA; CB = C_top B^T + C_bot B^T),
+// and P is block-diagonal: rows of the second chunk see no column of the
+// first, and their quadrant 2 takes the chunk start as its reference.
 // Every wait is bounded; a timeout sets the status word and the CTA unwinds.
 #include <stdlib.h>
 
@@ -76,9 +84,10 @@ constexpr uint32_t kColCB = 0;
 __host__ __device__ constexpr uint32_t col_p(int s) { return 128u + 64u * (uint32_t)s; }
 __host__ __device__ constexpr uint32_t col_z(int s, int H) { return 256u + 2u * (uint32_t)H * (uint32_t)s; }
 
-// Shared-memory layout of a CTA of row block I: C_I, (I = 1) CB_10, then the
-// stages; a stage holds X [128 (I + 1) rows x H] | h_c [S x H] | G[T] dt[T] D.
-// Block 0 needs neither X_1 nor CB_10, so it fits more stages.
+// Shared-memory layout of a CTA of row block I: C_I (for chunk pairs C_top
+// and C_bot), (I = 1) CB_10, then the stages; a stage holds
+// X [128 (I + 1) rows x H] | h_c [S x H] (two states for chunk pairs) |
+// G[T] dt[T] D.  Block 0 needs neither X_1 nor CB_10, so it fits more stages.
 struct CoLayout {
     int nst;    // pipeline stages
     int nfill;  // stage-fill barriers, lcm(nst, nstr)
@@ -86,8 +95,9 @@ struct CoLayout {
 };
 
 struct CoTcParams {
-    Geom g;
-    int T;            // chunk size (128 or 256)
+    Geom g;           // geometry of the row blocks: chunk 128 or 256 (64-token chunks in pairs)
+    int T;            // tokens a CTA's rows span (128 or 256)
+    int64_t h_chunks; // chunk states per (batch, head): the caller's chunk count
     int nhb;          // heads per CTA (all in one group)
     int nstr;         // epilogue head streams (2 for H = 64, 1 for H = 128)
     int head_blocks;  // nheads / nhb
@@ -166,8 +176,9 @@ __device__ __forceinline__ void scale_row4(uint8_t* base, uint32_t box_stride, i
 // share the head's decays (its P is formed once per virtual head): the stages
 // then hold half of the head's X and h_c, which lets a head of 128 columns
 // with a 256-wide state and a 256-token chunk fit, and gives such heads two
-// streams.  VS = 1: virtual and real heads coincide.
-template <int H, int T, int VS>
+// streams.  VS = 1: virtual and real heads coincide.  PAIR: the 128 rows are
+// two chunks of 64 tokens (T = 128).
+template <int H, int T, int VS, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_h,
@@ -195,7 +206,9 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     constexpr int nstr = (H == 64) ? 2 : 1;
     const int wps = kEpiWarps / nstr;  // warps per stream
 
+    static_assert(!PAIR || T == 128, "chunk pairs span 128 rows");
     uint8_t* sC = smem + p.off_C;
+    uint8_t* sC1 = sC + 128 * S * 2;  // C_bot (chunk pairs)
     uint8_t* sCB10 = smem + p.off_CB10;
     const CoLayout lay = I ? p.lay[1] : p.lay[0];
     uint8_t* sStage = smem + lay.off_stage;
@@ -223,6 +236,17 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         ctl->abort = 0;
         tc::fence_barrier_init();
     }
+    if (PAIR) {
+        // zero rows 64..127 of C_top and rows 0..63 of C_bot (the TMA fills
+        // the other halves); the MMAs read them through the async proxy
+        const int nbox = S / 64;
+        for (int u = threadIdx.x; u < nbox * 512; u += kThreads) {
+            const int kb = u >> 9, r = u & 511;  // 512 x 16 bytes per half box
+            *reinterpret_cast<uint4*>(sC + kb * 16384 + 8192 + r * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sC1 + kb * 16384 + r * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        tc::fence_proxy_async_smem();
+    }
     if (warp == 1) {
         tc::tmem_alloc(&ctl->tmem_base, 512);
         tc::tmem_relinquish();
@@ -244,7 +268,15 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::tma_prefetch_desc(&tm_h);
             tc::mbar_arrive_expect_tx(&bars[kBarCbFull], (uint32_t)(128 * S * 2 + Tj * S * 2));
             for (int kb = 0; kb < S / 64; ++kb) {
-                tc::tma_load_4d(sC + kb * 16384, &tm_c, &bars[kBarCbFull], kb * 64, grp, (int)(t0 + 128 * I), (int)b);
+                if (PAIR) {
+                    // 64-row boxes: rows of chunk 2c' into C_top, of 2c' + 1 into C_bot
+                    tc::tma_load_4d(sC + kb * 16384, &tm_c, &bars[kBarCbFull], kb * 64, grp, (int)t0, (int)b);
+                    tc::tma_load_4d(sC1 + kb * 16384 + 8192, &tm_c, &bars[kBarCbFull], kb * 64, grp,
+                                    (int)(t0 + 64), (int)b);
+                } else {
+                    tc::tma_load_4d(sC + kb * 16384, &tm_c, &bars[kBarCbFull], kb * 64, grp, (int)(t0 + 128 * I),
+                                    (int)b);
+                }
                 for (int rb = 0; rb < Tj / 128; ++rb)
                     tc::tma_load_4d(sB + kb * (Tj * 128) + rb * 16384, &tm_b, &bars[kBarCbFull], kb * 64, grp,
                                     (int)(t0 + 128 * rb), (int)b);
@@ -291,13 +323,20 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const int h = h0 + k / VS;          // real head
             const int col0 = (k % VS) * H;      // its first column in this virtual head
             if (lane == 0) {
-                tc::mbar_arrive_expect_tx(full, x_bytes + h_bytes);
+                tc::mbar_arrive_expect_tx(full, x_bytes + (PAIR ? 2 : 1) * h_bytes);
+                // state rows of the chunk (of both chunks of a pair; past the
+                // last chunk the pair's second state repeats the first, whose
+                // rows then multiply zeros of C_bot or fall past the end)
+                const int64_t hrow = (b * g.nheads + h) * p.h_chunks + (PAIR ? 2 * c : c);
+                const int64_t hrow1 = (PAIR && 2 * c + 1 < p.h_chunks) ? hrow + 1 : hrow;
                 for (int cb = 0; cb < H / 64; ++cb) {
                     for (int rb = 0; rb < Tj / 128; ++rb)
                         tc::tma_load_4d(sX + cb * (Tj * 128) + rb * 16384, &tm_x, full, col0 + cb * 64, h,
                                         (int)(t0 + 128 * rb), (int)b);
-                    tc::tma_load_2d(sH + cb * (S * 128), &tm_h, full, col0 + cb * 64,
-                                    (int)(((b * g.nheads + h) * g.nchunks + c) * S));
+                    tc::tma_load_2d(sH + cb * (S * 128), &tm_h, full, col0 + cb * 64, (int)(hrow * S));
+                    if (PAIR)
+                        tc::tma_load_2d(sH + h_bytes + cb * (S * 128), &tm_h, full, col0 + cb * 64,
+                                        (int)(hrow1 * S));
                 }
             }
             // G_j (past the last valid token: G of the last one) and dt_j (zero there)
@@ -344,6 +383,15 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tc::mma_bf16_ss(tmem + kColCB, da, tc::sdesc_sw128(bbase + I * 16384, 16, 1024), id_cb, k16 > 0);
                     if (I == 1) tc::mma_bf16_ss(tmem + 256, da, tc::sdesc_sw128(bbase, 16, 1024), id_cb, k16 > 0);
                 }
+                if (PAIR) {
+                    // CB = C_top B^T + C_bot B^T
+                    const uint32_t aC1 = tc::smem_u32(sC1);
+                    for (int k16 = 0; k16 < S / 16; ++k16) {
+                        const uint64_t da = tc::sdesc_sw128(aC1 + (k16 >> 2) * 16384 + (k16 & 3) * 32, 16, 1024);
+                        const uint32_t bbase = aB + (k16 >> 2) * (Tj * 128) + (k16 & 3) * 32;
+                        tc::mma_bf16_ss(tmem + kColCB, da, tc::sdesc_sw128(bbase, 16, 1024), id_cb, 1);
+                    }
+                }
                 tc::mma_commit(&bars[kBarCbDone]);
                 if (I == 1) ok = tc::mbar_wait(&bars[kBarCb10Ready], 0, abort_flag);
             }
@@ -355,6 +403,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             // advance 32 bytes per 16 columns inside a 64-column box and 16 KB
             // per box; MN-major B tiles (h_c, X) advance 2 KB per 16 rows.
             const uint64_t dC0 = tc::sdesc_sw128(aC, 16, 1024);
+            const uint64_t dC1 = tc::sdesc_sw128(tc::smem_u32(sC1), 16, 1024);  // C_bot (chunk pairs)
             const uint64_t dCB10 = tc::sdesc_sw128(tc::smem_u32(sCB10), 16, 1024);
             const uint64_t dH0 = tc::sdesc_sw128(tc::smem_u32(sStage + lay.off_h_in_stage), S * 128, 1024);
             const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(sStage), Tj * 128, 1024);
@@ -373,6 +422,12 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 // Z = C_I (a h_c)   (B operand: rows s = K, columns H = N, MN-major)
                 for (int k16 = 0; k16 < S / 16; ++k16)
                     tc::mma_bf16_ss(tz, dC0 + (k16 >> 2) * 1024 + (k16 & 3) * 2, dH + 128 * k16, id_y, k16 > 0);
+                if (PAIR) {
+                    // Z += C_bot h_2c'+1   (the second state follows the first in the stage)
+                    const uint64_t dH1 = dH + (h_bytes >> 4);
+                    for (int k16 = 0; k16 < S / 16; ++k16)
+                        tc::mma_bf16_ss(tz, dC1 + (k16 >> 2) * 1024 + (k16 & 3) * 2, dH1 + 128 * k16, id_y, 1);
+                }
                 if (I == 1) {
                     // Z += CB_10 (v . X_0)   (A: CB_10 bf16, K-major over j; B: rows 0..127 of
                     // the stage's X, scaled in place, MN-major)
@@ -419,7 +474,12 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t tz = tmem + col_z(sid, H), ty2 = tz + H, tp = tmem + col_p(sid);
         float* wv = reinterpret_cast<float*>(smem + lay.off_small) + e * 64;  // per warp: w of 2 column groups
-        const int rq = 128 * I + 32 * q - 1;   // the column before this quadrant (-1: before the chunk)
+        // the column before this quadrant (-1: before the chunk; quadrant 2
+        // of a chunk pair starts the pair's second chunk)
+        const int rq = (PAIR && q == 2) ? -1 : 128 * I + 32 * q - 1;
+        // 32-column groups of the diagonal block this quadrant's rows see
+        // (a chunk pair's second chunk sees none of the first's)
+        auto visible = [&](int gi) { return gi <= q && !(PAIR && q >= 2 && gi < 2); };
 
         bool ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
         tc::tc_fence_after();
@@ -495,7 +555,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             for (int t = 0; t < 2; ++t) {
                 if (t >= gpw) break;
                 const int gi = part * gpw + t;
-                if (gi > q) continue;
+                if (!visible(gi)) continue;
                 const int j = 128 * I + 32 * gi + lane;
                 const float wj = exp2f(fminf(gref - vG[j], kMildSpan)) * vDt[j];
                 wv[32 * t + lane] = wj > kWMax ? kWMax : wj;
@@ -522,7 +582,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             for (int t = 0; t < 2; ++t) {
                 if (t >= gpw) break;
                 const int gi = part * gpw + t;  // 32-column group 0..3 of the diagonal block
-                if (gi > q) {
+                if (!visible(gi)) {
                     uint32_t z[8];
 #pragma unroll
                     for (int x = 0; x < 8; ++x) z[x] = 0u;
@@ -676,11 +736,16 @@ int lcm_small(int a, int b) {
     return m;
 }
 
+// Chunks of 64 tokens run as pairs spanning 128 rows.
+bool is_pair(const Geom& g) { return g.chunk == 64; }
+int row_blocks(const Geom& g) { return is_pair(g) ? 1 : (int)(g.chunk / 128); }
+
 bool plan_layout(const Geom& g, int I, int vs, int nstr, uint32_t off_CB10, CoLayout& L) {
-    const int T = (int)g.chunk, S = (int)g.dstate, H = (int)g.headdim / vs, Tj = 128 * (I + 1);
+    const int T = 128 * row_blocks(g), S = (int)g.dstate, H = (int)g.headdim / vs, Tj = 128 * (I + 1);
+    const int nh_tiles = is_pair(g) ? 2 : 1;  // states per stage
     L.off_stage = off_CB10 + (I == 1 ? 32768u : 0u);
     L.off_h_in_stage = (uint32_t)(Tj * H * 2);
-    L.off_vec_in_stage = L.off_h_in_stage + (uint32_t)(S * H * 2);
+    L.off_vec_in_stage = L.off_h_in_stage + (uint32_t)(nh_tiles * S * H * 2);
     const uint32_t vec_bytes = (uint32_t)(2 * T + 4) * 4;
     L.stage_bytes = (L.off_vec_in_stage + vec_bytes + 1023) / 1024 * 1024;  // swizzled tiles: 1024-aligned
     for (int nst = kMaxStages; nst >= 1; --nst) {
@@ -708,13 +773,13 @@ bool plan_smem(const Geom& g, int vs, CoTcParams& p) {
     if (vs != 1 && !(vs == 2 && g.headdim == 128)) return false;
     p.nstr = (g.headdim / vs == 64) ? 2 : 1;
     p.off_C = 0;
-    p.off_CB10 = p.off_C + 128 * (uint32_t)g.dstate * 2;
+    p.off_CB10 = p.off_C + (is_pair(g) ? 2u : 1u) * 128 * (uint32_t)g.dstate * 2;
     p.smem_bytes = 0;
-    for (int I = 0; I < (int)(g.chunk / 128); ++I) {
+    for (int I = 0; I < row_blocks(g); ++I) {
         if (!plan_layout(g, I, vs, p.nstr, p.off_CB10, p.lay[I])) return false;
         if (p.lay[I].smem_bytes > p.smem_bytes) p.smem_bytes = p.lay[I].smem_bytes;
     }
-    if (g.chunk == 128) p.lay[1] = p.lay[0];  // unused
+    if (row_blocks(g) == 1) p.lay[1] = p.lay[0];  // unused
     return true;
 }
 
@@ -737,30 +802,43 @@ int pick_vs(const Geom& g) {
     }
     const bool whole = plan_smem(g, 1, p);
     bool deep = whole;
-    for (int I = 0; whole && I < (int)(g.chunk / 128); ++I) deep = deep && p.lay[I].nst >= 2;
+    for (int I = 0; whole && I < row_blocks(g); ++I) deep = deep && p.lay[I].nst >= 2;
     if (deep) return 1;
     if (plan_smem(g, 2, p)) return 2;
     return whole ? 1 : 0;
+}
+
+// The geometry of the CTAs' row blocks: a pair of 64-token chunks is one
+// block of 128 rows.
+Geom block_geom(const Geom& g) {
+    Geom gb = g;
+    if (is_pair(g)) {
+        gb.chunk = 128;
+        gb.nchunks = (g.seqlen + 127) / 128;
+    }
+    return gb;
 }
 
 }  // namespace
 
 // Shapes the tensor-core stage-3 kernel covers; others use the CUDA-core kernel.
 bool chunk_out_tc_fits(const Geom& g) {
-    if (g.chunk != 128 && g.chunk != 256) return false;
+    if (g.chunk != 64 && g.chunk != 128 && g.chunk != 256) return false;
     if (g.headdim != 64 && g.headdim != 128) return false;
     if (g.dstate != 64 && g.dstate != 128 && g.dstate != 256) return false;
     if (g.batch * g.nheads * g.nchunks * g.dstate >= (int64_t(1) << 31)) return false;
     if (g.batch * g.seqlen >= (int64_t(1) << 31)) return false;
-    // grid.x = head blocks x row blocks x chunks (at most nheads * 2 * nchunks)
-    if (g.nheads * (g.chunk / 128) * g.nchunks >= (int64_t(1) << 31)) return false;
+    // grid.x = head blocks x row blocks x row-block chunks (at most nheads * 2 * nchunks)
+    const Geom gb = block_geom(g);
+    if (g.nheads * row_blocks(g) * gb.nchunks >= (int64_t(1) << 31)) return false;
     return pick_vs(g) != 0;
 }
 
 cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream_t st) {
     CoTcParams p{};
-    p.g = g;
-    p.T = (int)g.chunk;
+    p.g = block_geom(g);
+    p.T = 128 * row_blocks(g);
+    p.h_chunks = g.nchunks;
     const int vs = pick_vs(g);
     if (vs == 0 || !plan_smem(g, vs, p)) return cudaErrorInvalidConfiguration;
     p.nhb = pick_heads_per_cta(g, vs);
@@ -782,8 +860,9 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
         const uint64_t dims[4] = {S, G, L, (uint64_t)g.batch};
         const uint64_t strides[3] = {S * 2, G * S * 2, L * G * S * 2};
         const uint32_t box[4] = {64, 1, 128, 1};
+        const uint32_t box_c[4] = {64, 1, is_pair(g) ? 64u : 128u, 1};  // C of a pair: one chunk per box
         if (!make_tmap_bf16(&tm_b, a.B, 4, dims, strides, box)) return cudaErrorInvalidValue;
-        if (!make_tmap_bf16(&tm_c, a.C, 4, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_tmap_bf16(&tm_c, a.C, 4, dims, strides, box_c)) return cudaErrorInvalidValue;
     }
     {
         const uint64_t rows = (uint64_t)g.batch * nh * g.nchunks * S;
@@ -792,13 +871,16 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
         const uint32_t box[2] = {64, (uint32_t)S};
         if (!make_tmap_bf16(&tm_h, a.chunk_states, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    auto kern = (g.headdim == 64)
-                    ? (p.T == 256 ? k_chunk_out_tc<64, 256, 1> : k_chunk_out_tc<64, 128, 1>)
-                    : (vs == 2 ? (p.T == 256 ? k_chunk_out_tc<64, 256, 2> : k_chunk_out_tc<64, 128, 2>)
-                               : (p.T == 256 ? k_chunk_out_tc<128, 256, 1> : k_chunk_out_tc<128, 128, 1>));
+    auto kern = is_pair(g)
+                    ? (g.headdim == 64 ? k_chunk_out_tc<64, 128, 1, true>
+                                       : (vs == 2 ? k_chunk_out_tc<64, 128, 2, true> : k_chunk_out_tc<128, 128, 1, true>))
+                : (g.headdim == 64)
+                    ? (p.T == 256 ? k_chunk_out_tc<64, 256, 1, false> : k_chunk_out_tc<64, 128, 1, false>)
+                    : (vs == 2 ? (p.T == 256 ? k_chunk_out_tc<64, 256, 2, false> : k_chunk_out_tc<64, 128, 2, false>)
+                               : (p.T == 256 ? k_chunk_out_tc<128, 256, 1, false> : k_chunk_out_tc<128, 128, 1, false>));
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((int64_t)p.head_blocks * (p.T / 128) * g.nchunks), (unsigned)g.batch);
+    dim3 grid((unsigned)((int64_t)p.head_blocks * (p.T / 128) * p.g.nchunks), (unsigned)g.batch);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);

@@ -189,6 +189,7 @@ TC_SHAPES = [
     Workload("tc_t256_h64", 2, 640, 4, 64, 128, 1, 256, init_state=True),
     Workload("tc_t128_h128_s256_g2", 1, 384, 4, 128, 256, 2, 128, init_state=True),
     Workload("tc_t128_h64_s64_ragged", 2, 333, 6, 64, 64, 3, 128, init_state=True),
+    Workload("tc_t64_h64_odd_chunks", 2, 300, 4, 64, 128, 1, 64, init_state=True),
 ]
 
 
@@ -223,6 +224,7 @@ STRONG_SHAPES = [
     Workload("strong_t128_h64", 1, 512, 6, 64, 64, 2, 128, init_state=True),
     Workload("strong_t128_h128_s256", 1, 384, 6, 128, 256, 3, 128, init_state=True),
     Workload("strong_t256_ragged", 1, 650, 6, 64, 128, 1, 256),
+    Workload("strong_t64_h64", 1, 500, 6, 64, 128, 2, 64, init_state=True),
 ]
 
 

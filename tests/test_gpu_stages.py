@@ -26,6 +26,11 @@ SHAPES = [
     ("bf16_t256_ragged", 2, 700, 2, 64, 128, 1, 256, "bf16", False),
     ("bf16_h128_s256", 1, 256, 4, 128, 256, 2, 128, "bf16", True),
     ("bf16_t128_ragged", 1, 333, 4, 128, 64, 4, 128, "bf16", True),
+    # chunks of 64 run in pairs in the tensor-core output kernel: an even and
+    # an odd chunk count (the last pair then holds one chunk), 128-wide heads
+    ("bf16_t64_pairs", 2, 384, 4, 64, 128, 2, 64, "bf16", True),
+    ("bf16_t64_odd_chunks", 1, 300, 3, 64, 64, 1, 64, "bf16", False),
+    ("bf16_t64_h128_s256", 1, 256, 4, 128, 256, 2, 64, "bf16", True),
 ]
 
 
@@ -169,6 +174,7 @@ STRONG = [
     ("strong_t256", 2, 512, 6, 64, 128, 1, 256, "bf16", True),
     ("strong_t128_h128", 1, 384, 6, 128, 256, 2, 128, "bf16", True),
     ("strong_t256_ragged", 1, 600, 6, 64, 64, 3, 256, "bf16", False),
+    ("strong_t64_pairs", 1, 448, 6, 64, 128, 1, 64, "bf16", True),
 ]
 
 
@@ -205,6 +211,7 @@ SPLIT = [
     ("h128_t256_s128", 2, 512, 2, 128, 128, 1, 256, "bf16", False),
     ("h128_t256_s256_ragged", 1, 700, 3, 128, 256, 1, 256, "bf16", True),
     ("h128_t128_s64_groups", 2, 300, 8, 128, 64, 2, 128, "bf16", True),
+    ("h128_t64_s64_pairs", 1, 320, 2, 128, 64, 1, 64, "bf16", True),
 ]
 
 
