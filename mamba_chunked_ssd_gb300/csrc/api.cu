@@ -146,6 +146,12 @@ mamba2_status run_chunk_out(const mamba2_shape& s, const ChunkOutArgs& a, cudaSt
     return from_cuda(launch_chunk_out(g, s.dtype == MAMBA2_BF16, a, st));
 }
 
+// Segments of the forward pass's state pass (bf16 on tensor cores only).
+int fwd_segments(const mamba2_shape& s) {
+    if (s.dtype != MAMBA2_BF16 || s.batch == 0 || s.seqlen == 0) return 1;
+    return state_pass_segments(make_geom(s));
+}
+
 }  // namespace m2
 
 using namespace m2;
@@ -194,7 +200,8 @@ mamba2_status mamba2_chunk_out(const mamba2_shape* shape, const void* x, const f
 size_t mamba2_ssd_fwd_workspace_size(const mamba2_shape* shape) {
     if (check_shape(shape) != MAMBA2_OK) return 0;
     const Sizes z = sizes_of(*shape);
-    return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256));
+    const int64_t seg = fwd_segments(*shape) > 1 ? state_pass_segment_bytes(make_geom(*shape)) : 0;
+    return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(seg, 256));
 }
 
 mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const float* dt,
@@ -232,7 +239,21 @@ mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const flo
     // dependent launch); they wait for it before reading its output
     StatePassArgs sp{x, dt, B, G, initial_state, cs, final_state};
     sp.pdl = true;
-    if ((rc = run_state_pass(*shape, sp, st)) != MAMBA2_OK) return rc;
+    const int nseg = fwd_segments(*shape);
+    if (nseg > 1) {
+        // few (batch, head) pairs: stage 2 over sequence segments (summary,
+        // carry, segment pass), so that every SM walks a part of a sequence
+        float* seg = reinterpret_cast<float*>(ws + round_up(z.G, 256) + round_up(z.cs, 256));
+        sp.segments = nseg;
+        sp.seg_states = seg;
+        sp.summary = true;
+        if ((rc = from_cuda(launch_state_pass_tc(g, sp, st))) != MAMBA2_OK) return rc;
+        if ((rc = from_cuda(launch_state_carry(g, G, seg, nseg, true, st))) != MAMBA2_OK) return rc;
+        sp.summary = false;
+        if ((rc = from_cuda(launch_state_pass_tc(g, sp, st))) != MAMBA2_OK) return rc;
+    } else if ((rc = run_state_pass(*shape, sp, st)) != MAMBA2_OK) {
+        return rc;
+    }
     ChunkOutArgs co{x, dt, B, C, D, G, cs, y};
     co.pdl = true;
     return run_chunk_out(*shape, co, st);

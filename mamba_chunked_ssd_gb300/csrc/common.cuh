@@ -66,6 +66,12 @@ struct StatePassArgs {
     // Launch with programmatic stream serialization (the forward pass: the
     // kernel may start while stage 1 runs and waits for it before reading G).
     bool pdl = false;
+    // Sequence segments (tensor-core kernel only, k_state_pass_tc.cu): with
+    // segments > 1 the launch is the summary pass (summary) or the segment
+    // pass over seg_states, [b, nh, segments - 1, S, H] fp32.
+    int segments = 1;
+    bool summary = false;
+    float* seg_states = nullptr;
 };
 
 struct ChunkOutArgs {
@@ -120,6 +126,13 @@ bool chunk_out_tc_fits(const Geom& g);
 cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream_t st);
 bool state_pass_tc_fits(const Geom& g);
 cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStream_t st);
+// Segments the forward pass splits each sequence into for stage 2 (1: one
+// pass over the whole sequence), the bytes of their states, and the carry
+// between the summary and segment passes.
+int state_pass_segments(const Geom& g);
+int64_t state_pass_segment_bytes(const Geom& g);
+cudaError_t launch_state_carry(const Geom& g, const float* G, float* seg_states, int nseg, bool pdl,
+                               cudaStream_t st);
 
 bool ssd_fused_fits(const Geom& g);
 cudaError_t launch_ssd_fused(const Geom& g, const FusedArgs& a, cudaStream_t st);

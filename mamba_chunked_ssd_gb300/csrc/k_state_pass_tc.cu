@@ -22,6 +22,21 @@
 // The weighted-operand fold applies the blog's "pre-multiplied operand" to X
 // instead of B (same product; X is the smaller per-head tile).  States past
 // dstate (when dstate = 64) are zero-filled by TMA and never stored.
+//
+// Sequence segments.  When there are too few (batch, head) pairs to fill the
+// GPU, the forward pass splits each sequence into segments of whole chunks
+// and runs this kernel twice around a short carry (k_state_carry below):
+//   summary pass  every segment but the last walks its chunks from a zero
+//                 state (segment 0 from the initial state) and writes only its
+//                 end state;
+//   carry         H_1 = end state of segment 0, and for k >= 1
+//                 H_{k+1} = exp2(D_k) H_k + (end state of segment k),
+//                 D_k being the sum of G_last over segment k's chunks: the
+//                 state entering each segment, by the jump formula;
+//   segment pass  every segment walks its chunks from its entering state,
+//                 storing the chunk states; the last one writes final_state.
+// The chunk states are those of one pass over the whole sequence; only the
+// order of the fp32 sums at segment boundaries differs.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap_host.cuh"
@@ -36,8 +51,16 @@ constexpr int kKb = 64;  // tokens per sub-block
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;
 
+// What a launch computes (sequence segments: see above).
+enum SpMode : int { kWholeSequence = 0, kSegmentSummary = 1, kSegmentPass = 2 };
+
 struct SpTcParams {
     Geom g;
+    int mode;           // SpMode
+    int nseg;           // segments of a sequence (1 for kWholeSequence)
+    int cps;            // chunks per segment
+    int seg_grid;       // segments this launch covers: nseg, or nseg - 1 for the summary
+    float* seg_states;  // [b, nh, nseg - 1, S, H] fp32: segment end states, then entering states
     int nsb;            // sub-blocks per chunk = chunk / 64
     int nst;            // ring stages
     uint32_t stage_bytes, off_x_in_stage, off_w_in_stage, off_stg, off_bar, smem_bytes, tmem_cols;
@@ -80,12 +103,16 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int mt = blockIdx.x;              // 128-row tile of the state
     const int h = blockIdx.y;
-    const int64_t b = blockIdx.z;
+    const int64_t b = blockIdx.z / (unsigned)p.seg_grid;
+    const int seg = (int)(blockIdx.z % (unsigned)p.seg_grid);
     const int64_t bh = b * g.nheads + h;
     const int grp = (int)(h / g.heads_per_group);
     const int S = (int)g.dstate;
     constexpr int nsb = T / kKb;              // sub-blocks per chunk
-    const int nsub = (int)g.nchunks * nsb;  // total sub-blocks
+    // this CTA's chunks [c_begin, c_begin + nchl)
+    const int c_begin = seg * p.cps;
+    const int nchl = (int)imin64(p.cps, g.nchunks - c_begin);
+    const int nsub = nchl * nsb;  // sub-blocks of those chunks
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + p.off_bar + kNumBars * 8);
@@ -134,7 +161,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (lane == 0) w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], slot_phase, abort_flag);
                 if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) { ok = false; break; }
             }
-            const int c = u / nsb, sb = u % nsb;
+            const int c = c_begin + u / nsb, sb = u % nsb;
             const int64_t t0 = (int64_t)c * T;
             const int tc = (int)imin64(T, g.seqlen - t0);
             const int tok = (int)(t0 + sb * kKb);
@@ -263,13 +290,21 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const int64_t t0 = (int64_t)c * T;
                 return Gbh[t0 + imin64(T, g.seqlen - t0) - 1];
             };
-            // h <- initial state (or zeros)
+            // the entering state of a later segment comes from the carry kernel
+            tc::griddep_wait();
+            // h <- initial state (segment 0), the segment's entering state
+            // (segment pass), or zeros
+            const float* h_in = nullptr;
+            if (seg == 0)
+                h_in = p.init ? p.init + bh * S * H : nullptr;
+            else if (p.mode == kSegmentPass)
+                h_in = p.seg_states + (bh * (p.nseg - 1) + seg - 1) * S * H;
 #pragma unroll 1
             for (int m = 0; m < H / 16; ++m) {
                 uint32_t r[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    r[e] = __float_as_uint((valid && p.init) ? p.init[(bh * S + s) * H + 16 * m + e] : 0.f);
+                    r[e] = __float_as_uint((valid && h_in) ? h_in[s * H + 16 * m + e] : 0.f);
                 tc::tmem_st16(tm_h + lane_base + 16 * m, r);
             }
             tc::tmem_wait_st();
@@ -280,19 +315,34 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             uint8_t* stg = smem + p.off_stg;
             const int hrow = (q & 1) * 32 + lane;  // row inside the 64-row tile
             const bool leader = (q == 0 && lane == 0);
-            tc::griddep_wait();  // G comes from the previous kernel
-            float gl_next = glast_of(0);
+            const bool store = p.mode != kSegmentSummary;  // the summary keeps only the end state
+            float gl_next = glast_of(c_begin);
             // Every scan warp runs every iteration and every named barrier below,
             // whatever its own waits return, so no warp is left at a barrier;
             // after a failed wait a warp only skips the work.
-            for (int c = 0; c < (int)g.nchunks; ++c) {
-                const int ub = c & 1;
+            for (int cl = 0; cl < nchl; ++cl) {
+                const int c = c_begin + cl, ub = cl & 1;
                 const float alpha = exp2f(gl_next);
-                if (c + 1 < (int)g.nchunks) gl_next = glast_of(c + 1);
-                if (ok) ok = tc::mbar_wait(&bars[kBarUDone + ub], (c >> 1) & 1, abort_flag);
+                if (cl + 1 < nchl) gl_next = glast_of(c + 1);
+                if (ok) ok = tc::mbar_wait(&bars[kBarUDone + ub], (cl >> 1) & 1, abort_flag);
                 tc::tc_fence_after();
                 const int64_t row0 = (bh * g.nchunks + c) * S + mt * 128;  // first state row of the tile
-                for (int half = 0; half < 2; ++half) {
+                if (!store && ok) {
+                    // h <- exp2(G_last) h + U_c only
+#pragma unroll 1
+                    for (int m = 0; m < H / 16; ++m) {
+                        uint32_t hv[16], uv[16];
+                        tc::tmem_ld16_nowait(tm_h + lane_base + 16 * m, hv);
+                        tc::tmem_ld16_nowait(tm_u0 + ub * H + lane_base + 16 * m, uv);
+                        tc::tmem_wait_ld16(hv);
+                        tc::tmem_wait_ld16(uv);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
+                        tc::tmem_st16(tm_h + lane_base + 16 * m, hv);
+                    }
+                }
+                for (int half = 0; store && half < 2; ++half) {
                     if (mt * 128 + 64 * half >= S) break;  // dstate = 64: one half only
                     if (ok && (q >> 1) == half) {
 #pragma unroll 1
@@ -334,12 +384,19 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (ok && lane == 0) tc::mbar_arrive(&bars[kBarUFree + ub]);
             }
             if (leader) tc::bulk_wait_all();
-            if (ok && p.final_state && valid) {
+            // the end state: a summary's into its segment slot, the last
+            // segment's into final_state
+            float* h_out = nullptr;
+            if (p.mode == kSegmentSummary)
+                h_out = p.seg_states + (bh * (p.nseg - 1) + seg) * S * H;
+            else if (seg == p.nseg - 1 && p.final_state)
+                h_out = p.final_state + bh * S * H;
+            if (ok && h_out && valid) {
 #pragma unroll 1
                 for (int m = 0; m < H / 16; ++m) {
                     uint32_t hv[16];
                     tc::tmem_ld16(tm_h + lane_base + 16 * m, hv);
-                    float4* d4 = reinterpret_cast<float4*>(p.final_state + (bh * S + s) * H + 16 * m);
+                    float4* d4 = reinterpret_cast<float4*>(h_out + s * H + 16 * m);
 #pragma unroll
                     for (int s4 = 0; s4 < 4; ++s4)
                         d4[s4] = make_float4(__uint_as_float(hv[4 * s4]), __uint_as_float(hv[4 * s4 + 1]),
@@ -355,6 +412,36 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (warp == 1) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+// Carry over segments (see the file comment): one thread per state element
+// of one (batch, head); slot k of seg_states holds segment k's end state on
+// entry and the state entering segment k + 1 on exit.
+__global__ void __launch_bounds__(256) k_state_carry(const float* __restrict__ G, float* seg_states, Geom g,
+                                                    int nseg, int cps) {
+    __shared__ float decay[64];  // exp2(D_k), k < nseg - 1
+    const int64_t bh = blockIdx.y;
+    const int64_t SH = g.dstate * g.headdim;
+    tc::griddep_launch_dependents();  // the segment pass may start; it waits for this grid
+    tc::griddep_wait();               // G and the end states come from the previous kernels
+    if (threadIdx.x < nseg - 1) {
+        // D_k = sum of G_last over the chunks of segment k (all whole chunks:
+        // only the last segment, which is never carried out of, can be ragged)
+        const float* Gbh = G + bh * g.seqlen;
+        const int k = threadIdx.x;
+        float d = 0.f;
+        for (int c = k * cps; c < (k + 1) * cps; ++c) d += Gbh[(int64_t)c * g.chunk + g.chunk - 1];
+        decay[k] = exp2f(d);
+    }
+    __syncthreads();
+    const int64_t e = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (e >= SH) return;
+    float* slot = seg_states + bh * (nseg - 1) * SH + e;
+    float hk = slot[0];  // H_1: segment 0 started from the initial state
+    for (int k = 1; k < nseg - 1; ++k) {
+        hk = fmaf(decay[k], hk, slot[k * SH]);
+        slot[k * SH] = hk;
     }
 }
 
@@ -381,6 +468,29 @@ bool plan(const Geom& g, SpTcParams& p) {
 
 }  // namespace
 
+// SMs of the GPU the library is built for (GB300); sets how many segments
+// fill it.  A pure function of the shape, so the workspace size is too.
+constexpr int kTargetSms = 152;
+
+int state_pass_segments(const Geom& g) {
+    SpTcParams p;
+    if (!state_pass_tc_fits(g) || !plan(g, p)) return 1;
+    const int64_t per_sm = (p.tmem_cols == 256) ? 2 : 1;  // resident CTAs per SM
+    const int64_t base = g.batch * g.nheads * ((g.dstate + 127) / 128);
+    int64_t nseg = kTargetSms * per_sm / base;
+    // at least 4 chunks a segment, at most 64 segments; worth it from 3
+    // segments on (the summary and segment passes each walk one segment)
+    nseg = imin64(imin64(nseg, g.nchunks / 4), 64);
+    if (nseg < 3) return 1;
+    const int64_t cps = (g.nchunks + nseg - 1) / nseg;
+    return (int)((g.nchunks + cps - 1) / cps);
+}
+
+int64_t state_pass_segment_bytes(const Geom& g) {
+    const int nseg = state_pass_segments(g);
+    return nseg > 1 ? g.batch * g.nheads * (nseg - 1) * g.dstate * g.headdim * 4 : 0;
+}
+
 bool state_pass_tc_fits(const Geom& g) {
     if (g.chunk != 64 && g.chunk != 128 && g.chunk != 256) return false;
     if (g.headdim != 64 && g.headdim != 128) return false;
@@ -394,6 +504,18 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     SpTcParams p{};
     p.g = g;
     if (!plan(g, p)) return cudaErrorInvalidConfiguration;
+    p.mode = kWholeSequence;
+    p.nseg = 1;
+    p.cps = (int)g.nchunks;
+    p.seg_grid = 1;
+    p.seg_states = nullptr;
+    if (a.segments > 1) {
+        p.mode = a.summary ? kSegmentSummary : kSegmentPass;
+        p.nseg = a.segments;
+        p.cps = (int)((g.nchunks + a.segments - 1) / a.segments);
+        p.seg_grid = a.summary ? a.segments - 1 : a.segments;
+        p.seg_states = a.seg_states;
+    }
     p.dt = a.dt;
     p.G = a.G;
     p.init = a.init;
@@ -430,7 +552,7 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     const int mtiles = (int)((g.dstate + 127) / 128);
-    dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)g.batch);
+    dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)(g.batch * p.seg_grid));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
@@ -442,6 +564,22 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_b, tm_cs, p);
+}
+
+cudaError_t launch_state_carry(const Geom& g, const float* G, float* seg_states, int nseg, bool pdl,
+                               cudaStream_t st) {
+    const int cps = (int)((g.nchunks + nseg - 1) / nseg);
+    dim3 grid((unsigned)((g.dstate * g.headdim + 255) / 256), (unsigned)(g.batch * g.nheads));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_state_carry, G, seg_states, g, nseg, cps);
 }
 
 }  // namespace m2

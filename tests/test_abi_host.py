@@ -105,6 +105,22 @@ def test_workspace_size(lib):
     assert lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s)) == up(g_bytes) + up(cs_bytes)
 
 
+def test_workspace_size_with_sequence_segments(lib):
+    """Two (batch, head) pairs of bf16 heads fill few SMs, so the forward
+    pass splits each sequence of 32 chunks into 8 segments of 4 chunks and
+    keeps the states of the first 7 segments (fp32 S x H each) in the
+    workspace after G and the chunk states."""
+    s = _shape(batch=1, seqlen=4096, nheads=2, headdim=64, dstate=128, chunk_size=128, dtype_code=1)
+    up = lambda v: (v + 255) // 256 * 256
+    g_bytes = 1 * 2 * 4096 * 4
+    cs_bytes = 1 * 2 * 32 * 128 * 64 * 2
+    seg_bytes = 1 * 2 * 7 * 128 * 64 * 4
+    assert lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s)) == up(g_bytes) + up(cs_bytes) + up(seg_bytes)
+    # many (batch, head) pairs: one pass, no segment states
+    s = _shape(batch=4, seqlen=4096, nheads=64, headdim=64, dstate=128, chunk_size=128, dtype_code=1)
+    assert lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s)) == up(4 * 64 * 4096 * 4) + up(4 * 64 * 32 * 128 * 64 * 2)
+
+
 def test_ssd_fwd_rejects_small_or_misaligned_workspace(lib):
     s = _shape()
     need = lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s))

@@ -58,7 +58,7 @@ def test_small_full_compare(w):
 
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "mamba2_1p3b_layer", "long_seq_carried_state",
-                                  "large_state"])
+                                  "large_state", "blog_example"])
 def test_named_workload_full_size(name):
     w = WORKLOADS[name]
     inp = make_inputs(w)
@@ -253,6 +253,8 @@ GUARD_SHAPES = [
     Workload("guard_bf16_t256_ragged", 1, 777, 3, 64, 128, 1, 256, init_state=True),
     Workload("guard_bf16_t128_h128", 2, 200, 4, 128, 256, 2, 128),
     Workload("guard_bf16_t64", 1, 320, 2, 64, 128, 1, 64, init_state=True),
+    # few (batch, head) pairs: the state pass runs over sequence segments
+    Workload("guard_bf16_segments", 1, 2048, 2, 64, 128, 1, 128, init_state=True),
 ]
 
 
@@ -307,3 +309,57 @@ def test_more_chunks_than_a_grid_y_dimension():
         assert rel_err(np64(y[:, end - 1024:end]), r["y"][:, -1024:]) <= TOL[w.dtype], end
         if end == w.seqlen:
             assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype]
+
+
+# Few (batch, head) pairs: the forward pass runs stage 2 over sequence
+# segments (a summary pass from zero states, the carry of the entering states
+# by the jump formula, then every segment from its entering state).  Each
+# shape has 4 to 10 segments; ragged ends, chunk 64/128/256, both head widths,
+# a 256-wide state (two state tiles), and the decay stress.
+SEGMENT_SHAPES = [
+    Workload("seg_t128_h64_init", 1, 4096, 2, 64, 128, 1, 128, init_state=True),
+    Workload("seg_t256_s64_ragged", 2, 8192 - 77, 2, 64, 64, 1, 256, init_state=True),
+    Workload("seg_t64_h128_s256_groups", 1, 3000, 2, 128, 256, 2, 64),
+    Workload("seg_t128_h128_s128", 1, 3333, 3, 128, 128, 1, 128, init_state=True),
+]
+
+
+@pytest.mark.parametrize("w", SEGMENT_SHAPES, ids=[w.name for w in SEGMENT_SHAPES])
+def test_sequence_segments(w):
+    """y and the final state against the fp64 recurrence, in full."""
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    y, fin = _fwd(d, w)
+    r = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"],
+                              init=inp["initial_state"])
+    assert rel_err(np64(y), r["y"]) <= TOL[w.dtype]
+    assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype]
+
+
+def test_sequence_segments_strong_decay():
+    w = Workload("seg_strong", 1, 2048, 6, 64, 128, 1, 128, init_state=True)
+    inp = strong_decay(make_inputs(w))
+    d = to_dev(inp)
+    y, fin = _fwd(d, w)
+    r = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"],
+                              init=inp["initial_state"])
+    assert torch.isfinite(y.float()).all()
+    for h in range(w.nheads):
+        assert rel_err(np64(y[:, :, h]), r["y"][:, :, h]) <= TOL[w.dtype], h
+        assert rel_err(np64(fin[:, h]), r["final_state"][:, h]) <= TOL[w.dtype], h
+
+
+def test_sequence_segments_match_one_pass():
+    """The segmented forward pass and the stage entry points (stage 2 in one
+    pass over each sequence) give the same outputs up to rounding: both are
+    within the tolerance of the oracle and within it of each other."""
+    w = Workload("seg_vs_stages", 2, 4096, 2, 64, 128, 1, 256, init_state=True)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    y, fin = _fwd(d, w)
+    G = bd.mamba2_chunk_cumsum(d["dt"], d["A"], w.chunk_size)
+    cs, fin1 = bd.mamba2_state_pass(d["x"], d["dt"], d["B"], G, w.chunk_size, initial_state=d["initial_state"])
+    y1 = bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], G, cs, w.chunk_size, D=d["D"])
+    bd.mamba2_check_device_status()
+    assert rel_err(np64(y), np64(y1)) <= TOL[w.dtype]
+    assert rel_err(np64(fin), np64(fin1)) <= TOL[w.dtype]
