@@ -425,35 +425,53 @@ __global__ void __launch_bounds__(256) k_state_carry(const float* __restrict__ G
     const int64_t SH = g.dstate * g.headdim;
     tc::griddep_launch_dependents();  // the segment pass may start; it waits for this grid
     tc::griddep_wait();               // G and the end states come from the previous kernels
-    if (threadIdx.x < nseg - 1) {
+    {
         // D_k = sum of G_last over the chunks of segment k (all whole chunks:
-        // only the last segment, which is never carried out of, can be ragged)
+        // only the last segment, which is never carried out of, can be ragged);
+        // warp w sums segments w, w + 8, ..., its lanes over strided chunks
         const float* Gbh = G + bh * g.seqlen;
-        const int k = threadIdx.x;
-        float d = 0.f;
-        for (int c = k * cps; c < (k + 1) * cps; ++c) d += Gbh[(int64_t)c * g.chunk + g.chunk - 1];
-        decay[k] = exp2f(d);
+        const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+        for (int k = w; k < nseg - 1; k += 8) {
+            float d = 0.f;
+            for (int c = k * cps + lane; c < (k + 1) * cps; c += 32) d += Gbh[(int64_t)c * g.chunk + g.chunk - 1];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            if (lane == 0) decay[k] = exp2f(d);
+        }
     }
     __syncthreads();
     const int64_t e = (int64_t)blockIdx.x * 256 + threadIdx.x;
     if (e >= SH) return;
     float* slot = seg_states + bh * (nseg - 1) * SH + e;
     float hk = slot[0];  // H_1: segment 0 started from the initial state
-    for (int k = 1; k < nseg - 1; ++k) {
-        hk = fmaf(decay[k], hk, slot[k * SH]);
-        slot[k * SH] = hk;
+    // eight end states are loaded before any is overwritten, so the loads
+    // overlap instead of waiting behind the stores
+    for (int k0 = 1; k0 < nseg - 1; k0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = (k0 + i < nseg - 1) ? slot[(k0 + i) * SH] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (k0 + i < nseg - 1) {
+                hk = fmaf(decay[k0 + i], hk, v[i]);
+                slot[(k0 + i) * SH] = hk;
+            }
+        }
     }
 }
 
-bool plan(const Geom& g, SpTcParams& p) {
+// Ring plan.  Two CTAs share an SM when TMEM allows and the grid has enough
+// CTAs to use them; a grid of at most one CTA per SM (ctas_per_sm_cap = 1)
+// gets the whole shared memory, i.e. a deeper ring.
+bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2) {
     const int H = (int)g.headdim;
     p.nsb = (int)(g.chunk / kKb);
     p.off_x_in_stage = 2 * kKb * 128;
     p.off_w_in_stage = p.off_x_in_stage + (H / 64) * kKb * 128;
     p.stage_bytes = p.off_w_in_stage + 1024;  // G[64], dt[64], G_last; padded to keep stages 1 KB aligned
     p.tmem_cols = (3 * H <= 256) ? 256 : 512;
-    // two CTAs per SM when TMEM allows, else one with a deeper ring
-    const uint32_t budget = (p.tmem_cols == 256) ? (kSmemLimit / 2 - 2048) : kSmemLimit;
+    const bool two = p.tmem_cols == 256 && ctas_per_sm_cap >= 2;
+    const uint32_t budget = two ? (kSmemLimit / 2 - 2048) : kSmemLimit;
     const uint32_t fixed = kNumBars * 8 + 64 + 1024;
     const uint32_t stg_bytes = (uint32_t)(H / 64) * 8192;  // 64 rows x H bf16, boxes of 64 columns
     int nst = (int)((budget - fixed - stg_bytes) / p.stage_bytes);
@@ -503,7 +521,10 @@ bool state_pass_tc_fits(const Geom& g) {
 cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStream_t st) {
     SpTcParams p{};
     p.g = g;
-    if (!plan(g, p)) return cudaErrorInvalidConfiguration;
+    const int mtiles = (int)((g.dstate + 127) / 128);
+    const int seg_grid = a.segments > 1 ? (a.summary ? a.segments - 1 : a.segments) : 1;
+    const int64_t ctas = (int64_t)mtiles * g.nheads * g.batch * seg_grid;
+    if (!plan(g, p, ctas <= kTargetSms ? 1 : 2)) return cudaErrorInvalidConfiguration;
     p.mode = kWholeSequence;
     p.nseg = 1;
     p.cps = (int)g.nchunks;
@@ -551,7 +572,6 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
                                       : (g.chunk == 128 ? k_state_pass_tc<128, 128> : k_state_pass_tc<128, 64>));
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
-    const int mtiles = (int)((g.dstate + 127) / 128);
     dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)(g.batch * p.seg_grid));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
