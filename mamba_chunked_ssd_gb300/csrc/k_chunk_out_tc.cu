@@ -91,6 +91,11 @@ __host__ __device__ constexpr uint32_t col_z(int s, int H) { return 256u + 2u * 
 struct CoLayout {
     int nst;    // pipeline stages
     int nfill;  // stage-fill barriers, lcm(nst, nstr)
+    // B (read only by the C B^T products) overlays the first `rot` stage
+    // slots; ring stage i lives in slot (i + rot) % nst, so the first
+    // nst - rot heads fill slots B never touches, without waiting for C B^T
+    // (rot = 0: every fill waits for C B^T)
+    int rot;
     uint32_t off_stage, stage_bytes, off_h_in_stage, off_vec_in_stage, off_small, off_bar, smem_bytes;
 };
 
@@ -212,7 +217,9 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     uint8_t* sCB10 = smem + p.off_CB10;
     const CoLayout lay = I ? p.lay[1] : p.lay[0];
     uint8_t* sStage = smem + lay.off_stage;
-    uint8_t* sB = sCB10;  // B overlays CB_10 and the stages until the CB products are done
+    uint8_t* sB = sCB10;  // B overlays CB_10 and the first stage slots until the CB products are done
+    // shared-memory slot of ring stage i
+    auto slot_of = [&](int i) { return i + lay.rot >= lay.nst ? i + lay.rot - lay.nst : i + lay.rot; };
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.off_bar);
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + lay.off_bar + kNumBars * 8);
 
@@ -284,10 +291,8 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         // h_c and G come from the previous kernels
         tc::griddep_wait();
-        // the B area is reused by the stages
         bool ok = true;
-        if (lane == 0) ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
-        ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+        bool b_free = false;  // the slots under B may be filled (C B^T done)
         // stage, its reuse phase and the fill barrier as counters (no divisions)
         int st = 0, fill = 0;
         uint32_t slot_phase = 1;  // phase of the previous use of the stage
@@ -295,7 +300,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // through TMA stores; rows past the sequence end are clipped
         auto store_y = [&](int kp, int st_kp, uint32_t ph) -> bool {
             if (!tc::mbar_wait(&bars[kBarYReady + st_kp], ph, abort_flag)) return false;
-            const uint8_t* sY = sStage + st_kp * lay.stage_bytes;
+            const uint8_t* sY = sStage + slot_of(st_kp) * lay.stage_bytes;
             for (int cb = 0; cb < H / 64; ++cb)
                 tc::tma_store_4d(&tm_y, sY + cb * (Tj * 128) + I * 16384, (kp % VS) * H + cb * 64, h0 + kp / VS,
                                  (int)(t0 + 128 * I), (int)b);
@@ -315,7 +320,16 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     break;
                 }
             }
-            uint8_t* sX = sStage + st * lay.stage_bytes;
+            if (!b_free && (lay.rot == 0 || slot_of(st) < lay.rot)) {
+                // this slot lies under B: wait until the C B^T products have read it
+                if (lane == 0) ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
+                if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                b_free = true;
+            }
+            uint8_t* sX = sStage + slot_of(st) * lay.stage_bytes;
             uint8_t* sH = sX + lay.off_h_in_stage;
             float* vG = reinterpret_cast<float*>(sX + lay.off_vec_in_stage);  // G[T], dt[T], D
             float* vDt = vG + T;
@@ -409,8 +423,9 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(sStage), Tj * 128, 1024);
             const uint64_t stage_step = lay.stage_bytes >> 4;
             int st = sid0 % lay.nst, fill = sid0 % lay.nfill;
+            int pst = slot_of(st);  // its shared-memory slot
             uint32_t fill_phase = (sid0 / lay.nfill) & 1;
-            uint64_t dstage = st * stage_step;  // stage offset, in descriptor units
+            uint64_t dstage = pst * stage_step;  // slot offset, in descriptor units
             for (int k = sid0; ok && k < nvh; k += nstr) {
                 const int s = k % nstr, n = k / nstr;
                 const uint32_t tz = tmem + col_z(s, H), ty2 = tz + H;
@@ -445,8 +460,9 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc::mma_commit(&bars[kBarSlotFree + st]);
 #pragma unroll
                 for (int i = 0; i < nstr; ++i) {
-                    if (++st == lay.nst) {
-                        st = 0;
+                    if (++st == lay.nst) st = 0;
+                    if (++pst == lay.nst) {
+                        pst = 0;
                         dstage = 0;
                     } else {
                         dstage += stage_step;
@@ -536,7 +552,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         for (int k = sid; ok && k < nvh; k += nstr) {
             const int n = k / nstr;
             if (ok) ok = tc::mbar_wait(&bars[kBarFull + fill], fill_phase, abort_flag);
-            uint8_t* sX = sStage + st * lay.stage_bytes;
+            uint8_t* sX = sStage + slot_of(st) * lay.stage_bytes;
           if (ok) {
             const float* vG = reinterpret_cast<const float*>(sX + lay.off_vec_in_stage);
             const float* vDt = vG + T;
@@ -759,6 +775,10 @@ bool plan_layout(const Geom& g, int I, int vs, int nstr, uint32_t off_CB10, CoLa
         if (total <= (uint32_t)kSmemLimit) {
             L.nst = nst;
             L.nfill = lcm_small(nst, nstr);
+            // stage slots that B overlaps
+            const int64_t over = (int64_t)b_end - (int64_t)L.off_stage;
+            L.rot = over <= 0 ? 0 : (int)((over + L.stage_bytes - 1) / L.stage_bytes);
+            if (L.rot >= nst) L.rot = 0;  // B covers every slot
             L.off_small = off_small;
             L.off_bar = off_bar;
             L.smem_bytes = total;
