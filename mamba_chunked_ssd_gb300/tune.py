@@ -19,6 +19,10 @@ Each line: workload, candidate, mean stage time in microseconds (CUDA events
 on the launching stream, a 256 MiB L2 flush before every timed launch), and
 the candidate the default rule picks.  Inputs are seeded synthetic tensors
 drawn on the GPU.
+
+    python -m mamba_chunked_ssd_gb300.tune --profile WORKLOAD [--steps K]
+runs K forward passes (default 3) of one named workload and nothing else,
+for a profiler's launch list.
 """
 from __future__ import annotations
 
@@ -139,11 +143,35 @@ def fwd_path_rows(workloads, steps=10, warmup=3):
     return rows
 
 
+def profile_run(name, steps):
+    """`steps` forward passes of one named workload, synchronised at the end."""
+    import torch
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300.synthetic import WORKLOADS, make_inputs
+
+    w = WORKLOADS[name]
+    d = make_inputs(w, device="cuda")
+    shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
+    ws = torch.empty(max(bd.mamba2_ssd_fwd_workspace_size(shape), 1), device="cuda", dtype=torch.uint8)
+    y = torch.empty_like(d["x"])
+    for _ in range(steps):
+        bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size, D=d["D"],
+                          initial_state=d["initial_state"], y=y, workspace=ws)
+    torch.cuda.synchronize()
+    bd.mamba2_check_device_status()
+    print(f"{name}: {steps} forward passes")
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--json", action="store_true")
+    ap.add_argument("--profile", metavar="WORKLOAD", default=None)
     args = ap.parse_args()
+    if args.profile:
+        profile_run(args.profile, args.steps or 3)
+        return
+    args.steps = args.steps or 10
     from mamba_chunked_ssd_gb300.synthetic import WORKLOADS, sweep_workloads
     ws = [WORKLOADS["large_state"], WORKLOADS["long_seq_carried_state"], WORKLOADS["mamba2_1p3b_layer"],
           WORKLOADS["blog_example"]] + sweep_workloads(seeds=(0,))
