@@ -63,7 +63,16 @@ namespace {
 
 constexpr int kEpiWarps = 16;
 constexpr int kIssuer2 = 2 + kEpiWarps;  // warp 18: MMA issuer of head stream 1 (two streams)
-constexpr int kThreads = (kIssuer2 + 1) * 32;
+constexpr int kStoreWarp = kIssuer2 + 1;  // warp 19: TMA stores of y (deep rings)
+constexpr int kThreads = (kStoreWarp + 1) * 32;
+// Chunks of one row block (T = 128, and chunk pairs) with at least this many
+// stages send y out through a warp of its own as soon as it is written, and
+// the producer refills a stage once that store has read it.  Otherwise the
+// producer stores y itself, just before it refills the stage.  Measured on
+// GB300: the store warp makes stage 3 4-8 % faster for 128-token chunks
+// (state 64 or 128, 4-5 stages) and 1.5-2 % slower for 256-token chunks,
+// even when only their first row block uses it.
+constexpr int kStoreWarpMinStages = 4;
 constexpr int kSmemLimit = 232448;
 constexpr int kMaxStages = 5;
 constexpr int kMaxStreams = 2;
@@ -123,8 +132,8 @@ enum : int {
     kBarYDone = kBarPReady + kMaxStreams,      // [kMaxStreams]
     kBarYFree = kBarYDone + kMaxStreams,       // [kMaxStreams]
     kBarFull = kBarYFree + kMaxStreams,        // [kMaxFill]
-    kBarSlotFree = kBarFull + kMaxFill,        // [kMaxStages] the MMAs have read the stage
-    kBarYReady = kBarSlotFree + kMaxStages,    // [kMaxStages] y is written over the stage's X
+    kBarStored = kBarFull + kMaxFill,          // [kMaxStages] y's store has read the stage (store warp)
+    kBarYReady = kBarStored + kMaxStages,      // [kMaxStages] y is written over the stage's X
     kNumBars = kBarYReady + kMaxStages
 };
 
@@ -234,10 +243,11 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::mbar_init(&bars[kBarYFree + i], wps);
         }
         for (int i = 0; i < kMaxFill; ++i) tc::mbar_init(&bars[kBarFull + i], kFillArrivals);
-        // a stage is refilled once the MMAs have read it and the producer has
-        // stored the y the epilogue wrote over X_I in it
+        // a stage is refilled once the y the epilogue wrote over X_I in it has
+        // been stored (the epilogue read Z and Y2 first, so the MMAs are done
+        // with the stage too)
         for (int i = 0; i < kMaxStages; ++i) {
-            tc::mbar_init(&bars[kBarSlotFree + i], 1);
+            tc::mbar_init(&bars[kBarStored + i], 1);
             tc::mbar_init(&bars[kBarYReady + i], wps);
         }
         ctl->abort = 0;
@@ -265,6 +275,16 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     volatile int* abort_flag = &ctl->abort;
     const uint32_t x_bytes = (uint32_t)Tj * H * 2;
     const uint32_t h_bytes = (uint32_t)S * H * 2;
+    const bool store_warp = T == 128 && lay.nst >= kStoreWarpMinStages;
+    // y of virtual head k leaves ring stage st through TMA stores; rows past
+    // the sequence end are clipped
+    auto issue_y_store = [&](int k, int st) {
+        const uint8_t* sY = sStage + slot_of(st) * lay.stage_bytes;
+        for (int cb = 0; cb < H / 64; ++cb)
+            tc::tma_store_4d(&tm_y, sY + cb * (Tj * 128) + I * 16384, (k % VS) * H + cb * 64, h0 + k / VS,
+                             (int)(t0 + 128 * I), (int)b);
+        tc::bulk_commit();
+    };
 
     if (warp == 0) {
         // ============== TMA producer + per-head G / dt / D gather ==============
@@ -296,24 +316,23 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // stage, its reuse phase and the fill barrier as counters (no divisions)
         int st = 0, fill = 0;
         uint32_t slot_phase = 1;  // phase of the previous use of the stage
-        // y of virtual head kp leaves stage st (its previous use: phase `ph`)
-        // through TMA stores; rows past the sequence end are clipped
+        // without the store warp: y of head kp (ring stage st_kp, its use of
+        // phase ph) is stored here, just before the stage is refilled
         auto store_y = [&](int kp, int st_kp, uint32_t ph) -> bool {
             if (!tc::mbar_wait(&bars[kBarYReady + st_kp], ph, abort_flag)) return false;
-            const uint8_t* sY = sStage + slot_of(st_kp) * lay.stage_bytes;
-            for (int cb = 0; cb < H / 64; ++cb)
-                tc::tma_store_4d(&tm_y, sY + cb * (Tj * 128) + I * 16384, (kp % VS) * H + cb * 64, h0 + kp / VS,
-                                 (int)(t0 + 128 * I), (int)b);
-            tc::bulk_commit();
+            issue_y_store(kp, st_kp);
             return true;
         };
         for (int k = 0; ok && k < nvh; ++k) {
             if (k >= lay.nst) {
                 bool w_ok = true;
                 if (lane == 0) {
-                    w_ok = tc::mbar_wait(&bars[kBarSlotFree + st], slot_phase, abort_flag) &&
-                           store_y(k - lay.nst, st, slot_phase);
-                    tc::bulk_wait_read_all();  // the stage may be overwritten
+                    if (store_warp) {
+                        w_ok = tc::mbar_wait(&bars[kBarStored + st], slot_phase, abort_flag);
+                    } else {
+                        w_ok = store_y(k - lay.nst, st, slot_phase);
+                        tc::bulk_wait_read_all();  // the stage may be overwritten
+                    }
                 }
                 if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) {
                     ok = false;
@@ -370,12 +389,36 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             if (++fill == lay.nfill) fill = 0;
         }
         // the y of the last heads still sits in the stages
-        if (lane == 0) {
+        if (lane == 0 && !store_warp) {
             for (int kp = nvh > lay.nst ? nvh - lay.nst : 0; ok && kp < nvh; ++kp)
                 ok = store_y(kp, kp % lay.nst, (uint32_t)(kp / lay.nst) & 1u);
             tc::bulk_wait_all();
         }
         if (!ok && lane == 0) set_abort(ctl, p.status);
+    } else if (warp == kStoreWarp) {
+        // ============ y stores (TMA) in head order, for deep rings ============
+        // y of head k leaves as soon as the epilogue has written it; once the
+        // store has read the stage, the producer may refill it.
+        if (lane == 0 && store_warp) {
+            bool ok = true;
+            int st = 0;
+            uint32_t ph = 0;
+            for (int k = 0; k < nvh; ++k) {
+                if (!tc::mbar_wait(&bars[kBarYReady + st], ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                issue_y_store(k, st);
+                tc::bulk_wait_read_all();  // this warp only stores, so it waits here
+                tc::mbar_arrive(&bars[kBarStored + st]);
+                if (++st == lay.nst) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+            tc::bulk_wait_all();
+            if (!ok) set_abort(ctl, p.status);
+        }
     } else if (warp == 1 || (nstr == 2 && warp == kIssuer2)) {
         // ========================= MMA issuers (one per stream) =========================
         // Warp 1 issues the C B^T products and the per-head products of stream
@@ -457,7 +500,6 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 for (int k16 = 0; k16 < 8; ++k16)
                     tc::mma_bf16_ts(ty2, tmem + col_p(s) + k16 * 8, dX + I * 1024 + 128 * k16, id_y, k16 > 0);
                 tc::mma_commit(&bars[kBarYDone + s]);
-                tc::mma_commit(&bars[kBarSlotFree + st]);
 #pragma unroll
                 for (int i = 0; i < nstr; ++i) {
                     if (++st == lay.nst) st = 0;

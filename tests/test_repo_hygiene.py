@@ -55,5 +55,7 @@ def test_profiles_are_text_summaries_with_their_command():
         path = os.path.join(ROOT, f)
         assert os.path.getsize(path) < 16 * 1024, f
         text = open(path, encoding="utf-8").read()
-        assert "Command" in text and "python bench.py" in text, f
+        # the command runs committed files: the benchmark or the package's tools
+        assert "Command" in text, f
+        assert "python bench.py" in text or "python -m mamba_chunked_ssd_gb300." in text, f
         assert "--clock-control none" in text, f
