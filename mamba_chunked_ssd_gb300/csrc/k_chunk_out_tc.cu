@@ -26,14 +26,15 @@
 // Once per CTA (per group, shared by every head):
 //   CB_II = C_I B_I^T -> TMEM, causally masked in place;  for I = 1 also
 //   CB_10 = C_1 B_0^T, converted to bf16 into shared memory as an MMA operand.
-// Per head, with a = exp2(G_127) and v_j = exp2(G_127 - G_j) dt_j for I = 1
-// (a = 1 and no second term for I = 0):
-//   Z  = C_I (a h_c) + CB_10 (v . X_0)     tcgen05; a h_c and v . X_0 are
-//                                          scaled in place in the stage
+// Per head, with a = exp2(G_ref) and v_j = exp2(G_ref - G_j) dt_j for I = 1,
+// G_ref = G_127 for heads that decay by more than 2^-64 over the first 128
+// tokens and 0 otherwise (a = 1 and no second term for I = 0):
+//   Z  = C_I (a h_c) + CB_10 (v . X_0)     tcgen05; a h_c (a != 1) and v . X_0
+//                                          are scaled in place in the stage
 //   P  = CB_II . w_j                       epilogue, written to TMEM as bf16 and
 //                                          consumed there as operand A
 //   Y2 = P X_I                             tcgen05, A from TMEM
-//   y_i = exp2(G_i - G_ref) Z + u_i Y2 + D x_i  (G_ref = G_127 for I = 1, else 0)
+//   y_i = exp2(G_i - G_ref) Z + u_i Y2 + D x_i  (G_ref = 0 for I = 0)
 // with the decay of each row split at r, the last column before the row's
 // 32-row quadrant:  exp2(G_i - G_j) dt_j = u_i w_j,  u_i = exp2(G_i - G_r),
 // w_j = exp2(G_r - G_j) dt_j.  Both splits are exact identities; a_t <= 0
@@ -620,13 +621,23 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             }
             __syncwarp();
 
+            // Row block 1 takes the carried state and the first 128 tokens in one
+            // product, relative to a reference G_ref: Z = C_1 (exp2(G_ref) h_c) +
+            // CB_10 (v . X_0), v_j = exp2(G_ref - G_j) dt_j, and the rows' factor
+            // is exp2(G_i - G_ref).  G_ref = G_127 keeps every factor <= 1 but
+            // rescales h_c in place; when G_127 >= -64, G_ref = 0 leaves h_c as
+            // it is (v stays below 2^64 dt, far inside the bf16 range).
+            const float g127 = I == 1 ? vG[127] : 0.f;
+            const bool scale_h = I == 1 && !(g127 >= -64.f);  // NaN: the safe branch
+            const float gref_z = scale_h ? g127 : 0.f;
             if (I == 1) {
-                // a h_c and v . X_0, in place in the stage
-                uint8_t* sH = sX + lay.off_h_in_stage;
-                const float g127 = vG[127];
-                const float a = exp2f(g127);
-                for (int r = il; r < S; r += 128) scale_row4(sH, S * 128, r, part * 4, a);
-                const float vj = exp2f(g127 - vG[il]) * vDt[il];
+                // (exp2(G_ref) h_c and) v . X_0, in place in the stage
+                if (scale_h) {
+                    uint8_t* sH = sX + lay.off_h_in_stage;
+                    const float a = exp2f(g127);
+                    for (int r = il; r < S; r += 128) scale_row4(sH, S * 128, r, part * 4, a);
+                }
+                const float vj = exp2f(gref_z - vG[il]) * vDt[il];
                 scale_row4(sX, Tj * 128, il, part * 4, vj);
                 tc::fence_proxy_async_smem();
                 __syncwarp();
@@ -699,10 +710,10 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[kBarPReady + sid]);
 
-            // ---- y = exp2(G_i - G_ref) Z + u_i Y2 + D x_i   (G_ref = G_127 for I = 1, else 0),
+            // ---- y = exp2(G_i - G_ref) Z + u_i Y2 + D x_i   (G_ref above; 0 for I = 0),
             // written over x_i in the stage (each thread rewrites exactly the
             // 16-byte pieces it reads; Y2, the last reader of X_I, is done)
-            const float si = exp2f(grow - (I == 1 ? vG[127] : 0.f));
+            const float si = exp2f(grow - gref_z);
             const float ui = mild ? exp2f(grow - gref) : 1.f;
             const float dh = vDt[T];
             const float2 si2 = make_float2(si, si), ui2 = make_float2(ui, ui), d2 = make_float2(dh, dh);
