@@ -120,8 +120,12 @@ MAMBA2_API mamba2_status mamba2_chunk_out(const mamba2_shape* shape, const void*
                                const void* chunk_states, void* y, struct CUstream_st* stream);
 
 /* Bytes of device workspace mamba2_ssd_fwd needs for `shape` (0 for an
- * invalid shape).  The workspace holds intermediates only; its contents on
- * entry do not matter. */
+ * invalid shape): G, the chunk states and, for bf16 problems with too few
+ * (batch, head) pairs to fill the GPU, the fp32 states at the boundaries of
+ * the sequence segments its state pass runs over.  A pure function of the
+ * shape (and of the MAMBA2_STATE_SEGMENTS environment variable, "1" = no
+ * segments).  The workspace holds intermediates only; its contents on entry
+ * do not matter. */
 MAMBA2_API size_t mamba2_ssd_fwd_workspace_size(const mamba2_shape* shape);
 
 /* The whole forward pass [blog §Mamba-2 architecture, "three kernels"]:

@@ -856,13 +856,13 @@ bool plan_smem(const Geom& g, int vs, CoTcParams& p) {
     return true;
 }
 
-// The virtual-head split used for a shape (0: none fits).  Heads stay whole
-// when every row block gets at least two pipeline stages; otherwise a head of
-// 128 columns is split in two (which halves a stage), and only if that does not
-// fit either do whole heads run with one stage.  Measured on GB300 (stage-3
-// time, whole vs split, µs): state 64: 522 vs 575 (chunk 128), 604 vs 658
-// (chunk 256); state 128: 563 vs 600 (128), 855 vs 722 (256, one stage whole);
-// state 256: 962 vs 737 (128, one stage whole), split only at chunk 256.
+// The virtual-head split used for a shape (0: none fits).  Heads of 128
+// columns are split in two when the state is 128 or wider, and stay whole
+// with state 64; whichever fits is taken when the preferred one does not.
+// Measured on GB300 (stage-3 time, whole vs split, µs, every sweep length
+// within 1 %): state 64: 424 vs 523 (chunk 128), 539 vs 611 (chunk 256);
+// state 128: 571 vs 555 (128), 837 vs 677 (256); state 256: 974 vs 714
+// (128), split only (256, 1297).
 // MAMBA2_CHUNK_OUT_HEAD_SPLIT=1 or =2 forces that variant, for timing both on
 // one shape; where the forced variant does not fit, stage 3 runs on the
 // CUDA-core kernel.
@@ -873,12 +873,11 @@ int pick_vs(const Geom& g) {
         const int want = env[0] - '0';
         return plan_smem(g, want, p) ? want : 0;
     }
+    const bool split = plan_smem(g, 2, p);
     const bool whole = plan_smem(g, 1, p);
-    bool deep = whole;
-    for (int I = 0; whole && I < row_blocks(g); ++I) deep = deep && p.lay[I].nst >= 2;
-    if (deep) return 1;
-    if (plan_smem(g, 2, p)) return 2;
-    return whole ? 1 : 0;
+    if (g.dstate >= 128 && split) return 2;
+    if (whole) return 1;
+    return split ? 2 : 0;
 }
 
 // The geometry of the CTAs' row blocks: a pair of 64-token chunks is one

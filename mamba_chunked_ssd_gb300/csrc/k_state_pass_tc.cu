@@ -37,6 +37,8 @@
 //                 storing the chunk states; the last one writes final_state.
 // The chunk states are those of one pass over the whole sequence; only the
 // order of the fp32 sums at segment boundaries differs.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap_host.cuh"
@@ -493,6 +495,10 @@ constexpr int kTargetSms = 152;
 int state_pass_segments(const Geom& g) {
     SpTcParams p;
     if (!state_pass_tc_fits(g) || !plan(g, p)) return 1;
+    // MAMBA2_STATE_SEGMENTS=1 forces one pass over each sequence (for timing
+    // both on one shape)
+    const char* env = getenv("MAMBA2_STATE_SEGMENTS");
+    if (env && env[0] == '1' && env[1] == 0) return 1;
     const int64_t per_sm = (p.tmem_cols == 256) ? 2 : 1;  // resident CTAs per SM
     const int64_t base = g.batch * g.nheads * ((g.dstate + 127) / 128);
     int64_t nseg = kTargetSms * per_sm / base;

@@ -13,6 +13,9 @@ be checked against measurements:
   MAMBA2_FWD_PATH = staged | fused      the whole forward pass as separate
       stages or with the fused state-pass + output kernel (where it fits:
       bf16, head dim 64 in pairs of one group, state 128, chunk 128 or 256).
+  MAMBA2_STATE_SEGMENTS = 1             the forward pass's state pass in one
+      pass over each sequence, instead of over sequence segments where the
+      (batch, head) pairs are few.
 
 Usage (one GPU):  python -m mamba_chunked_ssd_gb300.tune [--steps K] [--json]
 Each line: workload, candidate, mean stage time in microseconds (CUDA events
@@ -39,6 +42,7 @@ if ROOT not in sys.path:
 FLUSH_BYTES = 256 << 20
 HEAD_SPLIT_ENV = "MAMBA2_CHUNK_OUT_HEAD_SPLIT"
 FWD_PATH_ENV = "MAMBA2_FWD_PATH"
+SEGMENTS_ENV = "MAMBA2_STATE_SEGMENTS"
 
 
 def _time(fn, steps, warmup, flush, stream):
@@ -143,6 +147,51 @@ def fwd_path_rows(workloads, steps=10, warmup=3):
     return rows
 
 
+def segment_rows(workloads, steps=10, warmup=3):
+    """Whole-pass time with the state pass over sequence segments (the
+    default where it applies) and in one pass, per workload where the
+    default splits the sequences."""
+    import torch
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+
+    bd.load_library()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    rows = []
+    saved = os.environ.pop(SEGMENTS_ENV, None)
+    try:
+        for w in workloads:
+            if w.dtype != "bf16":
+                continue
+            d = make_inputs(w, device="cuda")
+            shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
+            need = bd.mamba2_ssd_fwd_workspace_size(shape)
+            os.environ[SEGMENTS_ENV] = "1"
+            one = bd.mamba2_ssd_fwd_workspace_size(shape)
+            os.environ.pop(SEGMENTS_ENV, None)
+            if need == one:  # the default runs one pass: nothing to compare
+                del d
+                continue
+            ws = torch.empty(need, device="cuda", dtype=torch.uint8)
+            y = torch.empty_like(d["x"])
+            fn = lambda: bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size,  # noqa: E731
+                                           D=d["D"], initial_state=d["initial_state"], y=y, workspace=ws)
+            seg_us = _time(fn, steps, warmup, flush, stream)
+            os.environ[SEGMENTS_ENV] = "1"
+            one_us = _time(fn, steps, warmup, flush, stream)
+            os.environ.pop(SEGMENTS_ENV, None)
+            bd.mamba2_check_device_status()
+            rows.append({"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                         "chunk_size": w.chunk_size, "segments_us": seg_us, "one_pass_us": one_us})
+            del d, ws, y
+    finally:
+        os.environ.pop(SEGMENTS_ENV, None)
+        if saved is not None:
+            os.environ[SEGMENTS_ENV] = saved
+    return rows
+
+
 def profile_run(name, steps):
     """`steps` forward passes of one named workload, synchronised at the end."""
     import torch
@@ -175,10 +224,15 @@ def main():
     from mamba_chunked_ssd_gb300.synthetic import WORKLOADS, sweep_workloads
     ws = [WORKLOADS["large_state"], WORKLOADS["long_seq_carried_state"], WORKLOADS["mamba2_1p3b_layer"],
           WORKLOADS["blog_example"]] + sweep_workloads(seeds=(0,))
+    from mamba_chunked_ssd_gb300.synthetic import Workload
+    seg_ws = [WORKLOADS["blog_example"],
+              Workload("few_heads_t256", 1, 32768, 4, 64, 128, 1, 256),
+              Workload("few_heads_h128", 2, 16384, 4, 128, 128, 1, 128)]
     rows = head_split_rows(ws, steps=args.steps)
     paths = fwd_path_rows(ws, steps=args.steps)
+    segs = segment_rows(seg_ws, steps=args.steps)
     if args.json:
-        print(json.dumps({"head_split": rows, "fwd_path": paths}))
+        print(json.dumps({"head_split": rows, "fwd_path": paths, "segments": segs}))
         return
     print("Stage 3, heads of 128 columns:")
     print("| workload | whole heads (µs) | split heads (µs) | default (µs) |")
@@ -191,6 +245,12 @@ def main():
     print("|---|---|---|")
     for r in paths:
         print(f"| {r['workload']} | {r['staged_us']:.1f} | {r['fused_us']:.1f} |")
+    print()
+    print("State pass over sequence segments vs one pass (whole forward pass):")
+    print("| workload | segments (µs) | one pass (µs) |")
+    print("|---|---|---|")
+    for r in segs:
+        print(f"| {r['workload']} | {r['segments_us']:.1f} | {r['one_pass_us']:.1f} |")
 
 
 if __name__ == "__main__":
