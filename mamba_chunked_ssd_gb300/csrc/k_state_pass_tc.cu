@@ -4,7 +4,7 @@
 //     h_{c+1} = exp2(G_last) h_c + (w . B_c)^T X_c,   w_t = dt_t exp2(G_last - G_t).
 // GB300 design.  One CTA owns (batch, head, 128-row tile of the S x H state)
 // and walks the chunks in order:
-//   warp 0      producer: TMA of 64-token sub-blocks of B (the tile's 128
+//   warp 0      producer: TMA of 64- or 128-token sub-blocks of B (the tile's 128
 //               state columns) and of X into a ring of shared-memory stages;
 //               its lanes also gather the sub-block's G_t and dt_t and the
 //               chunk's G_last into the stage with cp.async, so the other
@@ -49,7 +49,12 @@ namespace {
 constexpr int kFoldWarps = 4;  // warps 2..5
 constexpr int kScanWarps = 4;  // warps 6..9, one per TMEM lane quadrant
 constexpr int kThreads = (2 + kFoldWarps + kScanWarps) * 32;
-constexpr int kKb = 64;  // tokens per sub-block
+// Tokens per sub-block (KB): 64, or 128 where one CTA runs per SM and the
+// chunk has at least 128 tokens.  Measured on GB300 (state pass alone):
+// 128-token sub-blocks are 11-14 % faster with one CTA per SM (4 stages of
+// 128 against 8 of 64), 9 % slower with two CTAs per SM (2 stages against 4);
+// 32-token sub-blocks were 25-70 % slower than 64 (the per-sub-block
+// hand-offs cost more than a deeper ring gains).
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;
 
@@ -63,7 +68,8 @@ struct SpTcParams {
     int cps;            // chunks per segment
     int seg_grid;       // segments this launch covers: nseg, or nseg - 1 for the summary
     float* seg_states;  // [b, nh, nseg - 1, S, H] fp32: segment end states, then entering states
-    int nsb;            // sub-blocks per chunk = chunk / 64
+    int kb;             // tokens per sub-block (64 or 128)
+    int nsb;            // sub-blocks per chunk = chunk / kb
     int nst;            // ring stages
     uint32_t stage_bytes, off_x_in_stage, off_w_in_stage, off_stg, off_bar, smem_bytes, tmem_cols;
     const float* dt;
@@ -93,9 +99,9 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
     if (status) atomicExch(status, kStatusTimeout);
 }
 
-// H (head dim) and T (chunk) are compile-time, so the sub-block count and the
-// box and chunk offsets fold into constants.
-template <int H, int T>
+// H (head dim), T (chunk) and KB (tokens per sub-block) are compile-time, so
+// the sub-block count and the box and chunk offsets fold into constants.
+template <int H, int T, int KB>
 __global__ void __launch_bounds__(kThreads, 2)
 k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_cs, const SpTcParams p) {
@@ -110,6 +116,9 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int64_t bh = b * g.nheads + h;
     const int grp = (int)(h / g.heads_per_group);
     const int S = (int)g.dstate;
+    constexpr int kKb = KB;
+    static_assert(KB == 64 || KB == 128, "sub-blocks of 64 or 128 tokens");
+    static_assert(T % KB == 0, "whole sub-blocks per chunk");
     constexpr int nsb = T / kKb;              // sub-blocks per chunk
     // this CTA's chunks [c_begin, c_begin + nchl)
     const int c_begin = seg * p.cps;
@@ -169,7 +178,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const int tok = (int)(t0 + sb * kKb);
             uint8_t* sB = smem + st * p.stage_bytes;
             uint8_t* sX = sB + p.off_x_in_stage;
-            float* sV = reinterpret_cast<float*>(sB + p.off_w_in_stage);  // G[64], dt[64], G_last
+            float* sV = reinterpret_cast<float*>(sB + p.off_w_in_stage);  // G[kKb], dt[kKb], G_last
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(&bars[kBarFull + st], (2 + H / 64) * x_box_bytes);
                 for (int kb = 0; kb < 2; ++kb)
@@ -183,14 +192,14 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // straight into the stage; each lane arrives on the stage barrier
             // once its copies have landed.
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
+            for (int r = 0; r < kKb / 32; ++r) {
                 const int tl = sb * kKb + lane + 32 * r;
                 const int tv = tl < tc ? tl : tc - 1;
                 tc::cp_async4(sV + lane + 32 * r, Gbh + t0 + tv, 4);
-                tc::cp_async4(sV + 64 + lane + 32 * r, p.dt + (b * g.seqlen + t0 + tv) * g.nheads + h,
+                tc::cp_async4(sV + kKb + lane + 32 * r, p.dt + (b * g.seqlen + t0 + tv) * g.nheads + h,
                               tl < tc ? 4u : 0u);
             }
-            if (lane == 0) tc::cp_async4(sV + 128, Gbh + t0 + tc - 1, 4);
+            if (lane == 0) tc::cp_async4(sV + 2 * kKb, Gbh + t0 + tc - 1, 4);
             tc::cp_async_mbar_arrive_noinc(&bars[kBarFull + st]);
         }
         if (!ok && lane == 0) set_abort(ctl, p.status);
@@ -243,20 +252,21 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         bool ok = true;
         if (warp < 2 + kFoldWarps) {
             // ================= weight fold (warps 2..5) =================
-            // Two threads per token row of a 64-token sub-block, each taking
-            // half of the row's 16-byte chunks (rotated to spread banks).
+            // 128 / kKb threads per token row of a sub-block, each taking an
+            // equal share of the row's 16-byte chunks (rotated to spread banks).
+            constexpr int tpr = 128 / kKb;
             const int ft = (warp - 2) * 32 + lane;  // 0..127
-            const int frow = ft >> 1, fh = ft & 1;
-            const int per = 4 * (H / 64);           // chunks per thread (4 or 8)
+            const int frow = ft / tpr, fh = ft % tpr;
+            const int per = 8 * (H / 64) / tpr;     // chunks per thread (2 to 8)
             int st = 0;
             uint32_t full_phase = 0;
             for (int u = 0; ok && u < nsub; ++u, st = (st + 1 == p.nst) ? (full_phase ^= 1u, 0) : st + 1) {
                 if (!tc::mbar_wait(&bars[kBarFull + st], full_phase, abort_flag)) { ok = false; break; }
                 const float* sV = reinterpret_cast<const float*>(smem + st * p.stage_bytes + p.off_w_in_stage);
-                const float w = sV[64 + frow] * exp2f(sV[128] - sV[frow]);  // w_t = dt_t exp2(G_last - G_t)
+                const float w = sV[kKb + frow] * exp2f(sV[2 * kKb] - sV[frow]);  // w_t = dt_t exp2(G_last - G_t)
                 uint8_t* rowp = smem + st * p.stage_bytes + p.off_x_in_stage + frow * 128;
 #pragma unroll
-                for (int f0 = 0; f0 < 8; f0 += 2) {  // two chunks in flight
+                for (int f0 = 0; f0 < 16; f0 += 2) {  // two chunks in flight
                     if (f0 >= per) break;
                     uint4 v[2];
 #pragma unroll
@@ -467,12 +477,15 @@ __global__ void __launch_bounds__(256) k_state_carry(const float* __restrict__ G
 // gets the whole shared memory, i.e. a deeper ring.
 bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2) {
     const int H = (int)g.headdim;
+    p.tmem_cols = (3 * H <= 256) ? 256 : 512;
+    const bool two = p.tmem_cols == 256 && ctas_per_sm_cap >= 2;
+    const int kKb = (!two && g.chunk >= 128) ? 128 : 64;
+    p.kb = kKb;
     p.nsb = (int)(g.chunk / kKb);
     p.off_x_in_stage = 2 * kKb * 128;
     p.off_w_in_stage = p.off_x_in_stage + (H / 64) * kKb * 128;
-    p.stage_bytes = p.off_w_in_stage + 1024;  // G[64], dt[64], G_last; padded to keep stages 1 KB aligned
-    p.tmem_cols = (3 * H <= 256) ? 256 : 512;
-    const bool two = p.tmem_cols == 256 && ctas_per_sm_cap >= 2;
+    // G[kKb], dt[kKb], G_last; padded to keep stages 1 KB aligned
+    p.stage_bytes = p.off_w_in_stage + ((2 * kKb + 1) * 4 + 1023) / 1024 * 1024;
     const uint32_t budget = two ? (kSmemLimit / 2 - 2048) : kSmemLimit;
     const uint32_t fixed = kNumBars * 8 + 64 + 1024;
     const uint32_t stg_bytes = (uint32_t)(H / 64) * 8192;  // 64 rows x H bf16, boxes of 64 columns
@@ -550,6 +563,7 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     p.final_state = a.final_state;
     p.status = device_status_word();
     const uint64_t H = g.headdim, S = g.dstate, nh = g.nheads, L = g.seqlen, G = g.ngroups;
+    const int kKb = p.kb;
     CUtensorMap tm_x, tm_b;
     {
         const uint64_t dims[4] = {H, nh, L, (uint64_t)g.batch};
@@ -572,10 +586,11 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
         if (!make_tmap_bf16(&tm_cs, a.chunk_states, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
     auto kern = (g.headdim == 64)
-                    ? (g.chunk == 256 ? k_state_pass_tc<64, 256>
-                                      : (g.chunk == 128 ? k_state_pass_tc<64, 128> : k_state_pass_tc<64, 64>))
-                    : (g.chunk == 256 ? k_state_pass_tc<128, 256>
-                                      : (g.chunk == 128 ? k_state_pass_tc<128, 128> : k_state_pass_tc<128, 64>));
+                    ? (g.chunk == 256 ? (kKb == 128 ? k_state_pass_tc<64, 256, 128> : k_state_pass_tc<64, 256, 64>)
+                       : g.chunk == 128 ? (kKb == 128 ? k_state_pass_tc<64, 128, 128> : k_state_pass_tc<64, 128, 64>)
+                                        : k_state_pass_tc<64, 64, 64>)
+                    : (g.chunk == 256 ? k_state_pass_tc<128, 256, 128>
+                       : g.chunk == 128 ? k_state_pass_tc<128, 128, 128> : k_state_pass_tc<128, 64, 64>);
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)(g.batch * p.seg_grid));
