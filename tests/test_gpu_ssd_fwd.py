@@ -363,3 +363,20 @@ def test_sequence_segments_match_one_pass():
     bd.mamba2_check_device_status()
     assert rel_err(np64(y), np64(y1)) <= TOL[w.dtype]
     assert rel_err(np64(fin), np64(fin1)) <= TOL[w.dtype]
+
+
+def test_sequence_segments_override_gives_one_pass(monkeypatch):
+    """MAMBA2_STATE_SEGMENTS=1 (one pass over each sequence) and the default
+    (segments) agree within the tolerance, and both match the oracle."""
+    w = Workload("seg_override", 1, 4096, 2, 64, 128, 1, 128, init_state=True)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    y_seg, fin_seg = _fwd(d, w)
+    monkeypatch.setenv("MAMBA2_STATE_SEGMENTS", "1")
+    y_one, fin_one = _fwd(d, w)
+    r = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"],
+                              init=inp["initial_state"])
+    for y, fin in ((y_seg, fin_seg), (y_one, fin_one)):
+        assert rel_err(np64(y), r["y"]) <= TOL[w.dtype]
+        assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype]
+    assert rel_err(np64(y_seg), np64(y_one)) <= TOL[w.dtype]

@@ -232,3 +232,23 @@ def test_chunk_out_head_split_variants(spec, variant, monkeypatch):
     assert rel_err(np64(y), y_ref) <= TOL[w.dtype]
     for h in range(w.nheads):
         assert rel_err(np64(y[:, :, h]), y_ref[:, :, h]) <= TOL[w.dtype], h
+
+
+@pytest.mark.parametrize("spec", [s for s in SHAPES if s[8] == "bf16"], ids=[s[0] for s in SHAPES if s[8] == "bf16"])
+def test_chunk_out_reads_every_chunk_state(spec):
+    """Random chunk states that no state pass would produce (each chunk's
+    independent of its neighbours) with x = 0: y is the carried-state term
+    alone, so every chunk must use its own state, including the second chunk
+    of a pair of 64-token chunks."""
+    w = _w(*spec)
+    inp = make_inputs(w)
+    inp["x"].zero_()
+    d = to_dev(inp)
+    G32, _, _ = _oracle_stage_inputs(inp, w)
+    g = torch.Generator().manual_seed(7)
+    cs = torch.randn(w.batch, w.nheads, w.nchunks, w.dstate, w.headdim, generator=g).to(d["x"].dtype)
+    y = bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], torch.from_numpy(G32).cuda(), cs.cuda(),
+                            w.chunk_size, D=d["D"])
+    bd.mamba2_check_device_status()
+    y_ref = oracle.chunk_out(inp["x"], inp["dt"], inp["B"], inp["C"], G32, cs, w.chunk_size, D=inp["D"])
+    assert rel_err(np64(y), y_ref) <= TOL[w.dtype]
