@@ -146,6 +146,12 @@ mamba2_status run_chunk_out(const mamba2_shape& s, const ChunkOutArgs& a, cudaSt
     return from_cuda(launch_chunk_out(g, s.dtype == MAMBA2_BF16, a, st));
 }
 
+// Whether the forward pass runs an fp32 problem's stage 3 on the tensor cores.
+bool fwd_f32_tensor_cores(const mamba2_shape& s) {
+    if (s.dtype != MAMBA2_F32 || s.batch == 0 || s.seqlen == 0) return false;
+    return use_f32_tensor_cores(make_geom(s), false);
+}
+
 // Segments of the forward pass's state pass (bf16 on tensor cores only).
 int fwd_segments(const mamba2_shape& s) {
     if (s.dtype != MAMBA2_BF16 || s.batch == 0 || s.seqlen == 0) return 1;
@@ -201,7 +207,11 @@ size_t mamba2_ssd_fwd_workspace_size(const mamba2_shape* shape) {
     if (check_shape(shape) != MAMBA2_OK) return 0;
     const Sizes z = sizes_of(*shape);
     const int64_t seg = fwd_segments(*shape) > 1 ? state_pass_segment_bytes(make_geom(*shape)) : 0;
-    return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(seg, 256));
+    // fp32 on the tensor cores: bf16 hi/lo planes of the chunk states, x, B, C
+    const int64_t split = fwd_f32_tensor_cores(*shape)
+                              ? round_up(z.cs, 256) + round_up(z.x, 256) + 2 * round_up(z.bc, 256)
+                              : 0;
+    return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(seg, 256) + split);
 }
 
 mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const float* dt,
@@ -234,6 +244,34 @@ mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const flo
         FusedArgs fa{x, dt, B, C, D, G, initial_state, y, final_state};
         fa.pdl = true;
         return from_cuda(launch_ssd_fused(g, fa, st));
+    }
+    if (fwd_f32_tensor_cores(*shape)) {
+        // fp32: x, B, C and (after stage 2) the chunk states as bf16 hi/lo
+        // planes, stage 3 on the tensor cores with three products per product
+        char* q = ws + round_up(z.G, 256) + round_up(z.cs, 256);
+        void* cs2 = q;
+        q += round_up(z.cs, 256);
+        void* x2 = q;
+        q += round_up(z.x, 256);
+        void* B2 = q;
+        q += round_up(z.bc, 256);
+        void* C2 = q;
+        const int64_t tok = shape->batch * shape->seqlen;
+        if ((rc = from_cuda(launch_split_bf16(static_cast<const float*>(x), x2, tok * shape->nheads,
+                                              shape->headdim, st))) != MAMBA2_OK ||
+            (rc = from_cuda(launch_split_bf16(static_cast<const float*>(B), B2, tok * shape->ngroups,
+                                              shape->dstate, st))) != MAMBA2_OK ||
+            (rc = from_cuda(launch_split_bf16(static_cast<const float*>(C), C2, tok * shape->ngroups,
+                                              shape->dstate, st))) != MAMBA2_OK)
+            return rc;
+        StatePassArgs sp{x, dt, B, G, initial_state, cs, final_state};
+        if ((rc = run_state_pass(*shape, sp, st)) != MAMBA2_OK) return rc;
+        if ((rc = from_cuda(launch_split_bf16(static_cast<const float*>(cs), cs2,
+                                              shape->batch * shape->nheads * g.nchunks,
+                                              shape->dstate * shape->headdim, st))) != MAMBA2_OK)
+            return rc;
+        const F32ChunkOutArgs co{x2, dt, B2, C2, D, G, cs2, static_cast<float*>(y)};
+        return from_cuda(launch_chunk_out_f32tc(g, co, st));
     }
     // stages 2 and 3 may start while the stage before them runs (programmatic
     // dependent launch); they wait for it before reading its output

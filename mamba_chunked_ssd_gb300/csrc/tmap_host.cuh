@@ -28,11 +28,11 @@ inline EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// Tiled bf16 map of `rank` dims (dims[0] innermost, contiguous), strides in
-// bytes for dims 1..rank-1, box sizes per dim, 128-byte swizzle, zero fill
-// outside the tensor.  Returns false if the driver rejects it.
-inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                           const uint64_t* strides, const uint32_t* box) {
+// Tiled map of `rank` dims (dims[0] innermost, contiguous), strides in bytes
+// for dims 1..rank-1, box sizes per dim, 128-byte swizzle, zero fill outside
+// the tensor.  Returns false if the driver rejects it.
+inline bool make_tmap(CUtensorMap* m, CUtensorMapDataType type, const void* base, int rank,
+                      const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     cuuint64_t gd[5], gs[4];
@@ -43,10 +43,20 @@ inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uin
         es[i] = 1;
     }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx,
+    CUresult r = fn(m, type, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx,
                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides, const uint32_t* box) {
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box);
+}
+
+inline bool make_tmap_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides, const uint32_t* box) {
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides, box);
 }
 
 }  // namespace m2

@@ -380,3 +380,61 @@ def test_sequence_segments_override_gives_one_pass(monkeypatch):
         assert rel_err(np64(y), r["y"]) <= TOL[w.dtype]
         assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype]
     assert rel_err(np64(y_seg), np64(y_one)) <= TOL[w.dtype]
+
+
+# fp32 problems with chunks of 128, head dim 64 or 128 and state 64 or 128
+# run stage 3 on the tensor cores with split-bf16 operands (three products per
+# product); each is compared in full with the fp64 recurrence at the fp32
+# tolerance, and with the CUDA-core path.
+F32_TC_SHAPES = [
+    Workload("fp32_tc_h64_s128_groups", 2, 384, 4, 64, 128, 2, 128, dtype="fp32", init_state=True),
+    Workload("fp32_tc_h128_s64_ragged", 1, 333, 3, 128, 64, 1, 128, dtype="fp32", init_state=True),
+    Workload("fp32_tc_32_heads", 1, 256, 32, 64, 64, 1, 128, dtype="fp32"),
+    Workload("fp32_tc_h128_s128", 2, 300, 2, 128, 128, 2, 128, dtype="fp32", init_state=True),
+]
+
+
+@pytest.mark.parametrize("w", F32_TC_SHAPES, ids=[w.name for w in F32_TC_SHAPES])
+def test_fp32_tensor_core_path(w, monkeypatch):
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    y, fin = _fwd(d, w)
+    r = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"],
+                              init=inp["initial_state"])
+    assert rel_err(np64(y), r["y"]) <= TOL["fp32"]
+    assert rel_err(np64(fin), r["final_state"]) <= TOL["fp32"]
+    for h in range(w.nheads):
+        assert rel_err(np64(y[:, :, h]), r["y"][:, :, h]) <= TOL["fp32"], h
+    monkeypatch.setenv("MAMBA2_FP32_PATH", "simt")
+    y_simt, _ = _fwd(d, w)
+    assert rel_err(np64(y), np64(y_simt)) <= TOL["fp32"]
+
+
+def test_fp32_tensor_core_path_strong_decay():
+    w = Workload("fp32_tc_strong", 1, 512, 6, 64, 128, 1, 128, dtype="fp32", init_state=True)
+    inp = strong_decay(make_inputs(w))
+    d = to_dev(inp)
+    y, fin = _fwd(d, w)
+    r = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"],
+                              init=inp["initial_state"])
+    assert torch.isfinite(y).all()
+    for h in range(w.nheads):
+        assert rel_err(np64(y[:, :, h]), r["y"][:, :, h]) <= TOL["fp32"], h
+    assert rel_err(np64(fin), r["final_state"]) <= TOL["fp32"]
+
+
+def test_fp32_tensor_core_path_stays_in_its_buffers():
+    w = Workload("fp32_tc_guard", 1, 300, 4, 64, 128, 2, 128, dtype="fp32", init_state=True)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
+    y = Guarded(d["x"].shape, d["x"].dtype)
+    fin = Guarded((w.batch, w.nheads, w.dstate, w.headdim), torch.float32)
+    ws = Guarded((bd.mamba2_ssd_fwd_workspace_size(shape),), torch.uint8)
+    bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size, D=d["D"],
+                      initial_state=d["initial_state"], y=y.t, final_state=fin.t, workspace=ws.t)
+    bd.mamba2_check_device_status()
+    assert y.intact() and fin.intact() and ws.intact()
+    r = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"],
+                              init=inp["initial_state"])
+    assert rel_err(np64(y.t), r["y"]) <= TOL["fp32"]
