@@ -206,12 +206,12 @@ mamba2_status mamba2_chunk_out(const mamba2_shape* shape, const void* x, const f
 size_t mamba2_ssd_fwd_workspace_size(const mamba2_shape* shape) {
     if (check_shape(shape) != MAMBA2_OK) return 0;
     const Sizes z = sizes_of(*shape);
+    // fp32 on the tensor cores: G, then bf16 hi/lo planes of the chunk states
+    // (the bytes of fp32 states), x, B and C
+    if (fwd_f32_tensor_cores(*shape))
+        return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(z.x, 256) + 2 * round_up(z.bc, 256));
     const int64_t seg = fwd_segments(*shape) > 1 ? state_pass_segment_bytes(make_geom(*shape)) : 0;
-    // fp32 on the tensor cores: bf16 hi/lo planes of the chunk states, x, B, C
-    const int64_t split = fwd_f32_tensor_cores(*shape)
-                              ? round_up(z.cs, 256) + round_up(z.x, 256) + 2 * round_up(z.bc, 256)
-                              : 0;
-    return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(seg, 256) + split);
+    return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(seg, 256));
 }
 
 mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const float* dt,
@@ -246,9 +246,9 @@ mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const flo
         return from_cuda(launch_ssd_fused(g, fa, st));
     }
     if (fwd_f32_tensor_cores(*shape)) {
-        // fp32: x, B, C and (after stage 2) the chunk states as bf16 hi/lo
-        // planes, stage 3 on the tensor cores with three products per product
-        char* q = ws + round_up(z.G, 256) + round_up(z.cs, 256);
+        // fp32: x, B and C as bf16 hi/lo planes; stages 2 and 3 on the tensor
+        // cores with three products per product, the chunk states as planes
+        char* q = ws + round_up(z.G, 256);
         void* cs2 = q;
         q += round_up(z.cs, 256);
         void* x2 = q;
@@ -264,12 +264,9 @@ mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const flo
             (rc = from_cuda(launch_split_bf16(static_cast<const float*>(C), C2, tok * shape->ngroups,
                                               shape->dstate, st))) != MAMBA2_OK)
             return rc;
-        StatePassArgs sp{x, dt, B, G, initial_state, cs, final_state};
-        if ((rc = run_state_pass(*shape, sp, st)) != MAMBA2_OK) return rc;
-        if ((rc = from_cuda(launch_split_bf16(static_cast<const float*>(cs), cs2,
-                                              shape->batch * shape->nheads * g.nchunks,
-                                              shape->dstate * shape->headdim, st))) != MAMBA2_OK)
-            return rc;
+        StatePassArgs sp{x2, dt, B2, G, initial_state, cs2, final_state};
+        sp.split = true;
+        if ((rc = from_cuda(launch_state_pass_tc(g, sp, st))) != MAMBA2_OK) return rc;
         const F32ChunkOutArgs co{x2, dt, B2, C2, D, G, cs2, static_cast<float*>(y)};
         return from_cuda(launch_chunk_out_f32tc(g, co, st));
     }

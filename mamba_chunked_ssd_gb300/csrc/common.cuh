@@ -72,6 +72,10 @@ struct StatePassArgs {
     int segments = 1;
     bool summary = false;
     float* seg_states = nullptr;
+    // fp32 on the tensor cores (chunk 128, one pass): x and B are bf16 hi/lo
+    // planes ([b, L, 2 nh, H], [b, L, 2 G, S]) and the chunk states are
+    // written as hi/lo planes [b, nh, nc, 2, S, H]; init and final stay fp32.
+    bool split = false;
 };
 
 struct ChunkOutArgs {
@@ -125,6 +129,7 @@ cudaError_t launch_ssd_step(const Geom& g, bool bf16, const SsdStepArgs& a, cuda
 bool chunk_out_tc_fits(const Geom& g);
 cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream_t st);
 bool state_pass_tc_fits(const Geom& g);
+bool state_pass_split_fits(const Geom& g);
 cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStream_t st);
 // Segments the forward pass splits each sequence into for stage 2 (1: one
 // pass over the whole sequence), the bytes of their states, and the carry

@@ -28,12 +28,12 @@ bool use_fused_forward(const Geom& g, bool bf16) {
     return env && strcmp(env, "fused") == 0;
 }
 
-// fp32 problems whose stage 3 the split-bf16 tensor-core kernel covers run
-// it inside mamba2_ssd_fwd (the stage entry points keep the CUDA-core
-// kernels: they take no workspace for the bf16 planes).
+// fp32 problems whose stages 2 and 3 the split-bf16 tensor-core kernels
+// cover run them inside mamba2_ssd_fwd (the stage entry points keep the
+// CUDA-core kernels: they take no workspace for the bf16 planes).
 // MAMBA2_FP32_PATH=simt forces the CUDA-core kernel, for timing both.
 bool use_f32_tensor_cores(const Geom& g, bool bf16) {
-    if (bf16 || !chunk_out_f32tc_fits(g)) return false;
+    if (bf16 || !chunk_out_f32tc_fits(g) || !state_pass_split_fits(g)) return false;
     const char* env = getenv("MAMBA2_FP32_PATH");
     return !(env && strcmp(env, "simt") == 0);
 }

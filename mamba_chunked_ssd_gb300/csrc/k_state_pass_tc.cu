@@ -71,7 +71,9 @@ struct SpTcParams {
     int kb;             // tokens per sub-block (64 or 128)
     int nsb;            // sub-blocks per chunk = chunk / kb
     int nst;            // ring stages
-    uint32_t stage_bytes, off_x_in_stage, off_w_in_stage, off_stg, off_bar, smem_bytes, tmem_cols;
+    // stage: B [2 boxes] (split: B_hi, B_lo) | X [H / 64 boxes] (split: X_hi, X_lo) | G, dt, G_last
+    uint32_t stage_bytes, off_blo_in_stage, off_x_in_stage, off_xlo_in_stage, off_w_in_stage, off_stg, off_bar,
+        smem_bytes, tmem_cols;
     const float* dt;
     const float* G;
     const float* init;
@@ -101,7 +103,12 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
 
 // H (head dim), T (chunk) and KB (tokens per sub-block) are compile-time, so
 // the sub-block count and the box and chunk offsets fold into constants.
-template <int H, int T, int KB>
+// SPLIT: an fp32 problem whose x and B arrive as bf16 hi/lo planes (x as
+// [b, L, 2 nh, H], head 2h hi and 2h + 1 lo; B as [b, L, 2 G, S]); the fold
+// forms w x in fp32 from hi + lo and writes it back as a hi/lo pair, U takes
+// three products (B_hi (w x)_hi + B_hi (w x)_lo + B_lo (w x)_hi), and the
+// chunk states leave as hi/lo planes, rows [b, nh, nc, 2, S] x H.
+template <int H, int T, int KB, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 2)
 k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_cs, const SpTcParams p) {
@@ -180,12 +187,19 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             uint8_t* sX = sB + p.off_x_in_stage;
             float* sV = reinterpret_cast<float*>(sB + p.off_w_in_stage);  // G[kKb], dt[kKb], G_last
             if (lane == 0) {
-                tc::mbar_arrive_expect_tx(&bars[kBarFull + st], (2 + H / 64) * x_box_bytes);
-                for (int kb = 0; kb < 2; ++kb)
-                    tc::tma_load_4d(sB + kb * x_box_bytes, &tm_b, &bars[kBarFull + st], mt * 128 + kb * 64, grp, tok,
-                                    (int)b);
-                for (int cb = 0; cb < H / 64; ++cb)
-                    tc::tma_load_4d(sX + cb * x_box_bytes, &tm_x, &bars[kBarFull + st], cb * 64, h, tok, (int)b);
+                constexpr int planes = SPLIT ? 2 : 1;
+                tc::mbar_arrive_expect_tx(&bars[kBarFull + st], planes * (2 + H / 64) * x_box_bytes);
+                for (int pl = 0; pl < planes; ++pl) {
+                    uint8_t* sBp = sB + pl * p.off_blo_in_stage;
+                    uint8_t* sXp = pl ? sB + p.off_xlo_in_stage : sX;
+                    const int gi = SPLIT ? 2 * grp + pl : grp, hi = SPLIT ? 2 * h + pl : h;
+                    for (int kb = 0; kb < 2; ++kb)
+                        tc::tma_load_4d(sBp + kb * x_box_bytes, &tm_b, &bars[kBarFull + st], mt * 128 + kb * 64, gi,
+                                        tok, (int)b);
+                    for (int cb = 0; cb < H / 64; ++cb)
+                        tc::tma_load_4d(sXp + cb * x_box_bytes, &tm_x, &bars[kBarFull + st], cb * 64, hi, tok,
+                                        (int)b);
+                }
             }
             // G_t and dt_t of the sub-block's tokens (past the last valid token:
             // G of the last one and dt = 0) and G_last of the chunk, gathered
@@ -217,6 +231,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // below 256 KB) and by 2 KB (128 units) per 16 tokens.
             const uint64_t desc0 = tc::sdesc_sw128(tc::smem_u32(smem), x_box_bytes, 1024);
             const uint64_t stage_step = p.stage_bytes >> 4, x_step = p.off_x_in_stage >> 4;
+            const uint64_t blo_step = p.off_blo_in_stage >> 4, xlo_step = p.off_xlo_in_stage >> 4;
             uint64_t dstage = desc0;
             int st = 0;
             uint32_t phase = 0;
@@ -232,10 +247,20 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
                 tc::tc_fence_after();
                 const uint32_t tu = tm_u0 + ub * H;
+                if (SPLIT) {
+                    // B_hi (w x)_hi + B_hi (w x)_lo + B_lo (w x)_hi
+                    const uint64_t pa[3] = {0, 0, blo_step}, pb[3] = {x_step, xlo_step, x_step};
+                    for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
-                for (int k16 = 0; k16 < kKb / 16; ++k16)
-                    tc::mma_bf16_ss(tu, dstage + 128 * k16, dstage + x_step + 128 * k16, idesc,
-                                    (sb > 0 || k16 > 0) ? 1u : 0u);
+                        for (int k16 = 0; k16 < kKb / 16; ++k16)
+                            tc::mma_bf16_ss(tu, dstage + pa[ps] + 128 * k16, dstage + pb[ps] + 128 * k16, idesc,
+                                            (sb > 0 || ps > 0 || k16 > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int k16 = 0; k16 < kKb / 16; ++k16)
+                        tc::mma_bf16_ss(tu, dstage + 128 * k16, dstage + x_step + 128 * k16, idesc,
+                                        (sb > 0 || k16 > 0) ? 1u : 0u);
+                }
                 tc::mma_commit(&bars[kBarSlotFree + st]);
                 if (sb == nsb - 1) tc::mma_commit(&bars[kBarUDone + ub]);
                 if (++st == p.nst) {
@@ -265,8 +290,32 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const float* sV = reinterpret_cast<const float*>(smem + st * p.stage_bytes + p.off_w_in_stage);
                 const float w = sV[kKb + frow] * exp2f(sV[2 * kKb] - sV[frow]);  // w_t = dt_t exp2(G_last - G_t)
                 uint8_t* rowp = smem + st * p.stage_bytes + p.off_x_in_stage + frow * 128;
+                if (SPLIT) {
+                    // w x from hi + lo in fp32, written back as a hi/lo pair
+                    uint8_t* rowl = smem + st * p.stage_bytes + p.off_xlo_in_stage + frow * 128;
+#pragma unroll
+                    for (int f = 0; f < 16; ++f) {
+                        if (f >= per) break;
+                        const int flat = fh * per + f;
+                        const uint32_t off = (flat >> 3) * x_box_bytes + ((((flat & 7) + frow) & 7) << 4);
+                        const uint4 vh = *reinterpret_cast<const uint4*>(rowp + off);
+                        const uint4 vl = *reinterpret_cast<const uint4*>(rowl + off);
+                        const uint32_t hw[4] = {vh.x, vh.y, vh.z, vh.w}, lw[4] = {vl.x, vl.y, vl.z, vl.w};
+                        uint32_t oh[4], ol[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const float a0 = (tc::bf16_lo(hw[x]) + tc::bf16_lo(lw[x])) * w;
+                            const float a1 = (tc::bf16_hi(hw[x]) + tc::bf16_hi(lw[x])) * w;
+                            oh[x] = tc::pack_bf16x2(a0, a1);
+                            ol[x] = tc::pack_bf16x2(a0 - tc::bf16_lo(oh[x]), a1 - tc::bf16_hi(oh[x]));
+                        }
+                        *reinterpret_cast<uint4*>(rowp + off) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                        *reinterpret_cast<uint4*>(rowl + off) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                    }
+                }
 #pragma unroll
                 for (int f0 = 0; f0 < 16; f0 += 2) {  // two chunks in flight
+                    if (SPLIT) break;
                     if (f0 >= per) break;
                     uint4 v[2];
 #pragma unroll
@@ -338,7 +387,10 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (cl + 1 < nchl) gl_next = glast_of(c + 1);
                 if (ok) ok = tc::mbar_wait(&bars[kBarUDone + ub], (cl >> 1) & 1, abort_flag);
                 tc::tc_fence_after();
-                const int64_t row0 = (bh * g.nchunks + c) * S + mt * 128;  // first state row of the tile
+                // first state row of the tile (split: of its hi plane; the lo
+                // plane's rows follow S rows later)
+                const int64_t row0 = (SPLIT ? (bh * g.nchunks + c) * 2 * S : (bh * g.nchunks + c) * S) + mt * 128;
+                constexpr uint32_t lo_tile = (H / 64) * 8192;  // split: the lo tile follows the hi tile
                 if (!store && ok) {
                     // h <- exp2(G_last) h + U_c only
 #pragma unroll 1
@@ -368,11 +420,18 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                             for (int s4 = 0; s4 < 2; ++s4) {
                                 const int e = 8 * s4, j = 2 * (m & 3) + s4;  // 16-byte chunk in the row
-                                *reinterpret_cast<uint4*>(rowp + ((j ^ (hrow & 7)) << 4)) = make_uint4(
-                                    tc::pack_bf16x2(__uint_as_float(hv[e]), __uint_as_float(hv[e + 1])),
-                                    tc::pack_bf16x2(__uint_as_float(hv[e + 2]), __uint_as_float(hv[e + 3])),
-                                    tc::pack_bf16x2(__uint_as_float(hv[e + 4]), __uint_as_float(hv[e + 5])),
-                                    tc::pack_bf16x2(__uint_as_float(hv[e + 6]), __uint_as_float(hv[e + 7])));
+                                uint32_t wh[4], wl[4];
+#pragma unroll
+                                for (int x = 0; x < 4; ++x) {
+                                    const float a0 = __uint_as_float(hv[e + 2 * x]);
+                                    const float a1 = __uint_as_float(hv[e + 2 * x + 1]);
+                                    wh[x] = tc::pack_bf16x2(a0, a1);
+                                    if (SPLIT) wl[x] = tc::pack_bf16x2(a0 - tc::bf16_lo(wh[x]), a1 - tc::bf16_hi(wh[x]));
+                                }
+                                const uint32_t off = (j ^ (hrow & 7)) << 4;
+                                *reinterpret_cast<uint4*>(rowp + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                                if (SPLIT)
+                                    *reinterpret_cast<uint4*>(rowp + lo_tile + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                             }
 #pragma unroll
                             for (int e = 0; e < 16; ++e)
@@ -383,8 +442,11 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                     asm volatile("bar.sync 1, %0;" ::"r"(kScanWarps * 32) : "memory");
                     if (leader && ok) {
-                        for (int cb = 0; cb < H / 64; ++cb)
+                        for (int cb = 0; cb < H / 64; ++cb) {
                             tc::tma_store_2d(&tm_cs, stg + cb * 8192, cb * 64, (int)(row0 + 64 * half));
+                            if (SPLIT)
+                                tc::tma_store_2d(&tm_cs, stg + lo_tile + cb * 8192, cb * 64, (int)(row0 + S + 64 * half));
+                        }
                         tc::bulk_commit();
                         tc::bulk_wait_read_all();  // the tile may be refilled
                     }
@@ -475,20 +537,26 @@ __global__ void __launch_bounds__(256) k_state_carry(const float* __restrict__ G
 // Ring plan.  Two CTAs share an SM when TMEM allows and the grid has enough
 // CTAs to use them; a grid of at most one CTA per SM (ctas_per_sm_cap = 1)
 // gets the whole shared memory, i.e. a deeper ring.
-bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2) {
+// A split (fp32) problem's stages hold hi and lo planes: one CTA per SM
+// with a ring of 64-token sub-blocks.
+bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2, bool split = false) {
     const int H = (int)g.headdim;
     p.tmem_cols = (3 * H <= 256) ? 256 : 512;
-    const bool two = p.tmem_cols == 256 && ctas_per_sm_cap >= 2;
-    const int kKb = (!two && g.chunk >= 128) ? 128 : 64;
+    const bool two = p.tmem_cols == 256 && ctas_per_sm_cap >= 2 && !split;
+    const int kKb = (!two && g.chunk >= 128 && !split) ? 128 : 64;
+    const uint32_t planes = split ? 2 : 1;
     p.kb = kKb;
     p.nsb = (int)(g.chunk / kKb);
-    p.off_x_in_stage = 2 * kKb * 128;
-    p.off_w_in_stage = p.off_x_in_stage + (H / 64) * kKb * 128;
+    p.off_blo_in_stage = 2 * kKb * 128;
+    p.off_x_in_stage = planes * 2 * kKb * 128;
+    p.off_xlo_in_stage = p.off_x_in_stage + (H / 64) * kKb * 128;
+    p.off_w_in_stage = p.off_x_in_stage + planes * (H / 64) * kKb * 128;
     // G[kKb], dt[kKb], G_last; padded to keep stages 1 KB aligned
     p.stage_bytes = p.off_w_in_stage + ((2 * kKb + 1) * 4 + 1023) / 1024 * 1024;
     const uint32_t budget = two ? (kSmemLimit / 2 - 2048) : kSmemLimit;
     const uint32_t fixed = kNumBars * 8 + 64 + 1024;
-    const uint32_t stg_bytes = (uint32_t)(H / 64) * 8192;  // 64 rows x H bf16, boxes of 64 columns
+    // 64 rows x H bf16 (boxes of 64 columns) per plane
+    const uint32_t stg_bytes = planes * (uint32_t)(H / 64) * 8192;
     int nst = (int)((budget - fixed - stg_bytes) / p.stage_bytes);
     if (nst > kMaxStages) nst = kMaxStages;
     if (nst < 2) return false;
@@ -528,6 +596,12 @@ int64_t state_pass_segment_bytes(const Geom& g) {
     return nseg > 1 ? g.batch * g.nheads * (nseg - 1) * g.dstate * g.headdim * 4 : 0;
 }
 
+// The split (fp32) state pass: chunks of 128, one pass.
+bool state_pass_split_fits(const Geom& g) {
+    SpTcParams p;
+    return g.chunk == 128 && state_pass_tc_fits(g) && plan(g, p, 1, true);
+}
+
 bool state_pass_tc_fits(const Geom& g) {
     if (g.chunk != 64 && g.chunk != 128 && g.chunk != 256) return false;
     if (g.headdim != 64 && g.headdim != 128) return false;
@@ -543,7 +617,9 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     const int mtiles = (int)((g.dstate + 127) / 128);
     const int seg_grid = a.segments > 1 ? (a.summary ? a.segments - 1 : a.segments) : 1;
     const int64_t ctas = (int64_t)mtiles * g.nheads * g.batch * seg_grid;
-    if (!plan(g, p, ctas <= kTargetSms ? 1 : 2)) return cudaErrorInvalidConfiguration;
+    const bool split = a.split;
+    if (split && (a.segments > 1 || g.chunk != 128)) return cudaErrorInvalidConfiguration;
+    if (!plan(g, p, ctas <= kTargetSms ? 1 : 2, split)) return cudaErrorInvalidConfiguration;
     p.mode = kWholeSequence;
     p.nseg = 1;
     p.cps = (int)g.nchunks;
@@ -564,33 +640,35 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     p.status = device_status_word();
     const uint64_t H = g.headdim, S = g.dstate, nh = g.nheads, L = g.seqlen, G = g.ngroups;
     const int kKb = p.kb;
+    const uint64_t planes = split ? 2 : 1;  // split: hi/lo planes as twice the heads, groups and state rows
     CUtensorMap tm_x, tm_b;
     {
-        const uint64_t dims[4] = {H, nh, L, (uint64_t)g.batch};
-        const uint64_t strides[3] = {H * 2, nh * H * 2, L * nh * H * 2};
+        const uint64_t dims[4] = {H, planes * nh, L, (uint64_t)g.batch};
+        const uint64_t strides[3] = {H * 2, planes * nh * H * 2, L * planes * nh * H * 2};
         const uint32_t box[4] = {64, 1, kKb, 1};
         if (!make_tmap_bf16(&tm_x, a.x, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const uint64_t dims[4] = {S, G, L, (uint64_t)g.batch};
-        const uint64_t strides[3] = {S * 2, G * S * 2, L * G * S * 2};
+        const uint64_t dims[4] = {S, planes * G, L, (uint64_t)g.batch};
+        const uint64_t strides[3] = {S * 2, planes * G * S * 2, L * planes * G * S * 2};
         const uint32_t box[4] = {64, 1, kKb, 1};
         if (!make_tmap_bf16(&tm_b, a.B, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
     CUtensorMap tm_cs;
     {
-        const uint64_t rows = (uint64_t)g.batch * nh * g.nchunks * S;
+        const uint64_t rows = (uint64_t)g.batch * nh * g.nchunks * planes * S;
         const uint64_t dims[2] = {H, rows};
         const uint64_t strides[1] = {H * 2};
         const uint32_t box[2] = {64, 64};
         if (!make_tmap_bf16(&tm_cs, a.chunk_states, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    auto kern = (g.headdim == 64)
-                    ? (g.chunk == 256 ? (kKb == 128 ? k_state_pass_tc<64, 256, 128> : k_state_pass_tc<64, 256, 64>)
-                       : g.chunk == 128 ? (kKb == 128 ? k_state_pass_tc<64, 128, 128> : k_state_pass_tc<64, 128, 64>)
-                                        : k_state_pass_tc<64, 64, 64>)
-                    : (g.chunk == 256 ? k_state_pass_tc<128, 256, 128>
-                       : g.chunk == 128 ? k_state_pass_tc<128, 128, 128> : k_state_pass_tc<128, 64, 64>);
+    auto kern = split ? (g.headdim == 64 ? k_state_pass_tc<64, 128, 64, true> : k_state_pass_tc<128, 128, 64, true>)
+                : (g.headdim == 64)
+                    ? (g.chunk == 256 ? (kKb == 128 ? k_state_pass_tc<64, 256, 128, false> : k_state_pass_tc<64, 256, 64, false>)
+                       : g.chunk == 128 ? (kKb == 128 ? k_state_pass_tc<64, 128, 128, false> : k_state_pass_tc<64, 128, 64, false>)
+                                        : k_state_pass_tc<64, 64, 64, false>)
+                    : (g.chunk == 256 ? k_state_pass_tc<128, 256, 128, false>
+                       : g.chunk == 128 ? k_state_pass_tc<128, 128, 128, false> : k_state_pass_tc<128, 64, 64, false>);
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)(g.batch * p.seg_grid));
