@@ -458,7 +458,7 @@ def run_gpu(args, w, rank, world):
             "e2e_ms": e2e_total, "h2d": h2d, "d2h": d2h, "inp": inp, "host_us": host_us_per_call}
 
 
-EXTRA_WORKLOADS = ("mamba2_1p3b_layer", "large_state", "blog_example")
+EXTRA_WORKLOADS = ("mamba2_1p3b_layer", "large_state", "blog_example", "long_seq_fp32_t128")
 
 
 def run_extra(args, w, peaks, cpu_pairs):

@@ -66,6 +66,10 @@ WORKLOADS = {
     # the example problem the blog's usage snippet times: batch 4, 16384
     # tokens, one group, 8 heads, state 128, head dim 64, chunk 128
     "blog_example": Workload("blog_example", 4, 16384, 8, 64, 128, 1, 128),
+    # the long-sequence layer in fp32 with chunks of 128 (the fp32 path's
+    # tensor-core shapes)
+    "long_seq_fp32_t128": Workload("long_seq_fp32_t128", 4, 8192, 64, 64, 128, 1, 128, dtype="fp32",
+                                   init_state=True),
 }
 
 

@@ -16,6 +16,9 @@ be checked against measurements:
   MAMBA2_STATE_SEGMENTS = 1             the forward pass's state pass in one
       pass over each sequence, instead of over sequence segments where the
       (batch, head) pairs are few.
+  MAMBA2_FP32_PATH = simt               an fp32 forward pass on the CUDA
+      cores instead of the split-bf16 tensor-core kernels (where they fit:
+      chunk 128, head dim 64 or 128, state 64 or 128).
 
 Usage (one GPU):  python -m mamba_chunked_ssd_gb300.tune [--steps K] [--json]
 Each line: workload, candidate, mean stage time in microseconds (CUDA events
@@ -43,6 +46,7 @@ FLUSH_BYTES = 256 << 20
 HEAD_SPLIT_ENV = "MAMBA2_CHUNK_OUT_HEAD_SPLIT"
 FWD_PATH_ENV = "MAMBA2_FWD_PATH"
 SEGMENTS_ENV = "MAMBA2_STATE_SEGMENTS"
+FP32_ENV = "MAMBA2_FP32_PATH"
 
 
 def _time(fn, steps, warmup, flush, stream):
@@ -192,6 +196,45 @@ def segment_rows(workloads, steps=10, warmup=3):
     return rows
 
 
+def fp32_rows(workloads, steps=5, warmup=2):
+    """Whole-pass time of fp32 workloads on the tensor cores (split bf16) and
+    on the CUDA cores."""
+    import torch
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+
+    bd.load_library()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    rows = []
+    saved = os.environ.pop(FP32_ENV, None)
+    try:
+        for w in workloads:
+            if w.dtype != "fp32":
+                continue
+            d = make_inputs(w, device="cuda")
+            shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
+            times = {}
+            for cand in ("tc", "simt"):
+                if cand == "simt":
+                    os.environ[FP32_ENV] = "simt"
+                ws = torch.empty(max(bd.mamba2_ssd_fwd_workspace_size(shape), 1), device="cuda", dtype=torch.uint8)
+                y = torch.empty_like(d["x"])
+                fn = lambda: bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size,  # noqa: E731
+                                               D=d["D"], initial_state=d["initial_state"], y=y, workspace=ws)
+                times[cand] = _time(fn, steps, warmup, flush, stream)
+                os.environ.pop(FP32_ENV, None)
+                del ws, y
+            bd.mamba2_check_device_status()
+            rows.append({"workload": w.name, "tensor_cores_us": times["tc"], "cuda_cores_us": times["simt"]})
+            del d
+    finally:
+        os.environ.pop(FP32_ENV, None)
+        if saved is not None:
+            os.environ[FP32_ENV] = saved
+    return rows
+
+
 def profile_run(name, steps):
     """`steps` forward passes of one named workload, synchronised at the end."""
     import torch
@@ -231,8 +274,10 @@ def main():
     rows = head_split_rows(ws, steps=args.steps)
     paths = fwd_path_rows(ws, steps=args.steps)
     segs = segment_rows(seg_ws, steps=args.steps)
+    f32 = fp32_rows([WORKLOADS["long_seq_fp32_t128"],
+                     Workload("fp32_h128_s64", 2, 4096, 16, 128, 64, 2, 128, dtype="fp32")])
     if args.json:
-        print(json.dumps({"head_split": rows, "fwd_path": paths, "segments": segs}))
+        print(json.dumps({"head_split": rows, "fwd_path": paths, "segments": segs, "fp32": f32}))
         return
     print("Stage 3, heads of 128 columns:")
     print("| workload | whole heads (µs) | split heads (µs) | default (µs) |")
@@ -251,6 +296,12 @@ def main():
     print("|---|---|---|")
     for r in segs:
         print(f"| {r['workload']} | {r['segments_us']:.1f} | {r['one_pass_us']:.1f} |")
+    print()
+    print("fp32 forward pass, split-bf16 tensor cores vs CUDA cores:")
+    print("| workload | tensor cores (µs) | CUDA cores (µs) |")
+    print("|---|---|---|")
+    for r in f32:
+        print(f"| {r['workload']} | {r['tensor_cores_us']:.1f} | {r['cuda_cores_us']:.1f} |")
 
 
 if __name__ == "__main__":
