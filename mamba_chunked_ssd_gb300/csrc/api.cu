@@ -206,10 +206,10 @@ mamba2_status mamba2_chunk_out(const mamba2_shape* shape, const void* x, const f
 size_t mamba2_ssd_fwd_workspace_size(const mamba2_shape* shape) {
     if (check_shape(shape) != MAMBA2_OK) return 0;
     const Sizes z = sizes_of(*shape);
-    // fp32 on the tensor cores: G, then bf16 hi/lo planes of the chunk states
-    // (the bytes of fp32 states), x, B and C
+    // fp32 on the tensor cores: G, the fp32 chunk states, then B as bf16
+    // hi/lo planes (the bytes of fp32 B)
     if (fwd_f32_tensor_cores(*shape))
-        return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(z.x, 256) + 2 * round_up(z.bc, 256));
+        return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(z.bc, 256));
     const int64_t seg = fwd_segments(*shape) > 1 ? state_pass_segment_bytes(make_geom(*shape)) : 0;
     return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(seg, 256));
 }
@@ -246,28 +246,22 @@ mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const flo
         return from_cuda(launch_ssd_fused(g, fa, st));
     }
     if (fwd_f32_tensor_cores(*shape)) {
-        // fp32: x, B and C as bf16 hi/lo planes; stages 2 and 3 on the tensor
-        // cores with three products per product, the chunk states as planes
-        char* q = ws + round_up(z.G, 256);
-        void* cs2 = q;
-        q += round_up(z.cs, 256);
-        void* x2 = q;
-        q += round_up(z.x, 256);
-        void* B2 = q;
-        q += round_up(z.bc, 256);
-        void* C2 = q;
-        const int64_t tok = shape->batch * shape->seqlen;
-        if ((rc = from_cuda(launch_split_bf16(static_cast<const float*>(x), x2, tok * shape->nheads,
-                                              shape->headdim, st))) != MAMBA2_OK ||
-            (rc = from_cuda(launch_split_bf16(static_cast<const float*>(B), B2, tok * shape->ngroups,
-                                              shape->dstate, st))) != MAMBA2_OK ||
-            (rc = from_cuda(launch_split_bf16(static_cast<const float*>(C), C2, tok * shape->ngroups,
-                                              shape->dstate, st))) != MAMBA2_OK)
+        // fp32: stages 2 and 3 on the tensor cores with three products per
+        // product, each operand split on the chip into a bf16 hi/lo pair; only
+        // B, which every head of a group shares in stage 2, is split once
+        // here into hi/lo planes
+        void* cs = ws + round_up(z.G, 256);
+        void* B2 = static_cast<char*>(cs) + round_up(z.cs, 256);
+        if ((rc = from_cuda(launch_split_bf16(static_cast<const float*>(B), B2,
+                                              shape->batch * shape->seqlen * shape->ngroups, shape->dstate,
+                                              st))) != MAMBA2_OK)
             return rc;
-        StatePassArgs sp{x2, dt, B2, G, initial_state, cs2, final_state};
+        StatePassArgs sp{x, dt, B2, G, initial_state, cs, final_state};
         sp.split = true;
         if ((rc = from_cuda(launch_state_pass_tc(g, sp, st))) != MAMBA2_OK) return rc;
-        const F32ChunkOutArgs co{x2, dt, B2, C2, D, G, cs2, static_cast<float*>(y)};
+        const F32ChunkOutArgs co{static_cast<const float*>(x), dt, static_cast<const float*>(B),
+                                 static_cast<const float*>(C), D, G, static_cast<const float*>(cs),
+                                 static_cast<float*>(y)};
         return from_cuda(launch_chunk_out_f32tc(g, co, st));
     }
     // stages 2 and 3 may start while the stage before them runs (programmatic

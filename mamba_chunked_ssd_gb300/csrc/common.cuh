@@ -139,26 +139,25 @@ int64_t state_pass_segment_bytes(const Geom& g);
 cudaError_t launch_state_carry(const Geom& g, const float* G, float* seg_states, int nseg, bool pdl,
                                cudaStream_t st);
 
-// The fp32 forward pass on the tensor cores: fp32 x, B, C and chunk states
-// split into bf16 hi/lo planes (k_split_bf16.cu), stage 3 on them
-// (k_chunk_out_f32tc.cu).  x2 [b, L, 2 nh, H], B2 / C2 [b, L, 2 G, S],
-// cs2 [b, nh, nc, 2, S, H] (plane 0 hi, plane 1 lo); y fp32.
+// fp32 stage 3 on the tensor cores (k_chunk_out_f32tc.cu): fp32 x, B, C and
+// chunk states, split on chip into bf16 hi/lo pairs.
 struct F32ChunkOutArgs {
-    const void* x2;
+    const float* x;
     const float* dt;
-    const void* B2;
-    const void* C2;
+    const float* B;
+    const float* C;
     const float* D;  // may be null
     const float* G;
-    const void* cs2;
+    const float* cs;
     float* y;
 };
 // rows of `width` fp32 values (width % 4 == 0) -> rows of 2 x width bf16 (hi, lo)
 cudaError_t launch_split_bf16(const float* src, void* dst, int64_t rows, int width, cudaStream_t st);
 bool chunk_out_f32tc_fits(const Geom& g);
 cudaError_t launch_chunk_out_f32tc(const Geom& g, const F32ChunkOutArgs& a, cudaStream_t st);
-// Whether mamba2_ssd_fwd runs an fp32 problem's stage 3 on the tensor cores
-// (dispatch.cu).
+// Whether an fp32 problem's stage 3 runs on the tensor cores, and whether
+// mamba2_ssd_fwd runs its stages 2 and 3 there (dispatch.cu).
+bool f32_chunk_out_tensor_cores(const Geom& g, bool bf16);
 bool use_f32_tensor_cores(const Geom& g, bool bf16);
 
 bool ssd_fused_fits(const Geom& g);

@@ -13,6 +13,12 @@ cudaError_t launch_state_pass(const Geom& g, bool bf16, const StatePassArgs& a, 
 
 cudaError_t launch_chunk_out(const Geom& g, bool bf16, const ChunkOutArgs& a, cudaStream_t st) {
     if (bf16 && chunk_out_tc_fits(g)) return launch_chunk_out_tc(g, a, st);
+    if (f32_chunk_out_tensor_cores(g, bf16)) {
+        const F32ChunkOutArgs f{static_cast<const float*>(a.x), a.dt, static_cast<const float*>(a.B),
+                                static_cast<const float*>(a.C), a.D, a.G, static_cast<const float*>(a.chunk_states),
+                                static_cast<float*>(a.y)};
+        return launch_chunk_out_f32tc(g, f, st);
+    }
     return launch_chunk_out_simt(g, bf16, a, st);
 }
 
@@ -28,14 +34,23 @@ bool use_fused_forward(const Geom& g, bool bf16) {
     return env && strcmp(env, "fused") == 0;
 }
 
-// fp32 problems whose stages 2 and 3 the split-bf16 tensor-core kernels
-// cover run them inside mamba2_ssd_fwd (the stage entry points keep the
-// CUDA-core kernels: they take no workspace for the bf16 planes).
-// MAMBA2_FP32_PATH=simt forces the CUDA-core kernel, for timing both.
-bool use_f32_tensor_cores(const Geom& g, bool bf16) {
-    if (bf16 || !chunk_out_f32tc_fits(g) || !state_pass_split_fits(g)) return false;
+// fp32 problems run on the split-bf16 tensor-core kernels where they cover
+// the shape: stage 3 in both the forward pass and its own entry point (it
+// reads fp32 directly), stage 2 only inside mamba2_ssd_fwd (it reads B as
+// bf16 hi/lo planes, made in the forward pass's workspace; the stage entry
+// point takes no workspace and keeps the CUDA-core kernel).
+// MAMBA2_FP32_PATH=simt forces the CUDA-core kernels, for timing both.
+static bool fp32_path_simt() {
     const char* env = getenv("MAMBA2_FP32_PATH");
-    return !(env && strcmp(env, "simt") == 0);
+    return env && strcmp(env, "simt") == 0;
+}
+
+bool f32_chunk_out_tensor_cores(const Geom& g, bool bf16) {
+    return !bf16 && chunk_out_f32tc_fits(g) && !fp32_path_simt();
+}
+
+bool use_f32_tensor_cores(const Geom& g, bool bf16) {
+    return f32_chunk_out_tensor_cores(g, bf16) && state_pass_split_fits(g);
 }
 
 }  // namespace m2

@@ -5,22 +5,24 @@
 // CUDA Tile", §Kernel 3, computes per chunk and head
 //     Y = exp2(G) (C h_c) + ((C B^T) . exp2(G_i - G_j) . dt_j . causal M) X + D X.
 // The fp32 path must stay within 1e-4 of the exact result, which one tf32 or
-// bf16 product cannot.  Here every fp32 operand v arrives as two bf16 planes,
-// v_hi = bf16(v) and v_lo = bf16(v - v_hi) (k_split_bf16.cu), and every
-// product is taken as u_hi v_hi + u_hi v_lo + u_lo v_hi on the bf16 tensor
-// cores with fp32 accumulation: the terms left out are below 2^-16 |u v|.
+// bf16 product cannot.  Here every fp32 operand v is split on chip into
+// v_hi = bf16(v) and v_lo = bf16(v - v_hi), and every product is taken as
+// u_hi v_hi + u_hi v_lo + u_lo v_hi on the bf16 tensor cores with fp32
+// accumulation: the terms left out are below 2^-16 |u v|.  x, B, C and the
+// chunk states are read as fp32 (TMA boxes of 32 columns) and split in place
+// in shared memory into bf16 tiles of the bf16 kernel's layouts.
 //
 // GB300 design, the bf16 stage-3 kernel's (k_chunk_out_tc.cu) reduced to
 // chunks of 128 tokens and one head stream.  One CTA owns (batch, chunk, up to
 // 16 virtual 64-wide heads of one B/C group):
-//   warp 0       producer: TMA of C_hi, C_lo, B_hi, B_lo once, then per head
-//                X_hi, X_lo, h_hi, h_lo into a ring of stages, its lanes
-//                gathering G, dt and D with cp.async; stores y (fp32, TMA)
-//                before refilling a stage;
+//   warp 0       producer: TMA of C and B once, then per head X and h_c into
+//                a ring of stages, its lanes gathering G, dt and D with
+//                cp.async; stores y (fp32, TMA) before refilling a stage;
 //   warp 1       TMEM allocator; one thread issues every tcgen05.mma;
-//   warps 2..17  P formation and the epilogue.
-// Once per CTA:  CB = C B^T (three products) -> TMEM fp32, causally masked.
+//   warps 2..17  the hi/lo splits, P formation and the epilogue.
+// Once per CTA:  C, B split; CB = C B^T (three products) -> TMEM fp32, masked.
 // Per head:
+//   X, h_c split in place
 //   Z  = C h_c                          three products, B operand from smem
 //   P  = CB . w_j  -> P_hi, P_lo         written to TMEM as the A operand
 //   Y2 = P X                            three products, A from TMEM
@@ -66,6 +68,8 @@ struct F32Params {
 
 enum : int {
     kBarCbFull = 0,
+    kBarCbSplit,  // C and B split into hi/lo tiles
+    kBarSplit,    // the head's X and h_c split
     kBarCbDone,
     kBarPReady,
     kBarYDone,
@@ -100,10 +104,52 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
     lo = tc::pack_bf16x2(a - tc::bf16_lo(hi), b - tc::bf16_hi(hi));
 }
 
-// VS: virtual 64-wide heads per real head (1 or 2).  tm_x: split x as
-// [b, L, 2 nh, H_real] (head 2h: hi, 2h + 1: lo); tm_b, tm_c: split B, C as
-// [b, L, 2 G, S]; tm_h: split chunk states, rows [b, nh, nc, 2, S] x H_real;
-// tm_y: fp32 y [b, L, nh, H_real], boxes of 32 columns.
+// Splits, in place, a rows x cols fp32 tile loaded by TMA as boxes of 32
+// columns (rows x 128 bytes each, 128-byte swizzle) into the bf16 tiles hi
+// (at base) and lo (at base + rows cols 2), each in boxes of 64 columns
+// (rows x 128 bytes, 128-byte swizzle): the same bytes, laid out as the
+// tensor cores read bf16 operands.  A row keeps its lines (row r of every box
+// in both layouts), so rows are independent: the 512 threads of the epilogue
+// warps (index t) take 512 pieces of 8 columns per round, whole rows, and
+// read their round's pieces before the named barrier `bar_id` and write them
+// after it.  Every epilogue thread calls it (do_work = false skips the work
+// only).
+__device__ __forceinline__ void split_tile(uint8_t* base, int rows, int cols, int t, bool do_work, int bar_id) {
+    constexpr int kN = kEpiWarps * 32;
+    const int per_row = cols / 8;
+    const int pieces = rows * per_row;
+    const uint32_t lo_off = (uint32_t)rows * cols * 2;
+    for (int u0 = 0; u0 < pieces; u0 += kN) {
+        const int u = u0 + t;
+        const bool mine = do_work && u < pieces;
+        const int r = u / per_row, c0 = (u % per_row) * 8;
+        float4 f[2];
+        if (mine) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int c = c0 + 4 * q;
+                f[q] = *reinterpret_cast<const float4*>(base + (c >> 5) * (rows * 128) + r * 128 +
+                                                        ((((c & 31) >> 2) ^ (r & 7)) << 4));
+            }
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kN) : "memory");
+        if (mine) {
+            uint8_t* dst = base + (c0 >> 6) * (rows * 128) + r * 128 + ((((c0 & 63) >> 3) ^ (r & 7)) << 4);
+            uint32_t hi[4], lo[4];
+            split2(f[0].x, f[0].y, hi[0], lo[0]);
+            split2(f[0].z, f[0].w, hi[1], lo[1]);
+            split2(f[1].x, f[1].y, hi[2], lo[2]);
+            split2(f[1].z, f[1].w, hi[3], lo[3]);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(dst + lo_off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+    }
+    tc::fence_proxy_async_smem();  // the tiles are read by the tensor cores
+}
+
+// VS: virtual 64-wide heads per real head (1 or 2).  Every map is fp32 with
+// boxes of 32 columns: tm_x, tm_y [b, L, nh, H_real]; tm_b, tm_c
+// [b, L, G, S]; tm_h the chunk states, rows [b, nh, nc, S] x H_real.
 template <int VS>
 __global__ void __launch_bounds__(kThreads, 1)
 k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
@@ -135,6 +181,8 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&bars[kBarCbFull], 1);
+        tc::mbar_init(&bars[kBarCbSplit], kEpiWarps);
+        tc::mbar_init(&bars[kBarSplit], kEpiWarps);
         tc::mbar_init(&bars[kBarCbDone], 1);
         tc::mbar_init(&bars[kBarPReady], kEpiWarps);
         tc::mbar_init(&bars[kBarYDone], 1);
@@ -165,13 +213,11 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             tc::tma_prefetch_desc(&tm_b);
             tc::tma_prefetch_desc(&tm_c);
             tc::tma_prefetch_desc(&tm_h);
-            tc::mbar_arrive_expect_tx(&bars[kBarCbFull], (uint32_t)(4 * T * S * 2));
-            for (int kb = 0; kb < S / 64; ++kb) {
-                tc::tma_load_4d(sC + kb * 16384, &tm_c, &bars[kBarCbFull], kb * 64, 2 * grp, (int)t0, (int)b);
-                tc::tma_load_4d(sC1 + kb * 16384, &tm_c, &bars[kBarCbFull], kb * 64, 2 * grp + 1, (int)t0, (int)b);
-                tc::tma_load_4d(sB + kb * 16384, &tm_b, &bars[kBarCbFull], kb * 64, 2 * grp, (int)t0, (int)b);
-                tc::tma_load_4d(sB + T * S * 2 + kb * 16384, &tm_b, &bars[kBarCbFull], kb * 64, 2 * grp + 1,
-                                (int)t0, (int)b);
+            // C and B as fp32, boxes of 32 columns (split in place afterwards)
+            tc::mbar_arrive_expect_tx(&bars[kBarCbFull], (uint32_t)(2 * T * S * 4));
+            for (int kb = 0; kb < S / 32; ++kb) {
+                tc::tma_load_4d(sC + kb * 16384, &tm_c, &bars[kBarCbFull], kb * 32, grp, (int)t0, (int)b);
+                tc::tma_load_4d(sB + kb * 16384, &tm_b, &bars[kBarCbFull], kb * 32, grp, (int)t0, (int)b);
             }
         }
         tc::griddep_wait();  // the chunk states and G come from the previous kernels
@@ -215,12 +261,13 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             const int h = h0 + k / VS;
             const int col0 = (k % VS) * H;
             if (lane == 0) {
+                // X and h_c as fp32 (the bytes of their hi and lo tiles)
                 tc::mbar_arrive_expect_tx(full, 2 * x_tile + 2 * h_tile);
-                const int64_t hrow = (((b * g.nheads + h) * g.nchunks + c) * 2) * S;
-                tc::tma_load_4d(sX, &tm_x, full, col0, 2 * h, (int)t0, (int)b);
-                tc::tma_load_4d(sX + x_tile, &tm_x, full, col0, 2 * h + 1, (int)t0, (int)b);
-                tc::tma_load_2d(sX + p.off_h, &tm_h, full, col0, (int)hrow);
-                tc::tma_load_2d(sX + p.off_h + h_tile, &tm_h, full, col0, (int)(hrow + S));
+                const int64_t hrow = ((b * g.nheads + h) * g.nchunks + c) * S;
+                for (int xb = 0; xb < 2; ++xb) {
+                    tc::tma_load_4d(sX + xb * 16384, &tm_x, full, col0 + 32 * xb, h, (int)t0, (int)b);
+                    tc::tma_load_2d(sX + p.off_h + xb * (S * 128), &tm_h, full, col0 + 32 * xb, (int)hrow);
+                }
             }
             const float* Gh = p.G + (b * g.nheads + h) * g.seqlen + t0;
             const float* dth = p.dt + (b * g.seqlen + t0) * g.nheads + h;
@@ -245,7 +292,7 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     } else if (warp == 1) {
         // ========================= MMA issuer (one thread) =========================
         if (lane == 0) {
-            bool ok = tc::mbar_wait(&bars[kBarCbFull], 0, abort_flag);
+            bool ok = tc::mbar_wait(&bars[kBarCbSplit], 0, abort_flag);
             const uint32_t aC = tc::smem_u32(sC), aC1 = tc::smem_u32(sC1), aB = tc::smem_u32(sB);
             const uint32_t aB1 = aB + T * S * 2;
             if (ok) {
@@ -267,10 +314,10 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             const uint64_t dH0 = tc::sdesc_sw128(tc::smem_u32(sStage + p.off_h), S * 128, 1024);
             const uint64_t stage_step = p.stage_bytes >> 4, xlo = x_tile >> 4, hlo = h_tile >> 4;
             int st = 0, pst = slot_of(0);
-            uint32_t fill_phase = 0;
             uint64_t dstage = pst * stage_step;  // slot offset, in descriptor units
             for (int k = 0; ok && k < nvh; ++k) {
-                if (!tc::mbar_wait(&bars[kBarFull + st], fill_phase, abort_flag)) { ok = false; break; }
+                // the head's X and h_c are split (after their fill)
+                if (!tc::mbar_wait(&bars[kBarSplit], k & 1, abort_flag)) { ok = false; break; }
                 if (k >= 1 && !tc::mbar_wait(&bars[kBarYFree], (k - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 const uint64_t dH = dH0 + dstage, dX = dX0 + dstage;
@@ -298,7 +345,6 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 } else {
                     dstage += stage_step;
                 }
-                if (st == 0) fill_phase ^= 1u;
             }
             if (!ok) set_abort(ctl, p.status);
         }
@@ -313,7 +359,14 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         const int rq = 32 * q - 1;              // the column before this quadrant (-1: before the chunk)
         const bool visible = part <= q;         // causal: group `part` is seen by this quadrant's rows
 
-        bool ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
+        const int t = e * 32 + lane;  // 0..511
+        // C and B, loaded as fp32, become their hi/lo tiles
+        bool ok = tc::mbar_wait(&bars[kBarCbFull], 0, abort_flag);
+        split_tile(sC, T, S, t, ok, 3);
+        split_tile(sB, T, S, t, ok, 3);
+        __syncwarp();
+        if (ok && lane == 0) tc::mbar_arrive(&bars[kBarCbSplit]);
+        if (ok) ok = tc::mbar_wait(&bars[kBarCbDone], 0, abort_flag);
         tc::tc_fence_after();
         if (ok && e < 4) {
             // causal mask, once: zero CB above the diagonal inside this
@@ -344,6 +397,36 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         for (int k = 0; k < nvh; ++k) {
             if (ok) ok = tc::mbar_wait(&bars[kBarFull + st], fill_phase, abort_flag);
             uint8_t* sX = sStage + slot_of(st) * p.stage_bytes;
+            // X and h_c, loaded as fp32, become their hi/lo tiles.  X's piece
+            // of this thread (row il, columns [16 part, 16 part + 16)) is the
+            // one its output needs: it keeps the fp32 values for D x.
+            float xv[16];
+            if (ok) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 f = *reinterpret_cast<const float4*>(
+                        sX + (part >> 1) * (T * 128) + il * 128 + (((4 * (part & 1) + q4) ^ (il & 7)) << 4));
+                    xv[4 * q4] = f.x;
+                    xv[4 * q4 + 1] = f.y;
+                    xv[4 * q4 + 2] = f.z;
+                    xv[4 * q4 + 3] = f.w;
+                }
+            }
+            asm volatile("bar.sync 3, %0;" ::"r"(kEpiWarps * 32) : "memory");
+            if (ok) {
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    const uint32_t off = il * 128 + (((2 * part + h8) ^ (il & 7)) << 4);
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) split2(xv[8 * h8 + 2 * x], xv[8 * h8 + 2 * x + 1], hi[x], lo[x]);
+                    *reinterpret_cast<uint4*>(sX + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(sX + x_tile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+            split_tile(sX + p.off_h, S, H, t, ok, 3);
+            __syncwarp();
+            if (ok && lane == 0) tc::mbar_arrive(&bars[kBarSplit]);
             float si = 0.f, ui = 0.f, dh = 0.f;
             if (ok) {
                 const float* vG = reinterpret_cast<const float*>(sX + p.off_vec);
@@ -417,25 +500,15 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     tc::tmem_ld8_nowait(tmem + kColZ + lane_base + 16 * part + 8 * u, za[u]);
                     tc::tmem_ld8_nowait(tmem + kColY2 + lane_base + 16 * part + 8 * u, yb[u]);
                 }
-                uint4 xh[2], xl[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const uint32_t off = il * 128 + ((((2 * part + u) ^ (il & 7))) << 4);
-                    xh[u] = *reinterpret_cast<const uint4*>(sX + off);
-                    xl[u] = *reinterpret_cast<const uint4*>(sX + x_tile + off);
-                }
                 tc::tmem_wait_ld8(za[0]);
                 tc::tmem_tie8(yb[0]);
                 tc::tmem_tie8(za[1]);
                 tc::tmem_tie8(yb[1]);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const uint32_t hw[4] = {xh[u].x, xh[u].y, xh[u].z, xh[u].w};
-                    const uint32_t lw[4] = {xl[u].x, xl[u].y, xl[u].z, xl[u].w};
 #pragma unroll
                     for (int x = 0; x < 4; ++x) {
-                        const float x0 = tc::bf16_lo(hw[x]) + tc::bf16_lo(lw[x]);
-                        const float x1 = tc::bf16_hi(hw[x]) + tc::bf16_hi(lw[x]);
+                        const float x0 = xv[8 * u + 2 * x], x1 = xv[8 * u + 2 * x + 1];
                         yv[8 * u + 2 * x] = fmaf(si, __uint_as_float(za[u][2 * x]),
                                                  fmaf(ui, __uint_as_float(yb[u][2 * x]), dh * x0));
                         yv[8 * u + 2 * x + 1] = fmaf(si, __uint_as_float(za[u][2 * x + 1]),
@@ -523,7 +596,7 @@ bool chunk_out_f32tc_fits(const Geom& g) {
     if (g.headdim != 64 && g.headdim != 128) return false;
     if (g.dstate != 64 && g.dstate != 128) return false;
     if (g.batch * g.seqlen >= (int64_t(1) << 31)) return false;
-    if (g.batch * g.nheads * g.nchunks * 2 * g.dstate >= (int64_t(1) << 31)) return false;  // state rows
+    if (g.batch * g.nheads * g.nchunks * g.dstate >= (int64_t(1) << 31)) return false;  // state rows
     if (g.nheads * g.nchunks >= (int64_t(1) << 31)) return false;                          // grid.x
     F32Params p;
     return plan_f32(g, p);
@@ -543,24 +616,24 @@ cudaError_t launch_chunk_out_f32tc(const Geom& g, const F32ChunkOutArgs& a, cuda
     const uint64_t Hr = g.headdim, S = g.dstate, nh = g.nheads, L = g.seqlen, G = g.ngroups;
     CUtensorMap tm_x, tm_b, tm_c, tm_h, tm_y;
     {
-        const uint64_t dims[4] = {Hr, 2 * nh, L, (uint64_t)g.batch};
-        const uint64_t strides[3] = {Hr * 2, 2 * nh * Hr * 2, L * 2 * nh * Hr * 2};
-        const uint32_t box[4] = {64, 1, 128, 1};
-        if (!make_tmap_bf16(&tm_x, a.x2, 4, dims, strides, box)) return cudaErrorInvalidValue;
+        const uint64_t dims[4] = {Hr, nh, L, (uint64_t)g.batch};
+        const uint64_t strides[3] = {Hr * 4, nh * Hr * 4, L * nh * Hr * 4};
+        const uint32_t box[4] = {32, 1, 128, 1};
+        if (!make_tmap_f32(&tm_x, a.x, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const uint64_t dims[4] = {S, 2 * G, L, (uint64_t)g.batch};
-        const uint64_t strides[3] = {S * 2, 2 * G * S * 2, L * 2 * G * S * 2};
-        const uint32_t box[4] = {64, 1, 128, 1};
-        if (!make_tmap_bf16(&tm_b, a.B2, 4, dims, strides, box)) return cudaErrorInvalidValue;
-        if (!make_tmap_bf16(&tm_c, a.C2, 4, dims, strides, box)) return cudaErrorInvalidValue;
+        const uint64_t dims[4] = {S, G, L, (uint64_t)g.batch};
+        const uint64_t strides[3] = {S * 4, G * S * 4, L * G * S * 4};
+        const uint32_t box[4] = {32, 1, 128, 1};
+        if (!make_tmap_f32(&tm_b, a.B, 4, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_tmap_f32(&tm_c, a.C, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const uint64_t rows = (uint64_t)g.batch * nh * g.nchunks * 2 * S;
+        const uint64_t rows = (uint64_t)g.batch * nh * g.nchunks * S;
         const uint64_t dims[2] = {Hr, rows};
-        const uint64_t strides[1] = {Hr * 2};
-        const uint32_t box[2] = {64, (uint32_t)S};
-        if (!make_tmap_bf16(&tm_h, a.cs2, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        const uint64_t strides[1] = {Hr * 4};
+        const uint32_t box[2] = {32, (uint32_t)S};
+        if (!make_tmap_f32(&tm_h, a.cs, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
         const uint64_t dims[4] = {Hr, nh, L, (uint64_t)g.batch};

@@ -103,11 +103,12 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
 
 // H (head dim), T (chunk) and KB (tokens per sub-block) are compile-time, so
 // the sub-block count and the box and chunk offsets fold into constants.
-// SPLIT: an fp32 problem whose x and B arrive as bf16 hi/lo planes (x as
-// [b, L, 2 nh, H], head 2h hi and 2h + 1 lo; B as [b, L, 2 G, S]); the fold
-// forms w x in fp32 from hi + lo and writes it back as a hi/lo pair, U takes
-// three products (B_hi (w x)_hi + B_hi (w x)_lo + B_lo (w x)_hi), and the
-// chunk states leave as hi/lo planes, rows [b, nh, nc, 2, S] x H.
+// SPLIT: an fp32 problem.  x arrives as fp32 (boxes of 32 columns) and B as
+// bf16 hi/lo planes ([b, L, 2 G, S], group 2g hi and 2g + 1 lo); the fold
+// forms w x in fp32 and leaves it in place as a hi/lo pair (each 64-column
+// group's two fp32 boxes become its hi box and its lo box), U takes three
+// products (B_hi (w x)_hi + B_hi (w x)_lo + B_lo (w x)_hi), and the chunk
+// states leave as fp32, rows [b, nh, nc, S] x H.
 template <int H, int T, int KB, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 2)
 k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
@@ -126,6 +127,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     constexpr int kKb = KB;
     static_assert(KB == 64 || KB == 128, "sub-blocks of 64 or 128 tokens");
     static_assert(T % KB == 0, "whole sub-blocks per chunk");
+    static_assert(!SPLIT || KB == 64, "split: two fold threads per token row");
     constexpr int nsb = T / kKb;              // sub-blocks per chunk
     // this CTA's chunks [c_begin, c_begin + nchl)
     const int c_begin = seg * p.cps;
@@ -187,19 +189,16 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             uint8_t* sX = sB + p.off_x_in_stage;
             float* sV = reinterpret_cast<float*>(sB + p.off_w_in_stage);  // G[kKb], dt[kKb], G_last
             if (lane == 0) {
+                // split: B as two planes, x as fp32 (the same bytes as its hi/lo pair)
                 constexpr int planes = SPLIT ? 2 : 1;
                 tc::mbar_arrive_expect_tx(&bars[kBarFull + st], planes * (2 + H / 64) * x_box_bytes);
-                for (int pl = 0; pl < planes; ++pl) {
-                    uint8_t* sBp = sB + pl * p.off_blo_in_stage;
-                    uint8_t* sXp = pl ? sB + p.off_xlo_in_stage : sX;
-                    const int gi = SPLIT ? 2 * grp + pl : grp, hi = SPLIT ? 2 * h + pl : h;
+                for (int pl = 0; pl < planes; ++pl)
                     for (int kb = 0; kb < 2; ++kb)
-                        tc::tma_load_4d(sBp + kb * x_box_bytes, &tm_b, &bars[kBarFull + st], mt * 128 + kb * 64, gi,
-                                        tok, (int)b);
-                    for (int cb = 0; cb < H / 64; ++cb)
-                        tc::tma_load_4d(sXp + cb * x_box_bytes, &tm_x, &bars[kBarFull + st], cb * 64, hi, tok,
-                                        (int)b);
-                }
+                        tc::tma_load_4d(sB + pl * p.off_blo_in_stage + kb * x_box_bytes, &tm_b, &bars[kBarFull + st],
+                                        mt * 128 + kb * 64, SPLIT ? 2 * grp + pl : grp, tok, (int)b);
+                constexpr int xcols = SPLIT ? 32 : 64;  // columns per box
+                for (int cb = 0; cb < H / xcols; ++cb)
+                    tc::tma_load_4d(sX + cb * x_box_bytes, &tm_x, &bars[kBarFull + st], cb * xcols, h, tok, (int)b);
             }
             // G_t and dt_t of the sub-block's tokens (past the last valid token:
             // G of the last one and dt = 0) and G_last of the chunk, gathered
@@ -230,9 +229,12 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // address field, in 16-byte units, cannot carry: shared memory is
             // below 256 KB) and by 2 KB (128 units) per 16 tokens.
             const uint64_t desc0 = tc::sdesc_sw128(tc::smem_u32(smem), x_box_bytes, 1024);
+            // split: w x's 64-column hi boxes are two boxes apart (its lo
+            // boxes in between)
+            const uint64_t xdesc0 = tc::sdesc_sw128(tc::smem_u32(smem), (SPLIT ? 2 : 1) * x_box_bytes, 1024);
             const uint64_t stage_step = p.stage_bytes >> 4, x_step = p.off_x_in_stage >> 4;
             const uint64_t blo_step = p.off_blo_in_stage >> 4, xlo_step = p.off_xlo_in_stage >> 4;
-            uint64_t dstage = desc0;
+            uint64_t dstage = desc0, xstage = xdesc0;
             int st = 0;
             uint32_t phase = 0;
             for (int u = 0; u < nsub; ++u) {
@@ -253,7 +255,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
                         for (int k16 = 0; k16 < kKb / 16; ++k16)
-                            tc::mma_bf16_ss(tu, dstage + pa[ps] + 128 * k16, dstage + pb[ps] + 128 * k16, idesc,
+                            tc::mma_bf16_ss(tu, dstage + pa[ps] + 128 * k16, xstage + pb[ps] + 128 * k16, idesc,
                                             (sb > 0 || ps > 0 || k16 > 0) ? 1u : 0u);
                 } else {
 #pragma unroll
@@ -267,8 +269,10 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     st = 0;
                     phase ^= 1u;
                     dstage = desc0;
+                    xstage = xdesc0;
                 } else {
                     dstage += stage_step;
+                    xstage += stage_step;
                 }
             }
             if (!ok) set_abort(ctl, p.status);
@@ -291,26 +295,38 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const float w = sV[kKb + frow] * exp2f(sV[2 * kKb] - sV[frow]);  // w_t = dt_t exp2(G_last - G_t)
                 uint8_t* rowp = smem + st * p.stage_bytes + p.off_x_in_stage + frow * 128;
                 if (SPLIT) {
-                    // w x from hi + lo in fp32, written back as a hi/lo pair
-                    uint8_t* rowl = smem + st * p.stage_bytes + p.off_xlo_in_stage + frow * 128;
+                    // fp32 x -> w x as a hi/lo pair, one 64-column group at a
+                    // time: this thread reads its 32-column box of the row,
+                    // and after both threads of the row have read, writes its
+                    // 32 columns into the group's hi box (the first of the two)
+                    // and lo box (the second)
+#pragma unroll 1
+                    for (int cg = 0; cg < H / 64; ++cg) {
+                        uint8_t* grow = rowp + 2 * cg * x_box_bytes;
+                        float v[32];
 #pragma unroll
-                    for (int f = 0; f < 16; ++f) {
-                        if (f >= per) break;
-                        const int flat = fh * per + f;
-                        const uint32_t off = (flat >> 3) * x_box_bytes + ((((flat & 7) + frow) & 7) << 4);
-                        const uint4 vh = *reinterpret_cast<const uint4*>(rowp + off);
-                        const uint4 vl = *reinterpret_cast<const uint4*>(rowl + off);
-                        const uint32_t hw[4] = {vh.x, vh.y, vh.z, vh.w}, lw[4] = {vl.x, vl.y, vl.z, vl.w};
-                        uint32_t oh[4], ol[4];
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const float a0 = (tc::bf16_lo(hw[x]) + tc::bf16_lo(lw[x])) * w;
-                            const float a1 = (tc::bf16_hi(hw[x]) + tc::bf16_hi(lw[x])) * w;
-                            oh[x] = tc::pack_bf16x2(a0, a1);
-                            ol[x] = tc::pack_bf16x2(a0 - tc::bf16_lo(oh[x]), a1 - tc::bf16_hi(oh[x]));
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 f = *reinterpret_cast<const float4*>(grow + fh * x_box_bytes +
+                                                                              ((j ^ (frow & 7)) << 4));
+                            v[4 * j] = f.x * w;
+                            v[4 * j + 1] = f.y * w;
+                            v[4 * j + 2] = f.z * w;
+                            v[4 * j + 3] = f.w * w;
                         }
-                        *reinterpret_cast<uint4*>(rowp + off) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-                        *reinterpret_cast<uint4*>(rowl + off) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t off = (((4 * fh + j) ^ (frow & 7)) << 4);
+                            uint32_t oh[4], ol[4];
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) {
+                                const float a0 = v[8 * j + 2 * x], a1 = v[8 * j + 2 * x + 1];
+                                oh[x] = tc::pack_bf16x2(a0, a1);
+                                ol[x] = tc::pack_bf16x2(a0 - tc::bf16_lo(oh[x]), a1 - tc::bf16_hi(oh[x]));
+                            }
+                            *reinterpret_cast<uint4*>(grow + off) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                            *reinterpret_cast<uint4*>(grow + x_box_bytes + off) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                        }
                     }
                 }
 #pragma unroll
@@ -387,10 +403,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (cl + 1 < nchl) gl_next = glast_of(c + 1);
                 if (ok) ok = tc::mbar_wait(&bars[kBarUDone + ub], (cl >> 1) & 1, abort_flag);
                 tc::tc_fence_after();
-                // first state row of the tile (split: of its hi plane; the lo
-                // plane's rows follow S rows later)
-                const int64_t row0 = (SPLIT ? (bh * g.nchunks + c) * 2 * S : (bh * g.nchunks + c) * S) + mt * 128;
-                constexpr uint32_t lo_tile = (H / 64) * 8192;  // split: the lo tile follows the hi tile
+                const int64_t row0 = (bh * g.nchunks + c) * S + mt * 128;  // first state row of the tile
                 if (!store && ok) {
                     // h <- exp2(G_last) h + U_c only
 #pragma unroll 1
@@ -416,22 +429,27 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                             tc::tmem_ld16_nowait(tm_u0 + ub * H + lane_base + 16 * m, uv);
                             tc::tmem_wait_ld16(hv);
                             tc::tmem_wait_ld16(uv);
-                            uint8_t* rowp = stg + (m >> 2) * 8192 + hrow * 128;
+                            if (SPLIT) {
+                                // fp32: columns 16m .. 16m + 15 are 16-byte
+                                // chunks 4 (m & 1) .. + 3 of box m / 2
+                                uint8_t* rowp = stg + (m >> 1) * 8192 + hrow * 128;
 #pragma unroll
-                            for (int s4 = 0; s4 < 2; ++s4) {
-                                const int e = 8 * s4, j = 2 * (m & 3) + s4;  // 16-byte chunk in the row
-                                uint32_t wh[4], wl[4];
+                                for (int j = 0; j < 4; ++j)
+                                    *reinterpret_cast<uint4*>(rowp + (((4 * (m & 1) + j) ^ (hrow & 7)) << 4)) =
+                                        make_uint4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
+                            } else {
+                                uint8_t* rowp = stg + (m >> 2) * 8192 + hrow * 128;
 #pragma unroll
-                                for (int x = 0; x < 4; ++x) {
-                                    const float a0 = __uint_as_float(hv[e + 2 * x]);
-                                    const float a1 = __uint_as_float(hv[e + 2 * x + 1]);
-                                    wh[x] = tc::pack_bf16x2(a0, a1);
-                                    if (SPLIT) wl[x] = tc::pack_bf16x2(a0 - tc::bf16_lo(wh[x]), a1 - tc::bf16_hi(wh[x]));
+                                for (int s4 = 0; s4 < 2; ++s4) {
+                                    const int e = 8 * s4, j = 2 * (m & 3) + s4;  // 16-byte chunk in the row
+                                    uint32_t wh[4];
+#pragma unroll
+                                    for (int x = 0; x < 4; ++x)
+                                        wh[x] = tc::pack_bf16x2(__uint_as_float(hv[e + 2 * x]),
+                                                                __uint_as_float(hv[e + 2 * x + 1]));
+                                    *reinterpret_cast<uint4*>(rowp + ((j ^ (hrow & 7)) << 4)) =
+                                        make_uint4(wh[0], wh[1], wh[2], wh[3]);
                                 }
-                                const uint32_t off = (j ^ (hrow & 7)) << 4;
-                                *reinterpret_cast<uint4*>(rowp + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-                                if (SPLIT)
-                                    *reinterpret_cast<uint4*>(rowp + lo_tile + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                             }
 #pragma unroll
                             for (int e = 0; e < 16; ++e)
@@ -442,11 +460,9 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                     asm volatile("bar.sync 1, %0;" ::"r"(kScanWarps * 32) : "memory");
                     if (leader && ok) {
-                        for (int cb = 0; cb < H / 64; ++cb) {
-                            tc::tma_store_2d(&tm_cs, stg + cb * 8192, cb * 64, (int)(row0 + 64 * half));
-                            if (SPLIT)
-                                tc::tma_store_2d(&tm_cs, stg + lo_tile + cb * 8192, cb * 64, (int)(row0 + S + 64 * half));
-                        }
+                        constexpr int scols = SPLIT ? 32 : 64;  // columns per box (fp32 / bf16)
+                        for (int cb = 0; cb < H / scols; ++cb)
+                            tc::tma_store_2d(&tm_cs, stg + cb * 8192, cb * scols, (int)(row0 + 64 * half));
                         tc::bulk_commit();
                         tc::bulk_wait_read_all();  // the tile may be refilled
                     }
@@ -549,13 +565,14 @@ bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2, bool split = fa
     p.nsb = (int)(g.chunk / kKb);
     p.off_blo_in_stage = 2 * kKb * 128;
     p.off_x_in_stage = planes * 2 * kKb * 128;
-    p.off_xlo_in_stage = p.off_x_in_stage + (H / 64) * kKb * 128;
+    // split: a 64-column group's lo box follows its hi box
+    p.off_xlo_in_stage = p.off_x_in_stage + kKb * 128;
     p.off_w_in_stage = p.off_x_in_stage + planes * (H / 64) * kKb * 128;
     // G[kKb], dt[kKb], G_last; padded to keep stages 1 KB aligned
     p.stage_bytes = p.off_w_in_stage + ((2 * kKb + 1) * 4 + 1023) / 1024 * 1024;
     const uint32_t budget = two ? (kSmemLimit / 2 - 2048) : kSmemLimit;
     const uint32_t fixed = kNumBars * 8 + 64 + 1024;
-    // 64 rows x H bf16 (boxes of 64 columns) per plane
+    // 64 rows x H: bf16 (boxes of 64 columns), or fp32 (split; boxes of 32)
     const uint32_t stg_bytes = planes * (uint32_t)(H / 64) * 8192;
     int nst = (int)((budget - fixed - stg_bytes) / p.stage_bytes);
     if (nst > kMaxStages) nst = kMaxStages;
@@ -607,6 +624,8 @@ bool state_pass_tc_fits(const Geom& g) {
     if (g.headdim != 64 && g.headdim != 128) return false;
     if (g.dstate != 64 && g.dstate != 128 && g.dstate != 256) return false;
     if (g.batch * g.seqlen >= (int64_t(1) << 31)) return false;
+    // chunk-state rows are TMA coordinates (32-bit)
+    if (g.batch * g.nheads * g.nchunks * g.dstate >= (int64_t(1) << 31)) return false;
     SpTcParams p;
     return plan(g, p);
 }
@@ -640,13 +659,17 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     p.status = device_status_word();
     const uint64_t H = g.headdim, S = g.dstate, nh = g.nheads, L = g.seqlen, G = g.ngroups;
     const int kKb = p.kb;
-    const uint64_t planes = split ? 2 : 1;  // split: hi/lo planes as twice the heads, groups and state rows
+    const uint64_t planes = split ? 2 : 1;  // split: B's hi/lo planes as twice the groups
+    const uint64_t xe = split ? 4 : 2;       // bytes of an x and chunk-state element
+    const uint32_t xcols = split ? 32 : 64;  // columns of their boxes
     CUtensorMap tm_x, tm_b;
     {
-        const uint64_t dims[4] = {H, planes * nh, L, (uint64_t)g.batch};
-        const uint64_t strides[3] = {H * 2, planes * nh * H * 2, L * planes * nh * H * 2};
-        const uint32_t box[4] = {64, 1, kKb, 1};
-        if (!make_tmap_bf16(&tm_x, a.x, 4, dims, strides, box)) return cudaErrorInvalidValue;
+        const uint64_t dims[4] = {H, nh, L, (uint64_t)g.batch};
+        const uint64_t strides[3] = {H * xe, nh * H * xe, L * nh * H * xe};
+        const uint32_t box[4] = {xcols, 1, (uint32_t)kKb, 1};
+        if (!make_tmap(&tm_x, split ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, 4,
+                       dims, strides, box))
+            return cudaErrorInvalidValue;
     }
     {
         const uint64_t dims[4] = {S, planes * G, L, (uint64_t)g.batch};
@@ -656,11 +679,13 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     }
     CUtensorMap tm_cs;
     {
-        const uint64_t rows = (uint64_t)g.batch * nh * g.nchunks * planes * S;
+        const uint64_t rows = (uint64_t)g.batch * nh * g.nchunks * S;
         const uint64_t dims[2] = {H, rows};
-        const uint64_t strides[1] = {H * 2};
-        const uint32_t box[2] = {64, 64};
-        if (!make_tmap_bf16(&tm_cs, a.chunk_states, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        const uint64_t strides[1] = {H * xe};
+        const uint32_t box[2] = {xcols, 64};
+        if (!make_tmap(&tm_cs, split ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                       a.chunk_states, 2, dims, strides, box))
+            return cudaErrorInvalidValue;
     }
     auto kern = split ? (g.headdim == 64 ? k_state_pass_tc<64, 128, 64, true> : k_state_pass_tc<128, 128, 64, true>)
                 : (g.headdim == 64)

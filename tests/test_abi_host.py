@@ -164,3 +164,20 @@ def test_step_rejects_misaligned(lib):
 def test_selftest_rejects_out_of_range_limits(lib, limit):
     """Checked on the host: nothing is launched for a bad limit."""
     assert lib.mamba2_selftest_wait_timeout(limit, None) == INVALID
+
+
+def test_workspace_size_fp32_tensor_core_path(lib):
+    """An fp32 problem whose stages 2 and 3 run on the tensor cores (chunk
+    128, head dim 64, state 128) keeps G, the fp32 chunk states and B as bf16
+    hi/lo planes (the bytes of fp32 B) in the workspace; a CUDA-core shape
+    (chunk 32) keeps G and the fp32 chunk states only."""
+    up = lambda v: (v + 255) // 256 * 256
+    s = _shape(batch=2, seqlen=1000, nheads=4, headdim=64, dstate=128, chunk_size=128, dtype_code=0)
+    nc = 8
+    g_bytes = 2 * 4 * 1000 * 4
+    cs_bytes = 2 * 4 * nc * 128 * 64 * 4
+    b_bytes = 2 * 1000 * 1 * 128 * 4
+    assert lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s)) == up(g_bytes) + up(cs_bytes) + up(b_bytes)
+    s = _shape(batch=2, seqlen=1000, nheads=4, headdim=64, dstate=128, chunk_size=32, dtype_code=0)
+    cs_bytes = 2 * 4 * 32 * 128 * 64 * 4
+    assert lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s)) == up(g_bytes) + up(cs_bytes)

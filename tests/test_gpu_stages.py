@@ -21,6 +21,9 @@ SHAPES = [
     ("fp32_tiny", 1, 256, 2, 16, 16, 1, 64, "fp32", False),
     ("fp32_ragged", 2, 203, 3, 16, 32, 1, 64, "fp32", True),
     ("fp32_small_chunk", 1, 100, 4, 32, 16, 2, 16, "fp32", True),
+    # fp32 chunks of 128: stage 3 runs the split-bf16 tensor-core kernel
+    ("fp32_t128_tc", 2, 300, 4, 64, 128, 2, 128, "fp32", True),
+    ("fp32_t128_h128_s64", 1, 256, 2, 128, 64, 1, 128, "fp32", False),
     ("bf16_t128", 2, 384, 4, 64, 64, 2, 128, "bf16", True),
     ("bf16_t256", 1, 512, 3, 64, 128, 1, 256, "bf16", True),
     ("bf16_t256_ragged", 2, 700, 2, 64, 128, 1, 256, "bf16", False),
