@@ -318,6 +318,10 @@ def run_gpu(args, w, rank, world):
     stream = torch.cuda.current_stream()
     shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
     ws = torch.empty(max(bd.mamba2_ssd_fwd_workspace_size(shape), 1), device="cuda", dtype=torch.uint8)
+    # the chunk the forward pass runs this shape with (the per-stage timings
+    # below launch the stages at that chunk, as the pass does)
+    run_chunk = bd.mamba2_ssd_fwd_chunk_size(shape)
+    wr = w.with_(chunk_size=run_chunk)
     y = torch.empty_like(d["x"])
     fin = torch.empty(w.batch, w.nheads, w.dstate, w.headdim, device="cuda", dtype=torch.float32)
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
@@ -376,20 +380,21 @@ def run_gpu(args, w, rank, world):
     torch.cuda.synchronize()
     host_us_per_call = min(host_us)
 
-    # ---- per-kernel durations: the same launches through the per-stage entry points
+    # ---- per-kernel durations: the same launches through the per-stage entry
+    # points, at the chunk the forward pass runs
     kev = {k: [] for k in ("chunk_cumsum", "state_pass", "chunk_out")}
     G = ws[: 4 * w.batch * w.nheads * w.seqlen].view(torch.float32).view(w.batch, w.nheads, w.seqlen)
-    cs = torch.empty(w.batch, w.nheads, w.nchunks, w.dstate, w.headdim, device="cuda", dtype=d["x"].dtype)
+    cs = torch.empty(w.batch, w.nheads, wr.nchunks, w.dstate, w.headdim, device="cuda", dtype=d["x"].dtype)
     for i in range(args.warmup + args.steps):
         flush.zero_()
         e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         e[0].record(stream)
-        bd.mamba2_chunk_cumsum(d["dt"], d["A"], w.chunk_size, G=G)
+        bd.mamba2_chunk_cumsum(d["dt"], d["A"], run_chunk, G=G)
         e[1].record(stream)
-        bd.mamba2_state_pass(d["x"], d["dt"], d["B"], G, w.chunk_size, initial_state=d["initial_state"],
+        bd.mamba2_state_pass(d["x"], d["dt"], d["B"], G, run_chunk, initial_state=d["initial_state"],
                              chunk_states=cs, final_state=fin)
         e[2].record(stream)
-        bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], G, cs, w.chunk_size, D=d["D"], y=y)
+        bd.mamba2_chunk_out(d["x"], d["dt"], d["B"], d["C"], G, cs, run_chunk, D=d["D"], y=y)
         e[3].record(stream)
         if i >= args.warmup:
             kev["chunk_cumsum"].append((e[0], e[1]))
@@ -400,7 +405,8 @@ def run_gpu(args, w, rank, world):
 
     if args.no_e2e:
         return {"total_ms": total_ms, "step_ms": step_ms, "kernel_ms": kernel_ms, "clocks": clock_info,
-                "e2e_ms": None, "h2d": 0, "d2h": 0, "inp": inp, "host_us": host_us_per_call}
+                "e2e_ms": None, "h2d": 0, "d2h": 0, "inp": inp, "host_us": host_us_per_call,
+                "run_chunk": run_chunk}
 
     # ---- end to end through the public API with host buffers, pipelined as a
     # server runs it: two sets of device buffers; step i's inputs are copied in
@@ -455,7 +461,8 @@ def run_gpu(args, w, rank, world):
     bd.mamba2_check_device_status()
     e2e_total = max_over_ranks(sum(e2e_ms))
     return {"total_ms": total_ms, "step_ms": step_ms, "kernel_ms": kernel_ms, "clocks": clock_info,
-            "e2e_ms": e2e_total, "h2d": h2d, "d2h": d2h, "inp": inp, "host_us": host_us_per_call}
+            "e2e_ms": e2e_total, "h2d": h2d, "d2h": d2h, "inp": inp, "host_us": host_us_per_call,
+            "run_chunk": run_chunk}
 
 
 EXTRA_WORKLOADS = ("mamba2_1p3b_layer", "large_state", "blog_example", "long_seq_fp32_t128")
@@ -496,9 +503,11 @@ def run_extra(args, w, peaks, cpu_pairs):
     torch.cuda.synchronize()
     bd.mamba2_check_device_status()
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    flop, flop_dense, bytes_min = work_counts(w)
+    run_chunk = bd.mamba2_ssd_fwd_chunk_size(shape)
+    flop, flop_dense, bytes_min = work_counts(w.with_(chunk_size=run_chunk))
     out = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
            "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk_size": w.chunk_size,
+           "run_chunk_size": run_chunk,
            "seed": w.seed, "tokens_per_s": w.tokens / (ms * 1e-3), "ms_per_step": ms,
            "tflops": flop / (ms * 1e-3) / 1e12,
            "hbm_frac": bytes_min / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -525,12 +534,14 @@ def main():
     r = run_gpu(args, w, rank, world)
     if rank != 0:
         return
-    flop, flop_dense, bytes_min = work_counts(w)
+    # FLOPs and per-kernel bytes at the chunk the forward pass runs
+    wr = w.with_(chunk_size=r["run_chunk"])
+    flop, flop_dense, bytes_min = work_counts(wr)
     peaks = load_peaks()
     ms = r["total_ms"] / args.steps
     tokens = w.tokens * world
     value = job_tokens_per_s(w.tokens, world, ms)
-    kb = kernel_bytes(w)
+    kb = kernel_bytes(wr)
     top = max(r["kernel_ms"], key=r["kernel_ms"].get)
     achieved = kb[top] / (r["kernel_ms"][top] * 1e-3) / 1e9
     out = {
@@ -539,7 +550,8 @@ def main():
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
                    "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
-                   "chunk_size": w.chunk_size, "initial_state": w.init_state,
+                   "chunk_size": w.chunk_size, "run_chunk_size": r["run_chunk"],
+                   "initial_state": w.init_state,
                    "l2": "flushed: 256 MiB buffer written before every timed step",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tflops": flop / (ms * 1e-3) / 1e12 * world,

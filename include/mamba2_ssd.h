@@ -120,20 +120,32 @@ MAMBA2_API mamba2_status mamba2_chunk_out(const mamba2_shape* shape, const void*
                                const void* chunk_states, void* y, struct CUstream_st* stream);
 
 /* Bytes of device workspace mamba2_ssd_fwd needs for `shape` (0 for an
- * invalid shape): G, the chunk states and, for bf16 problems with too few
- * (batch, head) pairs to fill the GPU, the fp32 states at the boundaries of
- * the sequence segments its state pass runs over.  A pure function of the
- * shape (and of the MAMBA2_STATE_SEGMENTS environment variable, "1" = no
- * segments).  The workspace holds intermediates only; its contents on entry
- * do not matter. */
+ * invalid shape): G, the chunk states (at the chunk the pass runs with, see
+ * mamba2_ssd_fwd), for bf16 problems with too few (batch, head) pairs to fill
+ * the GPU the fp32 states at the boundaries of the sequence segments its
+ * state pass runs over, and for fp32 problems on the tensor cores B as bf16
+ * hi/lo planes.  A pure function of the shape (and of the environment
+ * variables MAMBA2_STATE_SEGMENTS, "1" = no segments, MAMBA2_FWD_CHUNK and
+ * MAMBA2_FP32_PATH, which force a variant).  The workspace holds
+ * intermediates only; its contents on entry do not matter. */
 MAMBA2_API size_t mamba2_ssd_fwd_workspace_size(const mamba2_shape* shape);
+
+/* The chunk mamba2_ssd_fwd runs `shape` with (see there): one of 64, 128 or
+ * 256 chosen per shape, or shape->chunk_size; 0 for an invalid shape.  A pure
+ * function of the shape and of the environment variables named under
+ * mamba2_ssd_fwd_workspace_size. */
+MAMBA2_API int64_t mamba2_ssd_fwd_chunk_size(const mamba2_shape* shape);
 
 /* The whole forward pass [blog §Mamba-2 architecture, "three kernels"]:
  * y and final_state of the recurrence above, from x, dt, A, B, C, D and an
  * optional initial_state (NULL means zeros; final_state NULL means not
  * written).  `workspace` must be a 256-byte aligned device buffer of at least
  * mamba2_ssd_fwd_workspace_size(shape) bytes, not overlapping any tensor.
- * Enqueues the stages on `stream`. */
+ * Enqueues the stages on `stream`.  y and final_state do not depend on the
+ * chunk length (it regroups the sums; only rounding changes), and neither G
+ * nor the chunk states leave this call, so the pass runs with the chunk
+ * measured fastest for the shape (64, 128 or 256), which need not be
+ * shape->chunk_size; MAMBA2_FWD_CHUNK=given makes it use shape->chunk_size. */
 MAMBA2_API mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const float* dt,
                              const float* A, const void* B, const void* C, const float* D,
                              const float* initial_state, void* y, float* final_state,

@@ -57,6 +57,7 @@ def load_library(path: str = LIB_PATH):
         "mamba2_state_pass": (ctypes.c_int, [S, P, P, P, P, P, P, P, P]),
         "mamba2_chunk_out": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P]),
         "mamba2_ssd_fwd_workspace_size": (ctypes.c_size_t, [S]),
+        "mamba2_ssd_fwd_chunk_size": (ctypes.c_int64, [S]),
         "mamba2_ssd_fwd": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]),
         "mamba2_ssd_fwd_noalloc": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P]),
         "mamba2_ssd_step": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P, P]),
@@ -162,6 +163,10 @@ def mamba2_chunk_out(x, dt, B, C, G, chunk_states, chunk_size, D=None, y=None, s
 
 def mamba2_ssd_fwd_workspace_size(shape: mamba2_shape) -> int:
     return int(load_library().mamba2_ssd_fwd_workspace_size(ctypes.byref(shape)))
+
+
+def mamba2_ssd_fwd_chunk_size(shape: mamba2_shape) -> int:
+    return int(load_library().mamba2_ssd_fwd_chunk_size(ctypes.byref(shape)))
 
 
 def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, D=None, initial_state=None, y=None, final_state=None,

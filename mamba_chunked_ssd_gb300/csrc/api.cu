@@ -1,6 +1,7 @@
 // api.cu — the extern "C" boundary: argument checks, workspace layout and
 // launch sequencing.  No arithmetic of the method lives here; every step of
 // the forward pass runs in the kernels of the other translation units.
+#include <stdlib.h>
 #include <string.h>
 
 #include <map>
@@ -12,7 +13,7 @@
 namespace m2 {
 namespace {
 
-constexpr int kVersion = 1 * 10000 + 1 * 100 + 0;
+constexpr int kVersion = 1 * 10000 + 2 * 100 + 0;
 
 // Per-device status word: kernels with bounded waits record a timeout here.
 __device__ unsigned int g_status_word = 0;
@@ -152,6 +153,48 @@ bool fwd_f32_tensor_cores(const mamba2_shape& s) {
     return use_f32_tensor_cores(make_geom(s), false);
 }
 
+// The chunk the forward pass evaluates with.  The output and the final state
+// do not depend on the chunk length (regrouping the sums of the chunked form
+// changes rounding only), and mamba2_ssd_fwd exposes neither G nor the chunk
+// states, so it runs the chunk measured fastest for the shape on GB300:
+//  - fp32 shapes the split-bf16 tensor-core kernels cover at chunk 128: 128;
+//  - bf16 tensor-core shapes: 256 for state 128 with head dim 128; 128 for
+//    state 64 or 256, and for state 128 with head dim 64 when the (batch,
+//    head) pairs outnumber the SMs; otherwise the caller's chunk (64 becomes
+//    128: chunks of 64 were never the fastest);
+//  - everything else (the CUDA-core kernels): the caller's chunk.
+// MAMBA2_FWD_CHUNK=given keeps the caller's; =64, =128 or =256 forces one
+// (for tests and for timing the candidates on one shape).
+int64_t fwd_chunk(const mamba2_shape& s) {
+    const char* env = getenv("MAMBA2_FWD_CHUNK");
+    if (env && strcmp(env, "given") == 0) return s.chunk_size;
+    if (env && (strcmp(env, "64") == 0 || strcmp(env, "128") == 0 || strcmp(env, "256") == 0))
+        return atoi(env);
+    if (s.batch == 0 || s.seqlen == 0) return s.chunk_size;
+    mamba2_shape t = s;
+    t.chunk_size = 128;
+    if (s.dtype == MAMBA2_F32) return use_f32_tensor_cores(make_geom(t), false) ? 128 : s.chunk_size;
+    const bool tc_h = s.headdim == 64 || s.headdim == 128;
+    const bool tc_s = s.dstate == 64 || s.dstate == 128 || s.dstate == 256;
+    if (!tc_h || !tc_s) return s.chunk_size;
+    int64_t want;
+    if (s.dstate == 128 && s.headdim == 128)
+        want = 256;
+    else if (s.dstate != 128 || s.batch * s.nheads > 152)
+        want = 128;
+    else
+        want = s.chunk_size == 64 ? 128 : s.chunk_size;
+    t.chunk_size = want;
+    const Geom g = make_geom(t);
+    return (chunk_out_tc_fits(g) && state_pass_tc_fits(g)) ? want : s.chunk_size;
+}
+
+mamba2_shape fwd_shape(const mamba2_shape& s) {
+    mamba2_shape r = s;
+    r.chunk_size = fwd_chunk(s);
+    return r;
+}
+
 // Segments of the forward pass's state pass (bf16 on tensor cores only).
 int fwd_segments(const mamba2_shape& s) {
     if (s.dtype != MAMBA2_BF16 || s.batch == 0 || s.seqlen == 0) return 1;
@@ -203,8 +246,15 @@ mamba2_status mamba2_chunk_out(const mamba2_shape* shape, const void* x, const f
     return run_chunk_out(*shape, a, (cudaStream_t)stream);
 }
 
-size_t mamba2_ssd_fwd_workspace_size(const mamba2_shape* shape) {
+int64_t mamba2_ssd_fwd_chunk_size(const mamba2_shape* shape) {
     if (check_shape(shape) != MAMBA2_OK) return 0;
+    return fwd_chunk(*shape);
+}
+
+size_t mamba2_ssd_fwd_workspace_size(const mamba2_shape* user_shape) {
+    if (check_shape(user_shape) != MAMBA2_OK) return 0;
+    const mamba2_shape si = fwd_shape(*user_shape);  // the chunk the pass runs with
+    const mamba2_shape* shape = &si;
     const Sizes z = sizes_of(*shape);
     // fp32 on the tensor cores: G, the fp32 chunk states, then B as bf16
     // hi/lo planes (the bytes of fp32 B)
@@ -214,14 +264,16 @@ size_t mamba2_ssd_fwd_workspace_size(const mamba2_shape* shape) {
     return (size_t)(round_up(z.G, 256) + round_up(z.cs, 256) + round_up(seg, 256));
 }
 
-mamba2_status mamba2_ssd_fwd(const mamba2_shape* shape, const void* x, const float* dt,
+mamba2_status mamba2_ssd_fwd(const mamba2_shape* user_shape, const void* x, const float* dt,
                              const float* A, const void* B, const void* C, const float* D,
                              const float* initial_state, void* y, float* final_state,
                              void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
-    mamba2_status rc = check_shape(shape);
+    mamba2_status rc = check_shape(user_shape);
     if (rc != MAMBA2_OK) return rc;
+    const mamba2_shape si = fwd_shape(*user_shape);  // the chunk the pass runs with
+    const mamba2_shape* shape = &si;
     const Sizes z = sizes_of(*shape);
-    const size_t need = mamba2_ssd_fwd_workspace_size(shape);
+    const size_t need = mamba2_ssd_fwd_workspace_size(user_shape);
     if (workspace_bytes < need) return MAMBA2_ERR_INVALID_ARG;
     if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return MAMBA2_ERR_INVALID_ARG;

@@ -19,13 +19,13 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = bd.header_functions()
-    assert len(names) == 11
+    assert len(names) == 12
     for n in names:
         assert hasattr(lib, n), f"{n} declared in the header but not exported"
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mamba2_version() == 10100
+    assert lib.mamba2_version() == 10200
     for code in range(5):
         s = lib.mamba2_status_string(code).decode()
         assert s.startswith(bd.STATUS[code])
@@ -166,18 +166,64 @@ def test_selftest_rejects_out_of_range_limits(lib, limit):
     assert lib.mamba2_selftest_wait_timeout(limit, None) == INVALID
 
 
-def test_workspace_size_fp32_tensor_core_path(lib):
-    """An fp32 problem whose stages 2 and 3 run on the tensor cores (chunk
-    128, head dim 64, state 128) keeps G, the fp32 chunk states and B as bf16
-    hi/lo planes (the bytes of fp32 B) in the workspace; a CUDA-core shape
-    (chunk 32) keeps G and the fp32 chunk states only."""
+def test_workspace_size_fp32_tensor_core_path(lib, monkeypatch):
+    """An fp32 problem whose stages 2 and 3 run on the tensor cores (head dim
+    64, state 128) keeps G, the fp32 chunk states at chunk 128 and B as bf16
+    hi/lo planes (the bytes of fp32 B) in the workspace, whatever chunk the
+    caller gives (the forward pass runs chunk 128 there); with
+    MAMBA2_FWD_CHUNK=given a chunk of 32 runs on the CUDA cores and keeps G
+    and the fp32 chunk states at chunk 32 only."""
     up = lambda v: (v + 255) // 256 * 256
-    s = _shape(batch=2, seqlen=1000, nheads=4, headdim=64, dstate=128, chunk_size=128, dtype_code=0)
-    nc = 8
     g_bytes = 2 * 4 * 1000 * 4
-    cs_bytes = 2 * 4 * nc * 128 * 64 * 4
+    cs_bytes = 2 * 4 * 8 * 128 * 64 * 4
     b_bytes = 2 * 1000 * 1 * 128 * 4
-    assert lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s)) == up(g_bytes) + up(cs_bytes) + up(b_bytes)
+    for T in (128, 32, 256):
+        s = _shape(batch=2, seqlen=1000, nheads=4, headdim=64, dstate=128, chunk_size=T, dtype_code=0)
+        assert lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s)) == up(g_bytes) + up(cs_bytes) + up(b_bytes)
+    monkeypatch.setenv("MAMBA2_FWD_CHUNK", "given")
     s = _shape(batch=2, seqlen=1000, nheads=4, headdim=64, dstate=128, chunk_size=32, dtype_code=0)
     cs_bytes = 2 * 4 * 32 * 128 * 64 * 4
     assert lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s)) == up(g_bytes) + up(cs_bytes)
+
+
+def test_forward_pass_chunk_choice(lib, monkeypatch):
+    """The forward pass's chunk (seen through the workspace's chunk-state
+    bytes): bf16 state 256 runs chunk 128 whatever the caller's chunk; state
+    128 with head dim 128 runs 256; state 128 with head dim 64 runs 128 when
+    the (batch, head) pairs outnumber the SMs and the caller's chunk
+    otherwise; MAMBA2_FWD_CHUNK forces one."""
+    up = lambda v: (v + 255) // 256 * 256
+
+    def ws(b, L, nh, H, S, T):
+        s = _shape(batch=b, seqlen=L, nheads=nh, headdim=H, dstate=S, chunk_size=T, dtype_code=1)
+        return lib.mamba2_ssd_fwd_workspace_size(ctypes.byref(s))
+
+    def expect(b, L, nh, H, S, Trun):
+        nc = -(-L // Trun)
+        return up(b * nh * L * 4) + up(b * nh * nc * S * H * 2)
+
+    assert ws(4, 4096, 64, 64, 256, 256) == expect(4, 4096, 64, 64, 256, 128)
+    assert ws(4, 4096, 64, 128, 128, 128) == expect(4, 4096, 64, 128, 128, 256)
+    assert ws(4, 4096, 64, 64, 128, 256) == expect(4, 4096, 64, 64, 128, 128)   # 256 pairs
+    assert ws(2, 4096, 64, 64, 128, 256) == expect(2, 4096, 64, 64, 128, 256)   # 128 pairs
+    assert ws(2, 4096, 64, 64, 128, 64) == expect(2, 4096, 64, 64, 128, 128)    # 64 -> 128
+    assert ws(4, 4096, 64, 16, 16, 32) == expect(4, 4096, 64, 16, 16, 32)       # CUDA cores
+    monkeypatch.setenv("MAMBA2_FWD_CHUNK", "given")
+    assert ws(4, 4096, 64, 64, 256, 256) == expect(4, 4096, 64, 64, 256, 256)
+    monkeypatch.setenv("MAMBA2_FWD_CHUNK", "64")
+    assert ws(4, 4096, 64, 64, 256, 256) == expect(4, 4096, 64, 64, 256, 64)
+
+
+def test_forward_pass_chunk_size_query(lib, monkeypatch):
+    """mamba2_ssd_fwd_chunk_size reports the chunk the forward pass runs
+    with: 0 for an invalid shape, the rule's choice, or the forced one."""
+    assert lib.mamba2_ssd_fwd_chunk_size(None) == 0
+    s = _shape(batch=4, seqlen=4096, nheads=64, headdim=64, dstate=256, chunk_size=256, dtype_code=1)
+    assert lib.mamba2_ssd_fwd_chunk_size(ctypes.byref(s)) == 128
+    s = _shape(batch=4, seqlen=4096, nheads=64, headdim=128, dstate=128, chunk_size=64, dtype_code=1)
+    assert lib.mamba2_ssd_fwd_chunk_size(ctypes.byref(s)) == 256
+    s = _shape(batch=1, seqlen=64, nheads=2, headdim=16, dstate=16, chunk_size=48, dtype_code=0)
+    assert lib.mamba2_ssd_fwd_chunk_size(ctypes.byref(s)) == 48
+    monkeypatch.setenv("MAMBA2_FWD_CHUNK", "given")
+    s = _shape(batch=4, seqlen=4096, nheads=64, headdim=64, dstate=256, chunk_size=256, dtype_code=1)
+    assert lib.mamba2_ssd_fwd_chunk_size(ctypes.byref(s)) == 256

@@ -48,13 +48,17 @@ def _lib():
 
 
 @pytest.mark.parametrize("w", SHAPES, ids=[w.name for w in SHAPES])
-def test_random_shape_matches_oracle(w):
+def test_random_shape_matches_oracle(w, monkeypatch):
+    """With the forward pass's own chunk choice and with the caller's chunk."""
     inp = make_inputs(w)
     d = to_dev(inp)
-    y, fin = bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size, D=d["D"],
-                               initial_state=d["initial_state"])
-    bd.mamba2_check_device_status()
     r = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"],
                               init=inp["initial_state"])
-    assert rel_err(np64(y), r["y"]) <= TOL[w.dtype]
-    assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype]
+    for chunk in (None, "given"):
+        if chunk:
+            monkeypatch.setenv("MAMBA2_FWD_CHUNK", chunk)
+        y, fin = bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size, D=d["D"],
+                                   initial_state=d["initial_state"])
+        bd.mamba2_check_device_status()
+        assert rel_err(np64(y), r["y"]) <= TOL[w.dtype], chunk
+        assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype], chunk

@@ -57,6 +57,24 @@ def test_small_full_compare(w):
     assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype]
 
 
+# The forward pass may run another chunk than the caller's (the result does
+# not depend on it); each forced chunk on shapes where it is not the given one.
+CHUNK_SHAPES = [w for w in SMALL if w.dtype == "bf16"]
+
+
+@pytest.mark.parametrize("chunk", ["given", "64", "128", "256"])
+@pytest.mark.parametrize("w", CHUNK_SHAPES, ids=[w.name for w in CHUNK_SHAPES])
+def test_forward_pass_chunk_override(w, chunk, monkeypatch):
+    monkeypatch.setenv("MAMBA2_FWD_CHUNK", chunk)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    y, fin = _fwd(d, w)
+    r = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"],
+                              init=inp["initial_state"])
+    assert rel_err(np64(y), r["y"]) <= TOL[w.dtype]
+    assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype]
+
+
 @pytest.mark.parametrize("name", ["tiny_fp32", "mamba2_1p3b_layer", "long_seq_carried_state",
                                   "large_state", "blog_example"])
 def test_named_workload_full_size(name):
@@ -391,6 +409,9 @@ F32_TC_SHAPES = [
     Workload("fp32_tc_h128_s64_ragged", 1, 333, 3, 128, 64, 1, 128, dtype="fp32", init_state=True),
     Workload("fp32_tc_32_heads", 1, 256, 32, 64, 64, 1, 128, dtype="fp32"),
     Workload("fp32_tc_h128_s128", 2, 300, 2, 128, 128, 2, 128, dtype="fp32", init_state=True),
+    # other chunks: the forward pass runs these at chunk 128 on the tensor cores
+    Workload("fp32_tc_given_t256", 1, 600, 4, 64, 128, 1, 256, dtype="fp32", init_state=True),
+    Workload("fp32_tc_given_t64", 2, 200, 2, 128, 64, 2, 64, dtype="fp32"),
 ]
 
 
