@@ -71,6 +71,7 @@ struct SpTcParams {
     int kb;             // tokens per sub-block (64 or 128)
     int nsb;            // sub-blocks per chunk = chunk / kb
     int nst;            // ring stages
+    int stg_tiles;      // 64-row staging tiles for the chunk-state stores (1 or 2)
     // stage: B [2 boxes] (split: B_hi, B_lo) | X [H / 64 boxes] (split: X_hi, X_lo) | G, dt, G_last
     uint32_t stage_bytes, off_blo_in_stage, off_x_in_stage, off_xlo_in_stage, off_w_in_stage, off_stg, off_bar,
         smem_bytes, tmem_cols;
@@ -159,7 +160,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     tc::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t tm_u0 = tmem;           // U buffers: [0, H), [H, 2H)
-    const uint32_t tm_h = tmem + 2 * H;    // running state: [2H, 3H)
+    const uint32_t tm_h = tmem + 2 * H;    // running state, two buffers: [2H, 3H), [3H, 4H)
     volatile int* abort_flag = &ctl->abort;
     const uint32_t x_box_bytes = kKb * 128;
 
@@ -385,14 +386,22 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 tc::tmem_st16(tm_h + lane_base + 16 * m, r);
             }
             tc::tmem_wait_st();
-            // Store h_c, then h <- exp2(G_last) h + U_c; G_last of the next chunk
-            // is fetched while this one waits for its U.  h_c leaves through a
-            // 64-row shared-memory tile (128-byte swizzle) and a TMA store: the
-            // warps of quadrants 0-1 fill it first, then those of quadrants 2-3.
+            // Per chunk: h_{c+1} = exp2(G_last) h_c + U_c into the other h
+            // buffer (then U_c's buffer is released to the MMA), then h_c is
+            // stored; G_last of the next chunk is fetched while this one waits
+            // for its U.  h_c leaves through 64-row shared-memory tiles
+            // (128-byte swizzle; quadrants 0-1 fill the first half's, 2-3 the
+            // second's) and TMA stores.
             uint8_t* stg = smem + p.off_stg;
             const int hrow = (q & 1) * 32 + lane;  // row inside the 64-row tile
             const bool leader = (q == 0 && lane == 0);
             const bool store = p.mode != kSegmentSummary;  // the summary keeps only the end state
+            // 64-row halves of this CTA's state rows (one for dstate 64) and
+            // the staging passes per chunk; a tile is 64 x H (bf16: boxes of
+            // 64 columns; split, fp32: boxes of 32)
+            const int nhalf = (S - mt * 128 >= 128) ? 2 : 1;
+            const int npass = p.stg_tiles >= nhalf ? 1 : nhalf;
+            constexpr uint32_t tile_bytes = (SPLIT ? H / 32 : H / 64) * 8192;
             float gl_next = glast_of(c_begin);
             // Every scan warp runs every iteration and every named barrier below,
             // whatever its own waits return, so no warp is left at a barrier;
@@ -404,41 +413,52 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (ok) ok = tc::mbar_wait(&bars[kBarUDone + ub], (cl >> 1) & 1, abort_flag);
                 tc::tc_fence_after();
                 const int64_t row0 = (bh * g.nchunks + c) * S + mt * 128;  // first state row of the tile
-                if (!store && ok) {
-                    // h <- exp2(G_last) h + U_c only
+                // h_{c+1} = exp2(G_last) h_c + U_c into the other h buffer;
+                // U_c's buffer is free once read
+                const uint32_t h_cur = tm_h + (cl & 1) * H, h_nxt = tm_h + ((cl + 1) & 1) * H;
+                if (ok) {
 #pragma unroll 1
                     for (int m = 0; m < H / 16; ++m) {
                         uint32_t hv[16], uv[16];
-                        tc::tmem_ld16_nowait(tm_h + lane_base + 16 * m, hv);
+                        tc::tmem_ld16_nowait(h_cur + lane_base + 16 * m, hv);
                         tc::tmem_ld16_nowait(tm_u0 + ub * H + lane_base + 16 * m, uv);
                         tc::tmem_wait_ld16(hv);
                         tc::tmem_wait_ld16(uv);
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
                             hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
-                        tc::tmem_st16(tm_h + lane_base + 16 * m, hv);
+                        tc::tmem_st16(h_nxt + lane_base + 16 * m, hv);
                     }
                 }
-                for (int half = 0; store && half < 2; ++half) {
-                    if (mt * 128 + 64 * half >= S) break;  // dstate = 64: one half only
-                    if (ok && (q >> 1) == half) {
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (ok && lane == 0) tc::mbar_arrive(&bars[kBarUFree + ub]);
+                // h_c, still in h_cur, leaves through the staging tiles: one
+                // pass when every 64-row half has its own tile (both quadrant
+                // pairs fill at once), else one pass per half through the one
+                // tile.  Each pass first waits until the stores before it have
+                // read the tiles (usually long done).
+                for (int pass = 0; store && pass < npass; ++pass) {
+                    if (leader) tc::bulk_wait_read_all();
+                    asm volatile("bar.sync 1, %0;" ::"r"(kScanWarps * 32) : "memory");
+                    const int hq = q >> 1;  // this quadrant pair's half
+                    if (ok && (npass == 1 ? hq < nhalf : hq == pass)) {
+                        uint8_t* tile = stg + (npass == 1 ? hq : 0) * tile_bytes;
 #pragma unroll 1
                         for (int m = 0; m < H / 16; ++m) {
-                            uint32_t hv[16], uv[16];
-                            tc::tmem_ld16_nowait(tm_h + lane_base + 16 * m, hv);
-                            tc::tmem_ld16_nowait(tm_u0 + ub * H + lane_base + 16 * m, uv);
-                            tc::tmem_wait_ld16(hv);
-                            tc::tmem_wait_ld16(uv);
+                            uint32_t hv[16];
+                            tc::tmem_ld16(h_cur + lane_base + 16 * m, hv);
                             if (SPLIT) {
                                 // fp32: columns 16m .. 16m + 15 are 16-byte
                                 // chunks 4 (m & 1) .. + 3 of box m / 2
-                                uint8_t* rowp = stg + (m >> 1) * 8192 + hrow * 128;
+                                uint8_t* rowp = tile + (m >> 1) * 8192 + hrow * 128;
 #pragma unroll
                                 for (int j = 0; j < 4; ++j)
                                     *reinterpret_cast<uint4*>(rowp + (((4 * (m & 1) + j) ^ (hrow & 7)) << 4)) =
                                         make_uint4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
                             } else {
-                                uint8_t* rowp = stg + (m >> 2) * 8192 + hrow * 128;
+                                uint8_t* rowp = tile + (m >> 2) * 8192 + hrow * 128;
 #pragma unroll
                                 for (int s4 = 0; s4 < 2; ++s4) {
                                     const int e = 8 * s4, j = 2 * (m & 3) + s4;  // 16-byte chunk in the row
@@ -451,27 +471,19 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                                         make_uint4(wh[0], wh[1], wh[2], wh[3]);
                                 }
                             }
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
-                            tc::tmem_st16(tm_h + lane_base + 16 * m, hv);
                         }
                         tc::fence_proxy_async_smem();
                     }
                     asm volatile("bar.sync 1, %0;" ::"r"(kScanWarps * 32) : "memory");
                     if (leader && ok) {
                         constexpr int scols = SPLIT ? 32 : 64;  // columns per box (fp32 / bf16)
-                        for (int cb = 0; cb < H / scols; ++cb)
-                            tc::tma_store_2d(&tm_cs, stg + cb * 8192, cb * scols, (int)(row0 + 64 * half));
+                        for (int hf = (npass == 1 ? 0 : pass); hf < (npass == 1 ? nhalf : pass + 1); ++hf)
+                            for (int cb = 0; cb < H / scols; ++cb)
+                                tc::tma_store_2d(&tm_cs, stg + (npass == 1 ? hf : 0) * tile_bytes + cb * 8192,
+                                                 cb * scols, (int)(row0 + 64 * hf));
                         tc::bulk_commit();
-                        tc::bulk_wait_read_all();  // the tile may be refilled
                     }
-                    asm volatile("bar.sync 1, %0;" ::"r"(kScanWarps * 32) : "memory");
                 }
-                tc::tmem_wait_st();
-                tc::tc_fence_before();
-                __syncwarp();
-                if (ok && lane == 0) tc::mbar_arrive(&bars[kBarUFree + ub]);
             }
             if (leader) tc::bulk_wait_all();
             // the end state: a summary's into its segment slot, the last
@@ -485,7 +497,7 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll 1
                 for (int m = 0; m < H / 16; ++m) {
                     uint32_t hv[16];
-                    tc::tmem_ld16(tm_h + lane_base + 16 * m, hv);
+                    tc::tmem_ld16(tm_h + (nchl & 1) * H + lane_base + 16 * m, hv);  // h after the last chunk
                     float4* d4 = reinterpret_cast<float4*>(h_out + s * H + 16 * m);
 #pragma unroll
                     for (int s4 = 0; s4 < 4; ++s4)
@@ -557,7 +569,7 @@ __global__ void __launch_bounds__(256) k_state_carry(const float* __restrict__ G
 // with a ring of 64-token sub-blocks.
 bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2, bool split = false) {
     const int H = (int)g.headdim;
-    p.tmem_cols = (3 * H <= 256) ? 256 : 512;
+    p.tmem_cols = (4 * H <= 256) ? 256 : 512;  // U x 2, h x 2
     const bool two = p.tmem_cols == 256 && ctas_per_sm_cap >= 2 && !split;
     const int kKb = (!two && g.chunk >= 128 && !split) ? 128 : 64;
     const uint32_t planes = split ? 2 : 1;
@@ -572,8 +584,13 @@ bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2, bool split = fa
     p.stage_bytes = p.off_w_in_stage + ((2 * kKb + 1) * 4 + 1023) / 1024 * 1024;
     const uint32_t budget = two ? (kSmemLimit / 2 - 2048) : kSmemLimit;
     const uint32_t fixed = kNumBars * 8 + 64 + 1024;
-    // 64 rows x H: bf16 (boxes of 64 columns), or fp32 (split; boxes of 32)
-    const uint32_t stg_bytes = planes * (uint32_t)(H / 64) * 8192;
+    // Staging tiles of 64 rows x H: bf16 (boxes of 64 columns), or fp32
+    // (split; boxes of 32).  A tile per 64-row half (the two halves of a
+    // chunk leave at once), except at two CTAs per SM with more than two
+    // sub-blocks per chunk, where one tile keeps a ring stage more (each
+    // measured faster where it is used).
+    p.stg_tiles = (g.dstate >= 128 && (!two || p.nsb <= 2)) ? 2 : 1;
+    const uint32_t stg_bytes = p.stg_tiles * planes * (uint32_t)(H / 64) * 8192;
     int nst = (int)((budget - fixed - stg_bytes) / p.stage_bytes);
     if (nst > kMaxStages) nst = kMaxStages;
     if (nst < 2) return false;
