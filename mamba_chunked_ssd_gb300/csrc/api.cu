@@ -158,10 +158,10 @@ bool fwd_f32_tensor_cores(const mamba2_shape& s) {
 // changes rounding only), and mamba2_ssd_fwd exposes neither G nor the chunk
 // states, so it runs the chunk measured fastest for the shape on GB300:
 //  - fp32 shapes the split-bf16 tensor-core kernels cover at chunk 128: 128;
-//  - bf16 tensor-core shapes: 256 for state 128 with head dim 128; 128 for
-//    state 64 or 256, and for state 128 with head dim 64 when the (batch,
-//    head) pairs outnumber the SMs; otherwise the caller's chunk (64 becomes
-//    128: chunks of 64 were never the fastest);
+//  - bf16 tensor-core shapes: 128, except with fewer than 16 (batch, head)
+//    pairs, where the state pass walks long sequence segments and the
+//    caller's chunk is kept (64 becomes 128: chunks of 64 were never the
+//    fastest);
 //  - everything else (the CUDA-core kernels): the caller's chunk.
 // MAMBA2_FWD_CHUNK=given keeps the caller's; =64, =128 or =256 forces one
 // (for tests and for timing the candidates on one shape).
@@ -177,13 +177,7 @@ int64_t fwd_chunk(const mamba2_shape& s) {
     const bool tc_h = s.headdim == 64 || s.headdim == 128;
     const bool tc_s = s.dstate == 64 || s.dstate == 128 || s.dstate == 256;
     if (!tc_h || !tc_s) return s.chunk_size;
-    int64_t want;
-    if (s.dstate == 128 && s.headdim == 128)
-        want = 256;
-    else if (s.dstate != 128 || s.batch * s.nheads > 152)
-        want = 128;
-    else
-        want = s.chunk_size == 64 ? 128 : s.chunk_size;
+    const int64_t want = (s.batch * s.nheads >= 16 || s.chunk_size == 64) ? 128 : s.chunk_size;
     t.chunk_size = want;
     const Geom g = make_geom(t);
     return (chunk_out_tc_fits(g) && state_pass_tc_fits(g)) ? want : s.chunk_size;

@@ -188,10 +188,10 @@ def test_workspace_size_fp32_tensor_core_path(lib, monkeypatch):
 
 def test_forward_pass_chunk_choice(lib, monkeypatch):
     """The forward pass's chunk (seen through the workspace's chunk-state
-    bytes): bf16 state 256 runs chunk 128 whatever the caller's chunk; state
-    128 with head dim 128 runs 256; state 128 with head dim 64 runs 128 when
-    the (batch, head) pairs outnumber the SMs and the caller's chunk
-    otherwise; MAMBA2_FWD_CHUNK forces one."""
+    bytes): bf16 tensor-core shapes run chunk 128 whatever the caller's chunk,
+    except with fewer than 16 (batch, head) pairs, which keep the caller's
+    (64 becomes 128); CUDA-core shapes keep the caller's; MAMBA2_FWD_CHUNK
+    forces one."""
     up = lambda v: (v + 255) // 256 * 256
 
     def ws(b, L, nh, H, S, T):
@@ -203,10 +203,10 @@ def test_forward_pass_chunk_choice(lib, monkeypatch):
         return up(b * nh * L * 4) + up(b * nh * nc * S * H * 2)
 
     assert ws(4, 4096, 64, 64, 256, 256) == expect(4, 4096, 64, 64, 256, 128)
-    assert ws(4, 4096, 64, 128, 128, 128) == expect(4, 4096, 64, 128, 128, 256)
-    assert ws(4, 4096, 64, 64, 128, 256) == expect(4, 4096, 64, 64, 128, 128)   # 256 pairs
-    assert ws(2, 4096, 64, 64, 128, 256) == expect(2, 4096, 64, 64, 128, 256)   # 128 pairs
-    assert ws(2, 4096, 64, 64, 128, 64) == expect(2, 4096, 64, 64, 128, 128)    # 64 -> 128
+    assert ws(4, 4096, 64, 128, 128, 256) == expect(4, 4096, 64, 128, 128, 128)
+    assert ws(2, 4096, 64, 64, 128, 64) == expect(2, 4096, 64, 64, 128, 128)
+    assert ws(1, 1024, 8, 64, 128, 256) == expect(1, 1024, 8, 64, 128, 256)     # 8 pairs
+    assert ws(1, 1024, 8, 64, 128, 64) == expect(1, 1024, 8, 64, 128, 128)      # 64 -> 128
     assert ws(4, 4096, 64, 16, 16, 32) == expect(4, 4096, 64, 16, 16, 32)       # CUDA cores
     monkeypatch.setenv("MAMBA2_FWD_CHUNK", "given")
     assert ws(4, 4096, 64, 64, 256, 256) == expect(4, 4096, 64, 64, 256, 256)
@@ -221,6 +221,8 @@ def test_forward_pass_chunk_size_query(lib, monkeypatch):
     s = _shape(batch=4, seqlen=4096, nheads=64, headdim=64, dstate=256, chunk_size=256, dtype_code=1)
     assert lib.mamba2_ssd_fwd_chunk_size(ctypes.byref(s)) == 128
     s = _shape(batch=4, seqlen=4096, nheads=64, headdim=128, dstate=128, chunk_size=64, dtype_code=1)
+    assert lib.mamba2_ssd_fwd_chunk_size(ctypes.byref(s)) == 128
+    s = _shape(batch=1, seqlen=4096, nheads=4, headdim=64, dstate=128, chunk_size=256, dtype_code=1)
     assert lib.mamba2_ssd_fwd_chunk_size(ctypes.byref(s)) == 256
     s = _shape(batch=1, seqlen=64, nheads=2, headdim=16, dstate=16, chunk_size=48, dtype_code=0)
     assert lib.mamba2_ssd_fwd_chunk_size(ctypes.byref(s)) == 48
