@@ -18,7 +18,10 @@ be checked against measurements:
       (batch, head) pairs are few.
   MAMBA2_FP32_PATH = simt               an fp32 forward pass on the CUDA
       cores instead of the split-bf16 tensor-core kernels (where they fit:
-      chunk 128, head dim 64 or 128, state 64 or 128).
+      head dim 64 or 128, state 64 or 128; run at chunk 128).
+  MAMBA2_FWD_CHUNK = given | 64 | 128 | 256   the chunk the forward pass
+      runs with: the caller's, or a fixed one (the result does not depend on
+      it; the default picks one per shape).
 
 Usage (one GPU):  python -m mamba_chunked_ssd_gb300.tune [--steps K] [--json]
 Each line: workload, candidate, mean stage time in microseconds (CUDA events
@@ -47,6 +50,7 @@ HEAD_SPLIT_ENV = "MAMBA2_CHUNK_OUT_HEAD_SPLIT"
 FWD_PATH_ENV = "MAMBA2_FWD_PATH"
 SEGMENTS_ENV = "MAMBA2_STATE_SEGMENTS"
 FP32_ENV = "MAMBA2_FP32_PATH"
+FWD_CHUNK_ENV = "MAMBA2_FWD_CHUNK"
 
 
 def _time(fn, steps, warmup, flush, stream):
@@ -235,6 +239,43 @@ def fp32_rows(workloads, steps=5, warmup=2):
     return rows
 
 
+def chunk_rows(workloads, steps=10, warmup=3):
+    """Whole-pass time (mamba2_ssd_fwd) with each chunk the forward pass can
+    run (64, 128, 256), and the one the default rule picks."""
+    import torch
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+
+    bd.load_library()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    rows = []
+    saved = os.environ.pop(FWD_CHUNK_ENV, None)
+    try:
+        for w in workloads:
+            d = make_inputs(w, device="cuda")
+            shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
+            default = bd.mamba2_ssd_fwd_chunk_size(shape)
+            y = torch.empty_like(d["x"])
+            times = {}
+            for cand in ("64", "128", "256"):
+                os.environ[FWD_CHUNK_ENV] = cand
+                ws = torch.empty(max(bd.mamba2_ssd_fwd_workspace_size(shape), 1), device="cuda", dtype=torch.uint8)
+                fn = lambda: bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size,  # noqa: E731
+                                               D=d["D"], initial_state=d["initial_state"], y=y, workspace=ws)
+                times[cand] = _time(fn, steps, warmup, flush, stream)
+                del ws
+            os.environ.pop(FWD_CHUNK_ENV, None)
+            bd.mamba2_check_device_status()
+            rows.append({"workload": w.name, "chunk_size": w.chunk_size, "default_chunk": default,
+                         **{f"chunk{k}_us": v for k, v in times.items()}})
+            del d, y
+    finally:
+        if saved is not None:
+            os.environ[FWD_CHUNK_ENV] = saved
+    return rows
+
+
 def profile_run(name, steps):
     """`steps` forward passes of one named workload, synchronised at the end."""
     import torch
@@ -271,14 +312,23 @@ def main():
     seg_ws = [WORKLOADS["blog_example"],
               Workload("few_heads_t256", 1, 32768, 4, 64, 128, 1, 256),
               Workload("few_heads_h128", 2, 16384, 4, 128, 128, 1, 128)]
+    chunks = chunk_rows([w for w in ws if w.dtype == "bf16"], steps=args.steps)
     rows = head_split_rows(ws, steps=args.steps)
     paths = fwd_path_rows(ws, steps=args.steps)
     segs = segment_rows(seg_ws, steps=args.steps)
     f32 = fp32_rows([WORKLOADS["long_seq_fp32_t128"],
                      Workload("fp32_h128_s64", 2, 4096, 16, 128, 64, 2, 128, dtype="fp32")])
     if args.json:
-        print(json.dumps({"head_split": rows, "fwd_path": paths, "segments": segs, "fp32": f32}))
+        print(json.dumps({"chunk": chunks, "head_split": rows, "fwd_path": paths, "segments": segs,
+                          "fp32": f32}))
         return
+    print("Whole forward pass at each chunk it can run:")
+    print("| workload (caller's chunk) | 64 (µs) | 128 (µs) | 256 (µs) | default |")
+    print("|---|---|---|---|---|")
+    for r in chunks:
+        print(f"| {r['workload']} ({r['chunk_size']}) | {r['chunk64_us']:.1f} | {r['chunk128_us']:.1f} | "
+              f"{r['chunk256_us']:.1f} | {r['default_chunk']} |")
+    print()
     print("Stage 3, heads of 128 columns:")
     print("| workload | whole heads (µs) | split heads (µs) | default (µs) |")
     print("|---|---|---|---|")
