@@ -72,9 +72,9 @@ struct StatePassArgs {
     int segments = 1;
     bool summary = false;
     float* seg_states = nullptr;
-    // fp32 on the tensor cores (chunk 128, one pass): x and B are bf16 hi/lo
-    // planes ([b, L, 2 nh, H], [b, L, 2 G, S]) and the chunk states are
-    // written as hi/lo planes [b, nh, nc, 2, S, H]; init and final stay fp32.
+    // fp32 on the tensor cores (chunk 128, one pass): x is fp32, B comes as
+    // bf16 hi/lo planes [b, L, 2 G, S], and the chunk states are written in
+    // fp32; init and final are fp32 as always.
     bool split = false;
 };
 

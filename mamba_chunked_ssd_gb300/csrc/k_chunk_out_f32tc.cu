@@ -203,8 +203,8 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     tc::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort;
-    const uint32_t x_tile = T * H * 2;            // one bf16 X plane of a virtual head (16 KB)
-    const uint32_t h_tile = (uint32_t)S * H * 2;  // one bf16 state plane
+    const uint32_t x_tile = T * H * 2;            // X_hi (or X_lo) of a virtual head, bf16 (16 KB)
+    const uint32_t h_tile = (uint32_t)S * H * 2;  // h_hi (or h_lo), bf16
 
     if (warp == 0) {
         // ================= TMA producer, G / dt / D gather, y stores =================

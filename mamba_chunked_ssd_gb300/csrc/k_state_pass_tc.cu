@@ -565,8 +565,9 @@ __global__ void __launch_bounds__(256) k_state_carry(const float* __restrict__ G
 // Ring plan.  Two CTAs share an SM when TMEM allows and the grid has enough
 // CTAs to use them; a grid of at most one CTA per SM (ctas_per_sm_cap = 1)
 // gets the whole shared memory, i.e. a deeper ring.
-// A split (fp32) problem's stages hold hi and lo planes: one CTA per SM
-// with a ring of 64-token sub-blocks.
+// A split (fp32) problem's stages hold B's hi and lo tiles and fp32 x (the
+// bytes of x's hi/lo pair): one CTA per SM with a ring of 64-token
+// sub-blocks.
 bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2, bool split = false) {
     const int H = (int)g.headdim;
     p.tmem_cols = (4 * H <= 256) ? 256 : 512;  // U x 2, h x 2
