@@ -46,8 +46,10 @@ constexpr int H = 64;                  // virtual head width (one MMA's N)
 constexpr int T = 128;                 // chunk (one 128-row block)
 
 // TMEM columns (512 allocated): CB fp32 [0, 128); P_hi [128, 192) and P_lo
-// [192, 256) (bf16 pairs, the A operand); Z [256, 320); Y2 [320, 384).
-constexpr uint32_t kColCB = 0, kColPhi = 128, kColPlo = 192, kColZ = 256, kColY2 = 320;
+// [192, 256) (bf16 pairs, the A operand); Z [256, 320); Y2 [320, 384); when
+// heads are split ahead, fp32 X of heads k even / odd for D x, [384, 448) /
+// [448, 512).
+constexpr uint32_t kColCB = 0, kColPhi = 128, kColPlo = 192, kColZ = 256, kColY2 = 320, kColX = 384;
 
 // Shared memory: C_hi | C_lo (128 x S bf16 each), then the stage ring; B_hi |
 // B_lo overlay the first stage slots until C B^T is done.  A stage holds
@@ -69,7 +71,8 @@ struct F32Params {
 enum : int {
     kBarCbFull = 0,
     kBarCbSplit,  // C and B split into hi/lo tiles
-    kBarSplit,    // the head's X and h_c split
+    kBarSplit,    // [2] head k's X and h_c split (barrier k % 2)
+    kBarSplit1,
     kBarCbDone,
     kBarPReady,
     kBarYDone,
@@ -150,7 +153,8 @@ __device__ __forceinline__ void split_tile(uint8_t* base, int rows, int cols, in
 // VS: virtual 64-wide heads per real head (1 or 2).  Every map is fp32 with
 // boxes of 32 columns: tm_x, tm_y [b, L, nh, H_real]; tm_b, tm_c
 // [b, L, G, S]; tm_h the chunk states, rows [b, nh, nc, S] x H_real.
-template <int VS>
+// AHEAD: split head k + 1 while head k's products run (three or more stages).
+template <int VS, bool AHEAD>
 __global__ void __launch_bounds__(kThreads, 1)
 k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                   const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_h,
@@ -183,6 +187,7 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         tc::mbar_init(&bars[kBarCbFull], 1);
         tc::mbar_init(&bars[kBarCbSplit], kEpiWarps);
         tc::mbar_init(&bars[kBarSplit], kEpiWarps);
+        tc::mbar_init(&bars[kBarSplit1], kEpiWarps);
         tc::mbar_init(&bars[kBarCbDone], 1);
         tc::mbar_init(&bars[kBarPReady], kEpiWarps);
         tc::mbar_init(&bars[kBarYDone], 1);
@@ -317,7 +322,7 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             uint64_t dstage = pst * stage_step;  // slot offset, in descriptor units
             for (int k = 0; ok && k < nvh; ++k) {
                 // the head's X and h_c are split (after their fill)
-                if (!tc::mbar_wait(&bars[kBarSplit], k & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarSplit + (k & 1)], (k >> 1) & 1, abort_flag)) { ok = false; break; }
                 if (k >= 1 && !tc::mbar_wait(&bars[kBarYFree], (k - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 const uint64_t dH = dH0 + dstage, dX = dX0 + dstage;
@@ -390,26 +395,30 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
         tc::tc_fence_after();
 
-        int st = 0;
-        uint32_t fill_phase = 0;
-        // Every warp runs every iteration and the named barrier in it, whatever
-        // its waits return; after a failed wait it only skips the work.
-        for (int k = 0; k < nvh; ++k) {
-            if (ok) ok = tc::mbar_wait(&bars[kBarFull + st], fill_phase, abort_flag);
-            uint8_t* sX = sStage + slot_of(st) * p.stage_bytes;
-            // X and h_c, loaded as fp32, become their hi/lo tiles.  X's piece
-            // of this thread (row il, columns [16 part, 16 part + 16)) is the
-            // one its output needs: it keeps the fp32 values for D x.
-            float xv[16];
+        // Head j's X and h_c, loaded as fp32, become their hi/lo tiles.  The
+        // thread's piece of X (row il, columns [16 part, 16 part + 16)) is
+        // the one its output needs: its fp32 values stay in xr for D x, and
+        // when heads are split ahead also go to tensor memory (xr is then
+        // reused for the next head).  With three or more stages head k + 1 is split while head k's
+        // products run, so the issuer finds it ready when it starts on head
+        // k + 1 (measured faster); with two, head k + 1's stage is refilled
+        // only after head k - 1's y has been stored, too late for that, and
+        // each head is split at the start of its own turn.  Every epilogue
+        // thread calls this, whatever its waits return; after a failed wait
+        // it only skips the work.
+        auto split_head = [&](int j, uint32_t (&xr)[16]) {
+            const int sj = j % p.nst;
+            if (ok) ok = tc::mbar_wait(&bars[kBarFull + sj], (uint32_t)((j / p.nst) & 1), abort_flag);
+            uint8_t* sXj = sStage + slot_of(sj) * p.stage_bytes;
             if (ok) {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 f = *reinterpret_cast<const float4*>(
-                        sX + (part >> 1) * (T * 128) + il * 128 + (((4 * (part & 1) + q4) ^ (il & 7)) << 4));
-                    xv[4 * q4] = f.x;
-                    xv[4 * q4 + 1] = f.y;
-                    xv[4 * q4 + 2] = f.z;
-                    xv[4 * q4 + 3] = f.w;
+                    const uint4 f = *reinterpret_cast<const uint4*>(
+                        sXj + (part >> 1) * (T * 128) + il * 128 + (((4 * (part & 1) + q4) ^ (il & 7)) << 4));
+                    xr[4 * q4] = f.x;
+                    xr[4 * q4 + 1] = f.y;
+                    xr[4 * q4 + 2] = f.z;
+                    xr[4 * q4 + 3] = f.w;
                 }
             }
             asm volatile("bar.sync 3, %0;" ::"r"(kEpiWarps * 32) : "memory");
@@ -419,14 +428,28 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     const uint32_t off = il * 128 + (((2 * part + h8) ^ (il & 7)) << 4);
                     uint32_t hi[4], lo[4];
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) split2(xv[8 * h8 + 2 * x], xv[8 * h8 + 2 * x + 1], hi[x], lo[x]);
-                    *reinterpret_cast<uint4*>(sX + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(sX + x_tile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    for (int x = 0; x < 4; ++x)
+                        split2(__uint_as_float(xr[8 * h8 + 2 * x]), __uint_as_float(xr[8 * h8 + 2 * x + 1]), hi[x],
+                               lo[x]);
+                    *reinterpret_cast<uint4*>(sXj + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(sXj + x_tile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                if (AHEAD) {
+                    tc::tmem_st16(tmem + kColX + 64 * (j & 1) + lane_base + 16 * part, xr);
+                    tc::tmem_wait_st();
                 }
             }
-            split_tile(sX + p.off_h, S, H, t, ok, 3);
+            split_tile(sXj + p.off_h, S, H, t, ok, 3);
             __syncwarp();
-            if (ok && lane == 0) tc::mbar_arrive(&bars[kBarSplit]);
+            if (ok && lane == 0) tc::mbar_arrive(&bars[kBarSplit + (j & 1)]);
+        };
+
+        uint32_t xr[16];  // this thread's fp32 piece of X
+        if (AHEAD) split_head(0, xr);
+        for (int k = 0; k < nvh; ++k) {
+            if (!AHEAD) split_head(k, xr);
+            const int st = k % p.nst;
+            uint8_t* sX = sStage + slot_of(st) * p.stage_bytes;
             float si = 0.f, ui = 0.f, dh = 0.f;
             if (ok) {
                 const float* vG = reinterpret_cast<const float*>(sX + p.off_vec);
@@ -488,9 +511,10 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 si = exp2f(grow);
                 ui = mild ? exp2f(grow - gref) : 1.f;
                 dh = vDt[T];
-                ok = tc::mbar_wait(&bars[kBarYDone], k & 1, abort_flag);
-                tc::tc_fence_after();
             }
+            if (AHEAD && k + 1 < nvh) split_head(k + 1, xr);
+            if (ok) ok = tc::mbar_wait(&bars[kBarYDone], k & 1, abort_flag);
+            tc::tc_fence_after();
             // ---- y = exp2(G_i) Z + u_i Y2 + D x_i, fp32, 16 columns [16 part, 16 part + 16)
             float yv[16];
             if (ok) {
@@ -500,15 +524,17 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     tc::tmem_ld8_nowait(tmem + kColZ + lane_base + 16 * part + 8 * u, za[u]);
                     tc::tmem_ld8_nowait(tmem + kColY2 + lane_base + 16 * part + 8 * u, yb[u]);
                 }
+                if (AHEAD) tc::tmem_ld16_nowait(tmem + kColX + 64 * (k & 1) + lane_base + 16 * part, xr);
                 tc::tmem_wait_ld8(za[0]);
                 tc::tmem_tie8(yb[0]);
                 tc::tmem_tie8(za[1]);
                 tc::tmem_tie8(yb[1]);
+                tc::tmem_tie16(xr);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
 #pragma unroll
                     for (int x = 0; x < 4; ++x) {
-                        const float x0 = xv[8 * u + 2 * x], x1 = xv[8 * u + 2 * x + 1];
+                        const float x0 = __uint_as_float(xr[8 * u + 2 * x]), x1 = __uint_as_float(xr[8 * u + 2 * x + 1]);
                         yv[8 * u + 2 * x] = fmaf(si, __uint_as_float(za[u][2 * x]),
                                                  fmaf(ui, __uint_as_float(yb[u][2 * x]), dh * x0));
                         yv[8 * u + 2 * x + 1] = fmaf(si, __uint_as_float(za[u][2 * x + 1]),
@@ -516,7 +542,8 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     }
                 }
             }
-            // every x of the stage has been read before any y is written over it
+            // every warp has read its Z, Y2 and X before any y is written over
+            // the stage's X tiles
             asm volatile("bar.sync 2, %0;" ::"r"(kEpiWarps * 32) : "memory");
             if (ok) {
                 // fp32 y tile: box part / 2 (32 columns, 128 rows x 128 bytes),
@@ -536,10 +563,6 @@ k_chunk_out_f32tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             if (ok && lane == 0) {
                 tc::mbar_arrive(&bars[kBarYFree]);
                 tc::mbar_arrive(&bars[kBarYReady + st]);
-            }
-            if (++st == p.nst) {
-                st = 0;
-                fill_phase ^= 1u;
             }
         }
         if (!ok) set_abort(ctl, p.status);
@@ -641,7 +664,8 @@ cudaError_t launch_chunk_out_f32tc(const Geom& g, const F32ChunkOutArgs& a, cuda
         const uint32_t box[4] = {32, 1, 128, 1};
         if (!make_tmap_f32(&tm_y, a.y, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    auto kern = (p.vs == 2) ? k_chunk_out_f32tc<2> : k_chunk_out_f32tc<1>;
+    auto kern = (p.vs == 2) ? (p.nst >= 3 ? k_chunk_out_f32tc<2, true> : k_chunk_out_f32tc<2, false>)
+                            : (p.nst >= 3 ? k_chunk_out_f32tc<1, true> : k_chunk_out_f32tc<1, false>);
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((int64_t)p.head_blocks * g.nchunks), (unsigned)g.batch);
