@@ -75,9 +75,14 @@ def test_forward_pass_chunk_override(w, chunk, monkeypatch):
     assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype]
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "mamba2_1p3b_layer", "long_seq_carried_state",
-                                  "large_state", "blog_example"])
-def test_named_workload_full_size(name):
+@pytest.mark.parametrize("name,chunk", [("tiny_fp32", None), ("mamba2_1p3b_layer", None),
+                                        ("long_seq_carried_state", None), ("large_state", None),
+                                        ("blog_example", None), ("long_seq_fp32_t128", None),
+                                        # the caller's chunk (256) rather than the pass's own
+                                        ("long_seq_carried_state", "given"), ("mamba2_1p3b_layer", "given")])
+def test_named_workload_full_size(name, chunk, monkeypatch):
+    if chunk:
+        monkeypatch.setenv("MAMBA2_FWD_CHUNK", chunk)
     w = WORKLOADS[name]
     inp = make_inputs(w)
     d = to_dev(inp)
