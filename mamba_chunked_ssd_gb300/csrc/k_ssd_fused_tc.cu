@@ -9,43 +9,47 @@
 // the same B, C group) and walks the sequence in blocks of 128 tokens, keeping
 // the fp32 state h of both heads in tensor memory.  A chunk of T = 128 is one
 // block; a chunk of T = 256 is two, and the second block reads the first one's
-// contribution through the state at the block boundary, an exact regrouping of
-// the chunk's output formula:
-//   y_i = exp2(G_i - G_s) C_i^T h_blk + sum_{j in block, j <= i} (C_i . B_j) exp2(G_i - G_j) dt_j x_j + D x_i
-//   h_next = exp2(G_l - G_s) h_blk + sum_{j in block} exp2(G_l - G_j) dt_j B_j x_j^T
-// where G is stage 1's chunk-local cumsum (log2 units), G_s its value just
-// before the block (0 at a chunk start) and G_l its value at the block's last
-// token.  Per block, with the pair's two heads a and b side by side as N:
-//   CB  = C B^T                        tcgen05, 128 x 128, K = state
-//   Z   = C [h_a | h_b]                tcgen05, N = 128; h in bf16 from the scan
-//   Z  <- f_i Z                        epilogue warps, in TMEM
-//   P   = CB . w (causal)              P warps, to TMEM as bf16, per head
-//   Y   = Z + P X                      tcgen05 accumulating onto Z, A from TMEM
-//   y   = u_i Y + D x                  epilogue
-//   h  <- exp2(G_l - G_s) h + B^T [w_a . X_a | w_b . X_b]    scan, then tcgen05
-// The decay of each P row is split at the column r before its 32-row quadrant:
-// exp2(G_i - G_j) dt_j = u_i w_j, u_i = exp2(G_i - G_r) <= 1, w_j =
-// exp2(G_r - G_j) dt_j, and exp2(G_i - G_s) = u_i exp2(G_r - G_s); so for such
-// rows f_i = exp2(G_r - G_s) <= 1 and u_i Y = exp2(G_i - G_s) Z + (exact P) X.
-// Rows whose u_i would fall below 2^-96 take exp2(G_i - G_j) dt_j per entry,
-// f_i = exp2(G_i - G_s) and u_i = 1.  With Z rescaled in place the output needs
-// one accumulator, so the C B^T product of the next block can start as soon as
-// this block's P warps have read CB.  Roles (30 warps):
-//   warp 0      X producer: TMA of both heads' X block into a double buffer;
-//               its lanes gather G, dt, D and G_s of both heads by cp.async;
-//               before refilling a buffer it stores the y the epilogue wrote
-//               over that buffer's X (TMA store)
-//   warp 1      TMEM allocator; issues CB and the TMA loads of C (one buffer)
-//               and B (two buffers)
-//   warp 2      issues Z and the state update (the state chain)
-//   warp 3      issues P X of head a, then of head b
-//   warps 4-19  P formation: (head, column half, TMEM lane quadrant); the
-//               first half covers column groups 0-1, the second groups 2-3
-//   warps 20-23 epilogue: Z rescaling, then y written over X in shared memory
-//   warps 24-27 scan, then fold: h -> bf16 tile for Z and h <- exp2(G_l - G_s) h
-//               in TMEM; once Z has read that tile, w . X into the same buffer
-// Tensor memory (512 columns): CB fp32 [0,128), Z / Y [128,256) (head a |
-// head b), P' bf16 [256,384), h fp32 [384,512).  Every wait is bounded; a
+// contribution through the state at the block boundary (an exact regrouping
+// of the chunk's output formula).  With G stage 1's chunk-local cumsum (log2
+// units), G_s its value just before the block (0 at a chunk start) and G_l its
+// value at the block's last token, per head:
+//   y_i    = exp2(G_i - G_s) C_i^T h + sum_{j <= i} (C_i . B_j) exp2(G_i - G_j) dt_j x_j + D x_i
+//   h_next = exp2(G_l - G_s) h + sum_j exp2(G_l - G_j) dt_j B_j x_j^T
+//
+// Mild blocks (the head's decay over the block spans at most 2 * 96 log2
+// units, every block of the bench workloads) split every decay at the
+// block's middle value G_m = (G_s + G_l) / 2:
+//   exp2(G_i - G_j) dt_j = u_i w_j,  u_i = exp2(G_i - G_m),  w_j = exp2(G_m - G_j) dt_j,
+// so with f = exp2(G_m - G_s) and d = exp2(G_l - G_m) (both <= 1), and every
+// factor between 2^-96 and 2^96:
+//   Y      = C (f h) + (C B^T . M) (w . X)         y_i = u_i Y_i + D x_i
+//   h_next = d (f h + B^T (w . X))
+// The masked C B^T (M the causal mask) carries no per-head factor, so one
+// bf16 copy of it serves both heads, and one w . X tile serves both the
+// output product and the state update.  Strong blocks (a larger span) take
+// exact per-entry weights instead: P = C B^T . exp2(G_i - G_j) dt_j . M per
+// head, Y = e . (C h) + P X with e_i = exp2(G_i - G_s) applied to C h in
+// tensor memory before P X accumulates onto it, and the state update with
+// w'_j = exp2(G_l - G_j) dt_j on h scaled by exp2(G_l - G_s).
+//
+// Per block (28 warps):
+//   warp 0       X producer: TMA of both heads' X block into a double buffer;
+//                its lanes gather G, dt, D and G_s of both heads by cp.async;
+//                before refilling a buffer it stores, by TMA, the y that the
+//                epilogue wrote over it
+//   warp 1       TMEM allocator; TMA loads of C (one buffer) and B (two);
+//                issues CB = C B^T
+//   warp 2       issues Z = C [z_a h_a | z_b h_b] and then P X onto it
+//   warp 3       issues the state update h += B^T [w_a . X_a | w_b . X_b]
+//   warps 4-7    one TMEM lane quadrant each: masked bf16 CB (and strong
+//                heads' P) into TMEM, then w . X in place over X
+//   warps 8-23   epilogue (lane quadrant, head, column half): rescales strong
+//                heads' Z, then y = u_i Y + D x over the buffer's X
+//   warps 24-27  scan (state rows): h <- d h, the bf16 tile z h for Z, and
+//                c h back into TMEM for the update (z = c = f for a mild
+//                block; z = 1, c = exp2(G_l - G_s) for a strong one)
+// Tensor memory (512 columns): CB fp32 [0,128), P slots bf16 [128,256),
+// Y [256,384) (head a | head b), h fp32 [384,512).  Every wait is bounded; a
 // timeout sets the status word and the CTA unwinds.
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -57,47 +61,51 @@ namespace {
 constexpr int kBlk = 128;  // tokens per block
 constexpr int kS = 128;    // state rows
 constexpr int kH = 64;     // head dim
+constexpr int kWarpFold0 = 4, kWarpEpi0 = 8, kWarpScan0 = 24;
 constexpr int kThreads = 28 * 32;
-constexpr int kWarpP0 = 4, kWarpEpi0 = 20, kWarpScan0 = 24;
 constexpr int kSmemLimit = 232448;
 
-constexpr uint32_t kColCB = 0, kColZ = 128, kColP = 256, kColH = 384;
+constexpr uint32_t kColCB = 0, kColP = 128, kColY = 256, kColH = 384;
+
+// Largest half-span (log2 units) of a mild block: every split factor stays
+// within 2^-96 .. 2^96.
+constexpr float kHalfSpan = 96.f;
 
 // Shared memory (offsets from the 1024-aligned base).  Tiles are 128-byte
 // swizzled boxes of 128 rows x 64 bf16 (16 KB).
 constexpr uint32_t kBox = 16384;
-constexpr uint32_t kOffC = 0;              // C block: states 0-63 | 64-127
-constexpr uint32_t kOffB = 2 * kBox;       // B double buffer: [2][states 0-63 | 64-127]
-constexpr uint32_t kOffX = 6 * kBox;       // X double buffer: [2][head a | head b]
-constexpr uint32_t kOffHW = 10 * kBox;     // h in bf16 (rows = states), then w . X (rows = tokens): head a | b
-constexpr uint32_t kOffVec = 12 * kBox;    // per X buffer: G[2][128], dt[2][128], misc[16]
+constexpr uint32_t kOffC = 0;            // C block: states 0-63 | 64-127
+constexpr uint32_t kOffB = 2 * kBox;     // B double buffer: [2][states 0-63 | 64-127]
+constexpr uint32_t kOffX = 6 * kBox;     // X double buffer: [2][head a | head b]; w . X, then y, in place
+constexpr uint32_t kOffT = 10 * kBox;    // bf16 z h for Z (rows = states): head a | head b
+constexpr uint32_t kOffVec = 12 * kBox;  // per X buffer: G[2][128], dt[2][128], misc[8]
 constexpr uint32_t kVecBytes = 2304;
-constexpr uint32_t kOffWv = kOffVec + 2 * kVecBytes;  // P warps' column weights [16][64]
-constexpr uint32_t kOffBar = kOffWv + 16 * 64 * 4;
+constexpr uint32_t kOffBar = kOffVec + 2 * kVecBytes;
 // misc: D_a, D_b, G_s of a, b
 constexpr int kMiscD = 0, kMiscGs = 2;
 
 enum : int {
     kBarCFull = 0,
-    kBarCFree,
+    kBarCFree,     // CB and Z have read C
     kBarCbDone,
+    kBarCbFree,    // the P warps have read CB
+    kBarPReady,
+    kBarTileReady, // the scan wrote the bf16 tile and prescaled h
     kBarZDone,
-    kBarZScaled,
-    kBarY2Done,
-    kBarEpiDone,
-    kBarHReady,
-    kBarWxReady,
+    kBarYDone,     // Z and P X of the block have completed
+    kBarYFree,     // the epilogue has read Y
     kBarUDone,
     kBarDrainA,
     kBarDrainB,
     kBarDrainC,
-    kBarCbRead,                 // the P warps have read CB
-    kBarPReady,                 // [2] per head
-    kBarBFull = kBarPReady + 2, // [2]
-    kBarBFree = kBarBFull + 2,  // [2]
-    kBarXFull = kBarBFree + 2,  // [2] X buffer filled (TMA + gathers)
-    kBarXRead = kBarXFull + 2,  // [2] the fold warps have read the buffer's X
-    kBarYReady = kBarXRead + 2, // [2] the epilogue has written y over the buffer's X
+    kBarZScaled,                       // [2] per head
+    kBarBFull = kBarZScaled + 2,       // [2]
+    kBarBFree = kBarBFull + 2,         // [2] CB and the update have read B
+    kBarXFull = kBarBFree + 2,         // [2] X buffer filled (TMA + gathers)
+    kBarFold1 = kBarXFull + 2,         // [2] mild heads' w . X written
+    kBarFold2 = kBarFold1 + 2,         // [2] every head's fold written
+    kBarXUsed = kBarFold2 + 2,         // [2] P X and the update have read the buffer
+    kBarYReady = kBarXUsed + 2,        // [2] the epilogue has written y over the buffer
     kNumBars = kBarYReady + 2
 };
 constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + ctl + alignment slack
@@ -109,6 +117,7 @@ struct FusedParams {
     const float* G;
     const float* D;
     const float* init;
+    const __nv_bfloat16* x;
     float* final_state;
     unsigned int* status;
 };
@@ -124,28 +133,69 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
     if (status) atomicExch(status, kStatusTimeout);
 }
 
-constexpr float kMildSpan = 96.f;
-constexpr float kWMax = 0x1p120f;
-
-__device__ __forceinline__ float exact_weight(float gi, float gj, float dtj) {
-    const float w = exp2f(fminf(gi - gj, kMildSpan)) * dtj;
-    return w > kWMax ? kWMax : w;
-}
-
 struct Vec {  // one X buffer's gathered per-token values
     float G[2][kBlk];
     float dt[2][kBlk];
-    float misc[16];
+    float misc[8];
 };
 static_assert(sizeof(Vec) <= kVecBytes, "per-buffer vector area too small");
 
-// Issues Y += P_hh X_hh for one head (A: P in TMEM; B: the head's X box,
-// MN-major); the accumulator already holds the rescaled Z.
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint64_t dXhead, int hh) {
-    const uint32_t id_y = tc::idesc_bf16(128, kH, false, true);
+// The block's split for head hh: mild, with the middle value G_m.  Every role
+// decides from the same shared-memory values with the same expression.
+struct Split {
+    bool mild;
+    float gs, gl, gm;
+};
+__device__ __forceinline__ Split block_split(const Vec* v, int hh) {
+    Split s;
+    s.gs = v->misc[kMiscGs + hh];
+    s.gl = v->G[hh][kBlk - 1];
+    s.mild = (s.gs - s.gl) <= 2.f * kHalfSpan;  // false for NaN
+    s.gm = 0.5f * (s.gs + s.gl);
+    return s;
+}
+
+// Multiplies the 8 bf16 of one 16-byte chunk by w (fp32 products, one
+// rounding to bf16 each).
+__device__ __forceinline__ uint4 scale_chunk(uint4 r, float w) {
+    const float2 w2 = make_float2(w, w);
+    uint32_t v[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int k16 = 0; k16 < kBlk / 16; ++k16)
-        tc::mma_bf16_ts(tmem + kColZ + hh * kH, tmem + kColP + hh * 64 + k16 * 8, dXhead + 128 * k16, id_y, 1u);
+    for (int e = 0; e < 4; ++e) {
+        const float2 p = tc::mul_f32x2(make_float2(tc::bf16_lo(v[e]), tc::bf16_hi(v[e])), w2);
+        v[e] = tc::pack_bf16x2(p.x, p.y);
+    }
+    return make_uint4(v[0], v[1], v[2], v[3]);
+}
+
+// A strong head's P for one 32-column group of one lane quadrant: the CB
+// entries times the exact weights exp2(G_i - G_j) dt_j, zero right of the
+// diagonal, into the head's own P slot.  Kept out of line: strong blocks are
+// rare, and the common path keeps its registers.
+__device__ __noinline__ void strong_p(uint32_t tmem, uint32_t lane_base, int gi, int q, int lane, const Vec* vec,
+                                      int sh) {
+    const int i = 32 * q + lane;
+    uint32_t r[2][16];
+    tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi, r[0]);
+    tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi + 16, r[1]);
+    tc::tmem_wait_ld16(r[0]);
+    tc::tmem_tie16(r[1]);
+    const float gi_ = vec->G[sh][i];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const int c0 = 32 * gi + 16 * hf;
+        uint32_t pk[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            const int j = c0 + 2 * x;
+            const float w0 = exp2f(gi_ - vec->G[sh][j]) * vec->dt[sh][j];
+            const float w1 = exp2f(gi_ - vec->G[sh][j + 1]) * vec->dt[sh][j + 1];
+            const float a0 = j <= i ? __uint_as_float(r[hf][2 * x]) * w0 : 0.f;
+            const float a1 = j + 1 <= i ? __uint_as_float(r[hf][2 * x + 1]) * w1 : 0.f;
+            pk[x] = tc::pack_bf16x2(a0, a1);
+        }
+        tc::tmem_st8(tmem + kColP + sh * 64 + lane_base + 16 * gi + 8 * hf, pk);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -168,26 +218,27 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&bars[kBarCFull], 1);
-        tc::mbar_init(&bars[kBarCFree], 2);     // after the CB and Z products
+        tc::mbar_init(&bars[kBarCFree], 2);
         tc::mbar_init(&bars[kBarCbDone], 1);
+        tc::mbar_init(&bars[kBarCbFree], 16);
+        tc::mbar_init(&bars[kBarPReady], 16);
+        tc::mbar_init(&bars[kBarTileReady], 4);
         tc::mbar_init(&bars[kBarZDone], 1);
-        tc::mbar_init(&bars[kBarZScaled], 4);
-        tc::mbar_init(&bars[kBarY2Done], 1);
-        tc::mbar_init(&bars[kBarEpiDone], 4);
-        tc::mbar_init(&bars[kBarHReady], 4);
-        tc::mbar_init(&bars[kBarWxReady], 4);
+        tc::mbar_init(&bars[kBarYDone], 1);
+        tc::mbar_init(&bars[kBarYFree], 16);
         tc::mbar_init(&bars[kBarUDone], 1);
         tc::mbar_init(&bars[kBarDrainA], 1);
         tc::mbar_init(&bars[kBarDrainB], 1);
         tc::mbar_init(&bars[kBarDrainC], 1);
-        tc::mbar_init(&bars[kBarCbRead], 16);
         for (int u = 0; u < 2; ++u) {
-            tc::mbar_init(&bars[kBarPReady + u], 8);
+            tc::mbar_init(&bars[kBarZScaled + u], 8);
             tc::mbar_init(&bars[kBarBFull + u], 1);
-            tc::mbar_init(&bars[kBarBFree + u], 2);  // after the CB product and the state update
+            tc::mbar_init(&bars[kBarBFree + u], 2);
             tc::mbar_init(&bars[kBarXFull + u], 1 + 32);  // expect-tx + one cp.async arrival per lane
-            tc::mbar_init(&bars[kBarXRead + u], 4);       // the fold warps
-            tc::mbar_init(&bars[kBarYReady + u], 4);      // the epilogue warps
+            tc::mbar_init(&bars[kBarFold1 + u], 4);
+            tc::mbar_init(&bars[kBarFold2 + u], 4);
+            tc::mbar_init(&bars[kBarXUsed + u], 2);
+            tc::mbar_init(&bars[kBarYReady + u], 16);
         }
         ctl->abort = 0;
         ctl->never = 0;
@@ -288,7 +339,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             if (fills1 > 0) (void)tc::mbar_wait(&bars[kBarXFull + 1], (fills1 - 1) & 1, never);
         }
     } else if (warp == 1) {
-        // ============== issuer of CB, and the C and B loads (TMA) ==============
+        // ============== C and B loads (TMA), issuer of CB = C B^T ==============
         if (lane == 0) {
             tc::tma_prefetch_desc(&tm_b);
             tc::tma_prefetch_desc(&tm_c);
@@ -308,10 +359,8 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tc::tma_load_4d(smem + kOffC + kb * kBox, &tm_c, &bars[kBarCFull], kb * 64, grp, k * kBlk, (int)b);
                 ++cfills;
             };
-            if (nblk > 0) {
-                load_b(0);
-                load_c(0);
-            }
+            load_b(0);
+            load_c(0);
             const uint32_t aC = tc::smem_u32(smem + kOffC), aB0 = tc::smem_u32(smem + kOffB);
             const uint32_t id_cb = tc::idesc_bf16(128, 128, false, false);
             for (int k = 0; ok && k < nblk; ++k) {
@@ -319,7 +368,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 if (!tc::mbar_wait(&bars[kBarCFull], k & 1, abort_flag)) { ok = false; break; }
                 if (!tc::mbar_wait(&bars[kBarBFull + u], v & 1, abort_flag)) { ok = false; break; }
                 // CB of block k - 1 has been read by every P warp
-                if (k >= 1 && !tc::mbar_wait(&bars[kBarCbRead], (k - 1) & 1, abort_flag)) { ok = false; break; }
+                if (k >= 1 && !tc::mbar_wait(&bars[kBarCbFree], (k - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 // CB = C B^T: both K-major over the state (two boxes of 64)
                 const uint32_t aB = aB0 + u * 2 * kBox;
@@ -333,13 +382,13 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc::mma_commit(&bars[kBarCFree]);
                 tc::mma_commit(&bars[kBarBFree + u]);
                 if (k + 1 < nblk) {
-                    // B of block k + 1 into the buffer block k - 1's CB and state update read
+                    // B of block k + 1 into the buffer that block k - 1's CB and update read
                     if (k >= 1 && !tc::mbar_wait(&bars[kBarBFree + (u ^ 1)], ((k - 1) >> 1) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     load_b(k + 1);
-                    // C of block k + 1 once block k's CB and Z products read it
+                    // C of block k + 1 once block k's CB and Z products have read it
                     if (!tc::mbar_wait(&bars[kBarCFree], k & 1, abort_flag)) { ok = false; break; }
                     load_c(k + 1);
                 }
@@ -353,290 +402,301 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             if (bfills1 > 0) (void)tc::mbar_wait(&bars[kBarBFull + 1], (bfills1 - 1) & 1, never);
             if (!ok) set_abort(ctl, p.status);
         }
-    } else if (warp == 3) {
-        // ============ issuer of P X onto the rescaled Z, head a then head b ============
-        if (lane == 0) {
-            bool ok = true;
-            const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffX), kBox, 1024);
-            for (int k = 0; ok && k < nblk; ++k) {
-                const int u = k & 1, v = k >> 1;
-                if (!tc::mbar_wait(&bars[kBarZScaled], k & 1, abort_flag)) { ok = false; break; }
-                if (!tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag)) { ok = false; break; }
-                for (int hh = 0; hh < 2 && ok; ++hh) {
-                    if (!tc::mbar_wait(&bars[kBarPReady + hh], k & 1, abort_flag)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    issue_pv(tmem, dX0 + (uint64_t)u * ((2 * kBox) >> 4) + (uint64_t)hh * (kBox >> 4), hh);
-                }
-                if (ok) tc::mma_commit(&bars[kBarY2Done]);
-            }
-            tc::mma_commit(&bars[kBarDrainC]);
-            (void)tc::mbar_wait(&bars[kBarDrainC], 0, never);
-            if (!ok) set_abort(ctl, p.status);
-        }
     } else if (warp == 2) {
-        // ============ issuer of the state chain: Z, state update ============
+        // ============ issuer of Z = C [z_a h_a | z_b h_b], then P X onto it ============
         if (lane == 0) {
             bool ok = true;
             const uint32_t aC = tc::smem_u32(smem + kOffC);
-            const uint32_t id_z = tc::idesc_bf16(128, 2 * kH, false, true);
-            const uint32_t id_u = tc::idesc_bf16(128, 2 * kH, true, true);
-            // B operands: h (rows = states = K) for Z, then w . X (rows = tokens =
-            // K) for the update, both in the shared buffer, MN-major with the two
-            // heads' boxes kBox apart; the update's A = B^T, MN-major: rows =
-            // tokens = K, the two 64-state boxes kBox apart
-            const uint64_t dHW = tc::sdesc_sw128(tc::smem_u32(smem + kOffHW), kBox, 1024);
-            const uint64_t dBt0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffB), kBox, 1024);
+            const uint32_t id_2 = tc::idesc_bf16(128, 2 * kH, false, true);  // both heads side by side
+            const uint32_t id_1 = tc::idesc_bf16(128, kH, false, true);      // one head
+            // B operands, MN-major (rows = K, 64 columns per row, the two heads'
+            // boxes kBox apart): the tile (K = state) and the X buffer (K = token)
+            const uint64_t dT = tc::sdesc_sw128(tc::smem_u32(smem + kOffT), kBox, 1024);
+            const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffX), kBox, 1024);
             for (int k = 0; ok && k < nblk; ++k) {
                 const int u = k & 1, v = k >> 1;
+                if (k >= 1 && !tc::mbar_wait(&bars[kBarYFree], (k - 1) & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarTileReady], k & 1, abort_flag)) { ok = false; break; }
                 if (!tc::mbar_wait(&bars[kBarCFull], k & 1, abort_flag)) { ok = false; break; }
-                if (!tc::mbar_wait(&bars[kBarHReady], k & 1, abort_flag)) { ok = false; break; }
-                if (k >= 1 && !tc::mbar_wait(&bars[kBarEpiDone], (k - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
-                // Z = C [h_a | h_b]   (K = state)
 #pragma unroll
                 for (int k16 = 0; k16 < kS / 16; ++k16)
-                    tc::mma_bf16_ss(tmem + kColZ,
-                                    tc::sdesc_sw128(aC + (k16 >> 2) * kBox + (k16 & 3) * 32, 16, 1024),
-                                    dHW + 128 * k16, id_z, k16 > 0);
+                    tc::mma_bf16_ss(tmem + kColY, tc::sdesc_sw128(aC + (k16 >> 2) * kBox + (k16 & 3) * 32, 16, 1024),
+                                    dT + 128 * k16, id_2, k16 > 0);
                 tc::mma_commit(&bars[kBarZDone]);
                 tc::mma_commit(&bars[kBarCFree]);
-                // h += B^T [w_a . X_a | w_b . X_b]   (K = token; h already scaled by the scan)
-                if (!tc::mbar_wait(&bars[kBarBFull + u], v & 1, abort_flag)) { ok = false; break; }
-                if (!tc::mbar_wait(&bars[kBarWxReady], k & 1, abort_flag)) { ok = false; break; }
+                // P X: the P slots, the mild heads' w . X and the strong heads' rescaled Z
+                if (!tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag)) { ok = false; break; }
+                const Vec* vec = vecs + u;
+                const bool mild0 = block_split(vec, 0).mild, mild1 = block_split(vec, 1).mild;
+                if (!tc::mbar_wait(&bars[kBarPReady], k & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarFold1 + u], v & 1, abort_flag)) { ok = false; break; }
+                if (!mild0 && !tc::mbar_wait(&bars[kBarZScaled + 0], k & 1, abort_flag)) { ok = false; break; }
+                if (!mild1 && !tc::mbar_wait(&bars[kBarZScaled + 1], k & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
-                const uint64_t dBt = dBt0 + (uint64_t)u * ((2 * kBox) >> 4);
+                const uint64_t dX = dX0 + (uint64_t)u * ((2 * kBox) >> 4);
+                if (mild0 && mild1) {
+                    // one product for both heads: the shared masked CB times [w_a X_a | w_b X_b]
 #pragma unroll
-                for (int k16 = 0; k16 < kBlk / 16; ++k16)
-                    tc::mma_bf16_ss(tmem + kColH, dBt + 128 * k16, dHW + 128 * k16, id_u, 1u);
-                tc::mma_commit(&bars[kBarUDone]);
-                tc::mma_commit(&bars[kBarBFree + u]);
+                    for (int k16 = 0; k16 < kBlk / 16; ++k16)
+                        tc::mma_bf16_ts(tmem + kColY, tmem + kColP + k16 * 8, dX + 128 * k16, id_2, 1u);
+                } else {
+                    // slot of the shared masked CB: the one head a's P does not take
+                    const uint32_t p0 = mild0 ? 0u : 1u;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t slot = (hh == 0 ? mild0 : mild1) ? p0 : (uint32_t)hh;
+                        const uint64_t dXh = dX + (uint64_t)hh * (kBox >> 4);
+#pragma unroll
+                        for (int k16 = 0; k16 < kBlk / 16; ++k16)
+                            tc::mma_bf16_ts(tmem + kColY + hh * kH, tmem + kColP + slot * 64 + k16 * 8,
+                                            dXh + 128 * k16, id_1, 1u);
+                    }
+                }
+                tc::mma_commit(&bars[kBarYDone]);
+                tc::mma_commit(&bars[kBarXUsed + u]);
             }
             tc::mma_commit(&bars[kBarDrainB]);
             (void)tc::mbar_wait(&bars[kBarDrainB], 0, never);
             if (!ok) set_abort(ctl, p.status);
         }
-    } else if (warp < kWarpEpi0) {
-        // ======== P formation (warps 4-19: head, column half, lane quadrant) ========
-        const int q = warp & 3;
-        const int role = (warp - kWarpP0) >> 2;  // 0..3
-        const int hh = role & 1, part = role >> 1;
-        const int i = 32 * q + lane;  // row of the block = TMEM lane
-        const int g_lo = 2 * part, g_hi = imin64(2 * part + 1, q);  // column groups with entries
-        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        const uint32_t tp = tmem + kColP + hh * 64 + lane_base;
-        float* wv = reinterpret_cast<float*>(smem + kOffWv) + (warp - kWarpP0) * 64;  // w of groups g_lo, g_lo + 1
-        bool ok = true;
-        for (int k = 0; k < nblk; ++k) {
-            const int u = k & 1, v = k >> 1;
-            if (ok) ok = tc::mbar_wait(&bars[kBarCbDone], k & 1, abort_flag);
-            if (ok) ok = tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag);
-            if (ok && k >= 1) ok = tc::mbar_wait(&bars[kBarY2Done], (k - 1) & 1, abort_flag);  // P free
-            if (!ok) break;
-            tc::tc_fence_after();
-            const Vec* vec = vecs + u;
-            const float grow = vec->G[hh][i];
-            const float gref = q == 0 ? vec->misc[kMiscGs + hh] : vec->G[hh][32 * q - 1];
-            const bool mild = gref - grow <= kMildSpan;  // false for NaN
-            const bool all_mild = __all_sync(0xffffffffu, mild);
-            for (int gi = g_lo; gi <= g_hi; ++gi) {
-                const int j = 32 * gi + lane;
-                const float wj = exp2f(fminf(gref - vec->G[hh][j], kMildSpan)) * vec->dt[hh][j];
-                wv[32 * (gi - g_lo) + lane] = wj > kWMax ? kWMax : wj;
+    } else if (warp == 3) {
+        // ============ issuer of the state update h += B^T [fold_a | fold_b] ============
+        if (lane == 0) {
+            bool ok = true;
+            const uint32_t id_u = tc::idesc_bf16(128, 2 * kH, true, true);
+            // A = B^T, MN-major: rows = tokens = K, the two 64-state boxes kBox
+            // apart; B = the folded X buffer, MN-major as for P X
+            const uint64_t dBt0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffB), kBox, 1024);
+            const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffX), kBox, 1024);
+            for (int k = 0; ok && k < nblk; ++k) {
+                const int u = k & 1, v = k >> 1;
+                if (!tc::mbar_wait(&bars[kBarTileReady], k & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarFold2 + u], v & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarBFull + u], v & 1, abort_flag)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint64_t dBt = dBt0 + (uint64_t)u * ((2 * kBox) >> 4);
+                const uint64_t dX = dX0 + (uint64_t)u * ((2 * kBox) >> 4);
+#pragma unroll
+                for (int k16 = 0; k16 < kBlk / 16; ++k16)
+                    tc::mma_bf16_ss(tmem + kColH, dBt + 128 * k16, dX + 128 * k16, id_u, 1u);
+                tc::mma_commit(&bars[kBarUDone]);
+                tc::mma_commit(&bars[kBarBFree + u]);
+                tc::mma_commit(&bars[kBarXUsed + u]);
             }
-            __syncwarp();
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int gi = g_lo + t;
-                if (gi > g_hi) {
-                    uint32_t z[8];
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) z[x] = 0u;
-                    tc::tmem_st8(tp + 16 * gi, z);
-                    tc::tmem_st8(tp + 16 * gi + 8, z);
-                    continue;
-                }
-                uint32_t r[2][16];
-                tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi, r[0]);
-                tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi + 16, r[1]);
-                tc::tmem_wait_ld16(r[0]);
-                tc::tmem_tie16(r[1]);
-                if (gi == g_hi) {
-                    // this warp's last read of CB: the next block's CB may be written
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&bars[kBarCbRead]);
-                }
-                if (gi == q) {  // causal mask inside the diagonal 32 x 32 group
-#pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        if (x > lane) r[0][x] = 0u;
-                        if (16 + x > lane) r[1][x] = 0u;
-                    }
-                }
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int col = 32 * gi + 16 * half;
-                    const float* w = wv + 32 * t + 16 * half;
-                    const uint32_t* rr = r[half];
-                    uint32_t pk[8];
-                    if (all_mild) {
-#pragma unroll
-                        for (int e4 = 0; e4 < 4; ++e4) {
-                            const float4 v4 = *reinterpret_cast<const float4*>(w + 4 * e4);
-                            const int o = 4 * e4;
-                            const float2 p0 = tc::mul_f32x2(
-                                make_float2(__uint_as_float(rr[o]), __uint_as_float(rr[o + 1])), make_float2(v4.x, v4.y));
-                            const float2 p1 = tc::mul_f32x2(
-                                make_float2(__uint_as_float(rr[o + 2]), __uint_as_float(rr[o + 3])), make_float2(v4.z, v4.w));
-                            pk[2 * e4] = tc::pack_bf16x2(p0.x, p0.y);
-                            pk[2 * e4 + 1] = tc::pack_bf16x2(p1.x, p1.y);
-                        }
-                    } else {
-                        // per row: the split weight (mild rows, the same products
-                        // as above) or the direct one
-                        const float* gj = &vec->G[hh][col];
-                        const float* dj = &vec->dt[hh][col];
-#pragma unroll
-                        for (int e4 = 0; e4 < 4; ++e4) {
-                            const float4 v4 = *reinterpret_cast<const float4*>(w + 4 * e4);
-                            const float4 g4 = *reinterpret_cast<const float4*>(gj + 4 * e4);
-                            const float4 d4 = *reinterpret_cast<const float4*>(dj + 4 * e4);
-                            const int o = 4 * e4;
-                            const float f0 = mild ? v4.x : exact_weight(grow, g4.x, d4.x);
-                            const float f1 = mild ? v4.y : exact_weight(grow, g4.y, d4.y);
-                            const float f2 = mild ? v4.z : exact_weight(grow, g4.z, d4.z);
-                            const float f3 = mild ? v4.w : exact_weight(grow, g4.w, d4.w);
-                            pk[2 * e4] = tc::pack_bf16x2(__uint_as_float(rr[o]) * f0, __uint_as_float(rr[o + 1]) * f1);
-                            pk[2 * e4 + 1] =
-                                tc::pack_bf16x2(__uint_as_float(rr[o + 2]) * f2, __uint_as_float(rr[o + 3]) * f3);
-                        }
-                    }
-                    tc::tmem_st8(tp + col / 2, pk);
-                }
-            }
-            if (g_hi < g_lo) {
-                // no column group of this warp has entries (second half, quadrants 0-1)
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&bars[kBarCbRead]);
-            }
-            tc::tmem_wait_st();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[kBarPReady + hh]);
+            tc::mma_commit(&bars[kBarDrainC]);
+            (void)tc::mbar_wait(&bars[kBarDrainC], 0, never);
+            if (!ok) set_abort(ctl, p.status);
         }
-        if (!ok) set_abort(ctl, p.status);
-    } else if (warp < kWarpScan0) {
-        // ========================= epilogue (warps 20-23) =========================
-        const int q = warp & 3;
-        const int i = 32 * q + lane;
-        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    } else if (warp < kWarpEpi0) {
+        // ============ fold (warps 4-7): w . X in place, token row i, both heads ============
+        // Mild heads first (P X reads them), then strong heads once P X has read
+        // their unscaled X.  Nothing else waits on these warps, so each block's
+        // fold runs as soon as its X lands.
+        const int i = 32 * (warp - kWarpFold0) + lane;
         bool ok = true;
         for (int k = 0; ok && k < nblk; ++k) {
             const int u = k & 1, v = k >> 1;
+            if (!(ok = tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag))) break;
             const Vec* vec = vecs + u;
-            // row factors of both heads: Z <- f_i Z now, y = u_i Y + D x later
-            float fz[2] = {0.f, 0.f}, fu[2] = {1.f, 1.f};
-            if (ok) ok = tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag);
-            if (ok) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const float grow = vec->G[hh][i];
-                    const float gs = vec->misc[kMiscGs + hh];
-                    const float gref = q == 0 ? gs : vec->G[hh][32 * q - 1];
-                    const bool mild = gref - grow <= kMildSpan;
-                    fz[hh] = mild ? exp2f(gref - gs) : exp2f(grow - gs);
-                    fu[hh] = mild ? exp2f(grow - gref) : 1.f;
-                }
-            }
-            if (ok) ok = tc::mbar_wait(&bars[kBarZDone], k & 1, abort_flag);
-            tc::tc_fence_after();
-            if (ok) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                    for (int m = 0; m < kH / 32; ++m) {
-                        uint32_t za[2][16];
-                        const uint32_t ta = tmem + kColZ + hh * kH + lane_base + 32 * m;
-                        tc::tmem_ld16_nowait(ta, za[0]);
-                        tc::tmem_ld16_nowait(ta + 16, za[1]);
-                        tc::tmem_wait_ld16(za[0]);
-                        tc::tmem_tie16(za[1]);
-#pragma unroll
-                        for (int t = 0; t < 2; ++t)
-#pragma unroll
-                            for (int x = 0; x < 16; ++x) za[t][x] = __float_as_uint(fz[hh] * __uint_as_float(za[t][x]));
-                        tc::tmem_st16(ta, za[0]);
-                        tc::tmem_st16(ta + 16, za[1]);
-                    }
-                }
-                tc::tmem_wait_st();
-            }
-            tc::tc_fence_before();
-            __syncwarp();
-            if (ok && lane == 0) tc::mbar_arrive(&bars[kBarZScaled]);
-            // ---- y = u_i Y + D x, written over x in the stage
-            if (ok) ok = tc::mbar_wait(&bars[kBarY2Done], k & 1, abort_flag);
-            if (ok) ok = tc::mbar_wait(&bars[kBarXRead + u], v & 1, abort_flag);  // y goes over X
-            tc::tc_fence_after();
+            const bool all_mild = block_split(vec, 0).mild && block_split(vec, 1).mild;
             uint8_t* sX = smem + kOffX + u * 2 * kBox;
-            if (ok) {
-#pragma unroll
+#pragma unroll 1
+            for (int pass = 0; pass < 2; ++pass) {
+                if (pass == 1 && !all_mild) {
+                    if (!(ok = tc::mbar_wait(&bars[kBarYDone], k & 1, abort_flag))) break;
+                }
+#pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
-                    const float dh = vec->misc[kMiscD + hh];
-                    const float2 d2 = make_float2(dh, dh), u2 = make_float2(fu[hh], fu[hh]);
-                    uint8_t* xrow = sX + hh * kBox + i * 128;
+                    const Split sp = block_split(vec, hh);
+                    if (sp.mild != (pass == 0)) continue;
+                    const float ref = sp.mild ? sp.gm : sp.gl;
+                    const float w = exp2f(ref - vec->G[hh][i]) * vec->dt[hh][i];
+                    uint8_t* row = sX + hh * kBox + i * 128;
+                    // every chunk of the row takes the same weight; visiting them in
+                    // swizzled order spreads a warp's accesses over the banks
 #pragma unroll
-                    for (int m = 0; m < kH / 32; ++m) {
-                        // 32 columns of Y and the four 16-byte x chunks under one wait
-                        uint32_t ya[4][8];
-                        uint4* px[4];
-                        uint4 xv[4];
+                    for (int c0 = 0; c0 < 8; c0 += 4) {
+                        uint4 a[4];
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const int kk = 32 * m + 8 * t;
-                            tc::tmem_ld8_nowait(tmem + kColZ + hh * kH + lane_base + kk, ya[t]);
-                            px[t] = reinterpret_cast<uint4*>(xrow + (((kk >> 3) ^ (i & 7)) << 4));
-                        }
+                        for (int c = 0; c < 4; ++c)
+                            a[c] = *reinterpret_cast<const uint4*>(row + ((((c0 + c) ^ i) & 7) << 4));
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) xv[t] = *px[t];
-                        tc::tmem_wait_ld8(ya[0]);
-                        tc::tmem_tie8(ya[1]);
-                        tc::tmem_tie8(ya[2]);
-                        tc::tmem_tie8(ya[3]);
-#pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const uint32_t xw[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
-                            uint32_t yw[4];
-#pragma unroll
-                            for (int x = 0; x < 4; ++x) {
-                                const float2 a2 = tc::fma_f32x2(
-                                    d2, make_float2(tc::bf16_lo(xw[x]), tc::bf16_hi(xw[x])),
-                                    tc::mul_f32x2(u2, make_float2(__uint_as_float(ya[t][2 * x]),
-                                                                  __uint_as_float(ya[t][2 * x + 1]))));
-                                yw[x] = tc::pack_bf16x2(a2.x, a2.y);
-                            }
-                            *px[t] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-                        }
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4*>(row + ((((c0 + c) ^ i) & 7) << 4)) = scale_chunk(a[c], w);
                     }
                 }
-            }
-            // Y has been read: Z of the next block may be written.  y is in
-            // shared memory for the X producer's TMA store.
-            tc::tc_fence_before();
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (ok && lane == 0) {
-                tc::mbar_arrive(&bars[kBarEpiDone]);
-                tc::mbar_arrive(&bars[kBarYReady + u]);
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[(pass == 0 ? kBarFold1 : kBarFold2) + u]);
             }
         }
         if (!ok) set_abort(ctl, p.status);
+    } else if (warp < kWarpScan0) {
+        // ====== epilogue and P formation (warps 8-23: quadrant q, slot e = 0..3) ======
+        // y: head e & 1, columns 32 (e >> 1) .. + 31 of the quadrant's rows.
+        // P of the next block: the quadrant's column group e (groups 0..q hold
+        // entries): the masked CB in bf16 into the shared slot, and strong
+        // heads' exact P into their own slots.
+        const int e = (warp - kWarpEpi0) >> 2;
+        const int q = warp & 3, hh = e & 1, half = e >> 1;
+        const int i = 32 * q + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const uint32_t ty = tmem + kColY + hh * kH + 32 * half + lane_base;
+        // the P slots' columns right of the diagonal (group e > q) stay zero;
+        // no warp ever writes them
+        if (e > q) {
+            uint32_t z[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) z[x] = 0u;
+#pragma unroll
+            for (int slot = 0; slot < 2; ++slot) {
+                tc::tmem_st8(tmem + kColP + slot * 64 + lane_base + 16 * e, z);
+                tc::tmem_st8(tmem + kColP + slot * 64 + lane_base + 16 * e + 8, z);
+            }
+            tc::tmem_wait_st();
+        }
+        // forms block kp's P tiles of this warp; false on a timeout
+        auto form_p = [&](int kp) -> bool {
+            const int up = kp & 1, vp = kp >> 1;
+            if (!tc::mbar_wait(&bars[kBarCbDone], kp & 1, abort_flag)) return false;
+            if (!tc::mbar_wait(&bars[kBarXFull + up], vp & 1, abort_flag)) return false;
+            tc::tc_fence_after();
+            const Vec* vec = vecs + up;
+            const bool m0 = block_split(vec, 0).mild, m1 = block_split(vec, 1).mild;
+            if (e <= q) {
+                const int gi = e;
+                // loads the group's 32 CB columns; entries right of the diagonal zeroed
+                auto load_cb = [&](uint32_t (&r)[2][16]) {
+                    tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi, r[0]);
+                    tc::tmem_ld16_nowait(tmem + kColCB + lane_base + 32 * gi + 16, r[1]);
+                    tc::tmem_wait_ld16(r[0]);
+                    tc::tmem_tie16(r[1]);
+                    if (gi == q) {  // causal mask inside the diagonal 32 x 32 group
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            if (x > lane) r[0][x] = 0u;
+                            if (16 + x > lane) r[1][x] = 0u;
+                        }
+                    }
+                };
+                if (m0 || m1) {
+                    const uint32_t p0 = m0 ? 0u : 1u;
+                    uint32_t r[2][16];
+                    load_cb(r);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            pk[x] = tc::pack_bf16x2(__uint_as_float(r[hf][2 * x]), __uint_as_float(r[hf][2 * x + 1]));
+                        tc::tmem_st8(tmem + kColP + p0 * 64 + lane_base + 16 * gi + 8 * hf, pk);
+                    }
+                }
+                if (!m0) strong_p(tmem, lane_base, gi, q, lane, vec, 0);
+                if (!m1) strong_p(tmem, lane_base, gi, q, lane, vec, 1);
+                // this warp's reads of CB are done: the next block's CB may be written
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[kBarCbFree]);
+                tc::tmem_wait_st();
+            } else {
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[kBarCbFree]);
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[kBarPReady]);
+            return true;
+        };
+        bool ok = form_p(0);
+        for (int k = 0; ok && k < nblk; ++k) {
+            const int u = k & 1, v = k >> 1;
+            const int64_t t = (int64_t)k * kBlk + i;
+            // x of this row (32 columns) for D x, from global memory: the X
+            // buffer holds w . X by the time y is formed
+            uint4 xv[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                           make_uint4(0, 0, 0, 0)};
+            if (t < g.seqlen) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    p.x + ((b * g.seqlen + t) * g.nheads + h0 + hh) * kH + 32 * half);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) xv[c] = __ldg(src + c);
+            }
+            if (!(ok = tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag))) break;
+            const Vec* vec = vecs + u;
+            const Split sp = block_split(vec, hh);
+            const float gi_ = vec->G[hh][i];
+            const float uf = sp.mild ? exp2f(gi_ - sp.gm) : 1.f;
+            const float dh = vec->misc[kMiscD + hh];
+            if (!sp.mild) {
+                // strong head: Z <- exp2(G_i - G_s) Z before P X accumulates onto it
+                if (!(ok = tc::mbar_wait(&bars[kBarZDone], k & 1, abort_flag))) break;
+                tc::tc_fence_after();
+                const float ez = exp2f(gi_ - sp.gs);
+                uint32_t r[2][16];
+                tc::tmem_ld16_nowait(ty, r[0]);
+                tc::tmem_ld16_nowait(ty + 16, r[1]);
+                tc::tmem_wait_ld16(r[0]);
+                tc::tmem_tie16(r[1]);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    r[0][x] = __float_as_uint(ez * __uint_as_float(r[0][x]));
+                    r[1][x] = __float_as_uint(ez * __uint_as_float(r[1][x]));
+                }
+                tc::tmem_st16(ty, r[0]);
+                tc::tmem_st16(ty + 16, r[1]);
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[kBarZScaled + hh]);
+            // ---- Y of the block: read it, release it, form y in registers
+            if (!(ok = tc::mbar_wait(&bars[kBarYDone], k & 1, abort_flag))) break;
+            tc::tc_fence_after();
+            uint4 yv[4];
+            {
+                uint32_t ya[2][16];
+                tc::tmem_ld16_nowait(ty, ya[0]);
+                tc::tmem_ld16_nowait(ty + 16, ya[1]);
+                tc::tmem_wait_ld16(ya[0]);
+                tc::tmem_tie16(ya[1]);
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[kBarYFree]);
+                const float2 d2 = make_float2(dh, dh), u2 = make_float2(uf, uf);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t xw[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+                    uint32_t yw[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int col = 8 * c + 2 * x;  // of this warp's 32
+                        const float2 a2 = tc::fma_f32x2(
+                            d2, make_float2(tc::bf16_lo(xw[x]), tc::bf16_hi(xw[x])),
+                            tc::mul_f32x2(u2, make_float2(__uint_as_float(ya[col >> 4][col & 15]),
+                                                          __uint_as_float(ya[col >> 4][(col & 15) + 1]))));
+                        yw[x] = tc::pack_bf16x2(a2.x, a2.y);
+                    }
+                    yv[c] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+                }
+            }
+            // the next block's P (its slots are free: P X of this block is done)
+            if (k + 1 < nblk && !(ok = form_p(k + 1))) break;
+            // y over the buffer once P X and the state update have read it
+            if (!(ok = tc::mbar_wait(&bars[kBarXUsed + u], v & 1, abort_flag))) break;
+            uint8_t* row = smem + kOffX + u * 2 * kBox + hh * kBox + i * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(row + (((4 * half + c) ^ (i & 7)) << 4)) = yv[c];
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[kBarYReady + u]);
+        }
+        if (!ok) set_abort(ctl, p.status);
     } else {
-        // ==================== scan, then fold (warps 16-19) ====================
+        // ==================== scan (warps 24-27: state rows) ====================
         const int q = warp & 3;
-        const int s = 32 * q + lane;       // scan: state row = TMEM lane
-        const int t = (warp - kWarpScan0) * 32 + lane;  // fold: token row of the block
+        const int s = 32 * q + lane;  // state row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         // h <- initial state (or zeros)
 #pragma unroll 1
@@ -657,80 +717,76 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             }
         }
         tc::tmem_wait_st();
+        float dprev0 = 1.f, dprev1 = 1.f;  // per head: h = dprev * (what TMEM holds)
         bool ok = true;
         for (int k = 0; k < nblk; ++k) {
             const int u = k & 1, v = k >> 1;
-            // ---- scan: h -> bf16 tile (rows = states), then h <- exp2(G_l - G_s) h
             if (ok && k >= 1) ok = tc::mbar_wait(&bars[kBarUDone], (k - 1) & 1, abort_flag);
+            if (ok && k >= 1) ok = tc::mbar_wait(&bars[kBarZDone], (k - 1) & 1, abort_flag);  // tile free
             if (ok) ok = tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag);
             if (!ok) break;
             tc::tc_fence_after();
             const Vec* vec = vecs + u;
-#pragma unroll 1
+            // per head: the tile gets z h, TMEM gets c h, with h = dprev * (TMEM)
+            // formed first (dprev and z or c may each be near 2^-96, so their
+            // product could leave the fp32 range)
+            float zf[2], cf[2], dn[2];
+#pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const float alpha = exp2f(vec->G[hh][kBlk - 1] - vec->misc[kMiscGs + hh]);
-                uint8_t* row = smem + kOffHW + hh * kBox + s * 128;
-#pragma unroll
-                for (int m = 0; m < kH / 16; ++m) {
-                    uint32_t hv[16];
-                    tc::tmem_ld16(tmem + kColH + hh * kH + lane_base + 16 * m, hv);
-#pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        const int e = 8 * c2, c = 2 * m + c2;  // 16-byte chunk of the row
-                        *reinterpret_cast<uint4*>(row + ((c ^ (s & 7)) << 4)) = make_uint4(
-                            tc::pack_bf16x2(__uint_as_float(hv[e]), __uint_as_float(hv[e + 1])),
-                            tc::pack_bf16x2(__uint_as_float(hv[e + 2]), __uint_as_float(hv[e + 3])),
-                            tc::pack_bf16x2(__uint_as_float(hv[e + 4]), __uint_as_float(hv[e + 5])),
-                            tc::pack_bf16x2(__uint_as_float(hv[e + 6]), __uint_as_float(hv[e + 7])));
-                    }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) hv[e] = __float_as_uint(alpha * __uint_as_float(hv[e]));
-                    tc::tmem_st16(tmem + kColH + hh * kH + lane_base + 16 * m, hv);
+                const Split sp = block_split(vec, hh);
+                if (sp.mild) {
+                    zf[hh] = cf[hh] = exp2f(sp.gm - sp.gs);
+                    dn[hh] = exp2f(sp.gl - sp.gm);
+                } else {
+                    zf[hh] = 1.f;
+                    cf[hh] = exp2f(sp.gl - sp.gs);
+                    dn[hh] = 1.f;
                 }
             }
+            const float dp[2] = {dprev0, dprev1};
+#pragma unroll 1
+            for (int ch = 0; ch < kH / 8; ++ch) {
+                // both heads' 8 columns (one 16-byte chunk of each tile row) under one wait
+                uint32_t hv[2][8];
+                tc::tmem_ld8_nowait(tmem + kColH + lane_base + 8 * ch, hv[0]);
+                tc::tmem_ld8_nowait(tmem + kColH + kH + lane_base + 8 * ch, hv[1]);
+                tc::tmem_wait_ld8(hv[0]);
+                tc::tmem_tie8(hv[1]);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const float2 d2 = make_float2(dp[hh], dp[hh]), z2 = make_float2(zf[hh], zf[hh]),
+                                 c2v = make_float2(cf[hh], cf[hh]);
+                    uint32_t tz[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const float2 t = tc::mul_f32x2(
+                            d2, make_float2(__uint_as_float(hv[hh][2 * x]), __uint_as_float(hv[hh][2 * x + 1])));
+                        const float2 tzv = tc::mul_f32x2(z2, t);
+                        const float2 tcv = tc::mul_f32x2(c2v, t);
+                        tz[x] = tc::pack_bf16x2(tzv.x, tzv.y);
+                        hv[hh][2 * x] = __float_as_uint(tcv.x);
+                        hv[hh][2 * x + 1] = __float_as_uint(tcv.y);
+                    }
+                    *reinterpret_cast<uint4*>(smem + kOffT + hh * kBox + s * 128 + ((ch ^ (s & 7)) << 4)) =
+                        make_uint4(tz[0], tz[1], tz[2], tz[3]);
+                    tc::tmem_st8(tmem + kColH + hh * kH + lane_base + 8 * ch, hv[hh]);
+                }
+            }
+            dprev0 = dn[0];
+            dprev1 = dn[1];
             tc::tmem_wait_st();
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[kBarHReady]);
-            // ---- fold: once Z has read the h tile, w . X into the same buffer
-            ok = tc::mbar_wait(&bars[kBarZDone], k & 1, abort_flag);
-            if (!ok) break;
-            const uint8_t* sX = smem + kOffX + u * 2 * kBox;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float w = vec->dt[hh][t] * exp2f(vec->G[hh][kBlk - 1] - vec->G[hh][t]);
-                const uint8_t* src = sX + hh * kBox + t * 128;
-                uint8_t* dst = smem + kOffHW + hh * kBox + t * 128;
-#pragma unroll
-                for (int c0 = 0; c0 < 8; c0 += 4) {
-                    uint4 a[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint4*>(src + (((c0 + c + t) & 7) << 4));
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 r = a[c];
-                        r.x = tc::pack_bf16x2(tc::bf16_lo(r.x) * w, tc::bf16_hi(r.x) * w);
-                        r.y = tc::pack_bf16x2(tc::bf16_lo(r.y) * w, tc::bf16_hi(r.y) * w);
-                        r.z = tc::pack_bf16x2(tc::bf16_lo(r.z) * w, tc::bf16_hi(r.z) * w);
-                        r.w = tc::pack_bf16x2(tc::bf16_lo(r.w) * w, tc::bf16_hi(r.w) * w);
-                        *reinterpret_cast<uint4*>(dst + (((c0 + c + t) & 7) << 4)) = r;
-                    }
-                }
-            }
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&bars[kBarWxReady]);
-                tc::mbar_arrive(&bars[kBarXRead + u]);
-            }
+            if (lane == 0) tc::mbar_arrive(&bars[kBarTileReady]);
         }
         // the last state update has landed: write the final state
-        if (ok && nblk > 0) ok = tc::mbar_wait(&bars[kBarUDone], (nblk - 1) & 1, abort_flag);
+        if (ok) ok = tc::mbar_wait(&bars[kBarUDone], (nblk - 1) & 1, abort_flag);
         if (ok && p.final_state) {
             tc::tc_fence_after();
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
+                const float dprev = hh ? dprev1 : dprev0;
                 float* dst = p.final_state + ((b * g.nheads + h0 + hh) * kS + s) * kH;
 #pragma unroll 1
                 for (int m = 0; m < kH / 16; ++m) {
@@ -739,8 +795,8 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
                     for (int e = 0; e < 16; e += 4)
                         *reinterpret_cast<float4*>(dst + 16 * m + e) =
-                            make_float4(__uint_as_float(hv[e]), __uint_as_float(hv[e + 1]),
-                                        __uint_as_float(hv[e + 2]), __uint_as_float(hv[e + 3]));
+                            make_float4(dprev * __uint_as_float(hv[e]), dprev * __uint_as_float(hv[e + 1]),
+                                        dprev * __uint_as_float(hv[e + 2]), dprev * __uint_as_float(hv[e + 3]));
                 }
             }
         }
@@ -777,6 +833,7 @@ cudaError_t launch_ssd_fused(const Geom& g, const FusedArgs& a, cudaStream_t st)
     p.G = a.G;
     p.D = a.D;
     p.init = a.init;
+    p.x = static_cast<const __nv_bfloat16*>(a.x);
     p.final_state = a.final_state;
     p.status = device_status_word();
     const uint64_t H = g.headdim, S = g.dstate, nh = g.nheads, L = g.seqlen, G = g.ngroups;
