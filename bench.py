@@ -143,6 +143,39 @@ def load_traffic(kernel, workload):
         return None
 
 
+def load_ncu_dram(kernel, workload):
+    """(duration in us, DRAM throughput in % of peak) of `kernel` from the
+    committed ncu summary of this workload, or None when there is none or the
+    kernel's source has changed since it was captured."""
+    if load_traffic(kernel, workload) is None:
+        return None
+    path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_{workload}.md")
+    dur = pct = None
+    try:
+        for line in open(path):
+            if line.startswith("|") and "`gpu__time_duration.sum`" in line:
+                dur = float(line.split("|")[2])
+            if line.startswith("|") and "`gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed`" in line:
+                pct = float(line.split("|")[2])
+    except Exception:
+        return None
+    return None if dur is None or pct is None else (dur, pct)
+
+
+def step_ncu_dram(kernels, workload):
+    """ncu's DRAM throughput over the pass, time-weighted across its kernels
+    (each kernel's own capture: serialised, cold L2), or None unless every
+    kernel has a summary of its current source."""
+    got = {k: load_ncu_dram(k, workload) for k in kernels}
+    if any(v is None for v in got.values()):
+        return None
+    total = sum(d for d, _ in got.values())
+    return {"dram_pct_of_peak_time_weighted": sum(d * p for d, p in got.values()) / total,
+            "per_kernel": {k: {"us": d, "dram_pct": p} for k, (d, p) in got.items()},
+            "source": f"profiles/ncu_<kernel>_{workload}.md (ncu gpu__dram_throughput, "
+                      "% of the hardware's peak)"}
+
+
 # ------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
@@ -563,6 +596,7 @@ def main():
         "roofline": {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": load_traffic(top, w.name), "algorithmic_bytes": kb[top]},
+        "step_ncu": step_ncu_dram(list(r["kernel_ms"]), w.name),
         "kernel_ms": r["kernel_ms"],
         "host_us_per_call": r["host_us"],
         "gpu_launches": 3 * args.steps,

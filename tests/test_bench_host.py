@@ -123,3 +123,31 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_step_ncu_dram_weights_the_committed_summaries(tmp_path, monkeypatch):
+    """The pass's ncu DRAM throughput is each kernel's figure weighted by its
+    captured duration, and no figure at all once any kernel's source has
+    changed since its capture."""
+    import hashlib
+    (tmp_path / "profiles").mkdir()
+    src_dir = tmp_path / "csrc"
+    src_dir.mkdir()
+    figures = {"a": (10.0, 20.0), "b": (30.0, 60.0)}
+    for k, (us, pct) in figures.items():
+        src = src_dir / f"{k}.cu"
+        src.write_text(f"// kernel {k}\n")
+        sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+        with open(tmp_path / "profiles" / f"ncu_{k}_wl.md", "w") as f:
+            f.write("# summary\n\n| counter | value | unit |\n|---|---|---|\n"
+                    f"| duration (`gpu__time_duration.sum`) | {us} | us |\n"
+                    f"| DRAM throughput (`gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed`) | {pct} | % |\n"
+                    "\ntraffic_bytes_per_launch: 1000\n"
+                    f"source: csrc/{k}.cu\nsource_sha256_16: {sha}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    r = bench.step_ncu_dram(["a", "b"], "wl")
+    assert r["dram_pct_of_peak_time_weighted"] == pytest.approx((10 * 20 + 30 * 60) / 40)
+    assert r["per_kernel"]["b"] == {"us": 30.0, "dram_pct": 60.0}
+    with open(src_dir / "b.cu", "a") as f:
+        f.write("// changed\n")
+    assert bench.step_ncu_dram(["a", "b"], "wl") is None
