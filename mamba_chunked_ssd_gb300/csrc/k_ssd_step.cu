@@ -41,6 +41,31 @@ __global__ void __launch_bounds__(kThreads) k_ssd_step(Geom g, const T* __restri
     const int64_t h = blockIdx.x, b = blockIdx.y;
     const int64_t grp = h / g.heads_per_group;
     const int tid = threadIdx.x;
+    const int cols = H / VEC;              // column groups per row
+    const int rows_per_pass = kThreads / cols;
+    const int c = tid % cols, r0 = tid / cols;
+    const bool active = r0 < rows_per_pass;  // threads beyond rows_per_pass * cols idle
+    const int64_t base = (b * g.nheads + h) * (int64_t)S * H;
+
+    // The state stream depends on nothing else: its first pass of loads is in
+    // flight before the small loads of dt, B, C and x below (each thread
+    // reads and later writes only its own elements, so an in-place update is
+    // safe).
+    using V = typename std::conditional<VEC == 4, float4, float>::type;
+    V hv[kUnroll];
+    auto load_pass = [&](int r) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int rr = r + u * rows_per_pass;
+            if (rr < S) {
+                if (state_in)
+                    hv[u] = *reinterpret_cast<const V*>(state_in + base + (int64_t)rr * H + c * VEC);
+                else
+                    hv[u] = V{};
+            }
+        }
+    };
+    if (active) load_pass(r0);
 
     const float dtv = dt[b * g.nheads + h];
     const float decay = exp2f(kLog2e * (A[h] * dtv));
@@ -54,12 +79,6 @@ __global__ void __launch_bounds__(kThreads) k_ssd_step(Geom g, const T* __restri
     for (int i = tid; i < H; i += kThreads) s_x[i] = to_f32(xr[i]);
     __syncthreads();
 
-    const int cols = H / VEC;              // column groups per row
-    const int rows_per_pass = kThreads / cols;
-    const int c = tid % cols, r0 = tid / cols;
-    const bool active = r0 < rows_per_pass;  // threads beyond rows_per_pass * cols idle
-    const int64_t base = (b * g.nheads + h) * (int64_t)S * H;
-
     float acc[VEC];
 #pragma unroll
     for (int k = 0; k < VEC; ++k) acc[k] = 0.f;
@@ -68,19 +87,7 @@ __global__ void __launch_bounds__(kThreads) k_ssd_step(Geom g, const T* __restri
     for (int k = 0; k < VEC; ++k) xv[k] = s_x[c * VEC + k];
 
     if (active) {
-        using V = typename std::conditional<VEC == 4, float4, float>::type;
         for (int r = r0; r < S; r += rows_per_pass * kUnroll) {
-            V hv[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int rr = r + u * rows_per_pass;
-                if (rr < S) {
-                    if (state_in)
-                        hv[u] = *reinterpret_cast<const V*>(state_in + base + (int64_t)rr * H + c * VEC);
-                    else
-                        hv[u] = V{};
-                }
-            }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int rr = r + u * rows_per_pass;
@@ -95,6 +102,7 @@ __global__ void __launch_bounds__(kThreads) k_ssd_step(Geom g, const T* __restri
                     *reinterpret_cast<V*>(state_out + base + (int64_t)rr * H + c * VEC) = hv[u];
                 }
             }
+            if (r + rows_per_pass * kUnroll < S) load_pass(r + rows_per_pass * kUnroll);
         }
     }
     // Partial sums, laid out [row-slab][column], then one thread per column adds
