@@ -368,24 +368,41 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const int64_t t0 = (int64_t)c * T;
                 return Gbh[t0 + imin64(T, g.seqlen - t0) - 1];
             };
-            // the entering state of a later segment comes from the carry kernel
-            tc::griddep_wait();
             // h <- initial state (segment 0), the segment's entering state
-            // (segment pass), or zeros
-            const float* h_in = nullptr;
-            if (seg == 0)
-                h_in = p.init ? p.init + bh * S * H : nullptr;
-            else if (p.mode == kSegmentPass)
-                h_in = p.seg_states + (bh * (p.nseg - 1) + seg - 1) * S * H;
+            // (segment pass), or zeros; 32 columns (eight 16-byte loads) per
+            // round.  The initial state is the caller's input, so its loads
+            // start before the wait for the previous kernel; the entering
+            // state of a later segment comes from the carry kernel.
+            auto load_h = [&](const float* h_in) {
 #pragma unroll 1
-            for (int m = 0; m < H / 16; ++m) {
-                uint32_t r[16];
+                for (int m = 0; m < H / 32; ++m) {
+                    float4 f[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    r[e] = __float_as_uint((valid && h_in) ? h_in[s * H + 16 * m + e] : 0.f);
-                tc::tmem_st16(tm_h + lane_base + 16 * m, r);
+                    for (int j = 0; j < 8; ++j)
+                        f[j] = (valid && h_in) ? *reinterpret_cast<const float4*>(h_in + s * H + 32 * m + 4 * j)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t r[16];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            r[4 * j] = __float_as_uint(f[4 * hf + j].x);
+                            r[4 * j + 1] = __float_as_uint(f[4 * hf + j].y);
+                            r[4 * j + 2] = __float_as_uint(f[4 * hf + j].z);
+                            r[4 * j + 3] = __float_as_uint(f[4 * hf + j].w);
+                        }
+                        tc::tmem_st16(tm_h + lane_base + 32 * m + 16 * hf, r);
+                    }
+                }
+                tc::tmem_wait_st();
+            };
+            if (seg == 0) {
+                load_h(p.init ? p.init + bh * S * H : nullptr);
+                tc::griddep_wait();
+            } else {
+                tc::griddep_wait();
+                load_h(p.mode == kSegmentPass ? p.seg_states + (bh * (p.nseg - 1) + seg - 1) * S * H : nullptr);
             }
-            tc::tmem_wait_st();
             // Per chunk: h_{c+1} = exp2(G_last) h_c + U_c into the other h
             // buffer (then U_c's buffer is released to the MMA), then h_c is
             // stored; G_last of the next chunk is fetched while this one waits
