@@ -33,11 +33,12 @@
 // w'_j = exp2(G_l - G_j) dt_j on h scaled by exp2(G_l - G_s).
 //
 // Per block (28 warps):
-//   warp 0       X producer: TMA of both heads' X block into a double buffer;
+//   warp 0       X producer: TMA of both heads' X block into a ring of three;
 //                its lanes gather G, dt, D and G_s of both heads by cp.async;
 //                before refilling a buffer it stores, by TMA, the y that the
 //                epilogue wrote over it
-//   warp 1       TMEM allocator; TMA loads of C (one buffer) and B (two);
+//   warp 1       TMEM allocator; TMA loads of C and B (one buffer each; the
+//                next block's B once this block's CB and update have read B);
 //                issues CB = C B^T
 //   warp 2       issues Z = C [z_a h_a | z_b h_b] and then P X onto it
 //   warp 3       issues the state update h += B^T [w_a . X_a | w_b . X_b]
@@ -72,15 +73,20 @@ constexpr uint32_t kColCB = 0, kColP = 128, kColY = 256, kColH = 384;
 constexpr float kHalfSpan = 96.f;
 
 // Shared memory (offsets from the 1024-aligned base).  Tiles are 128-byte
-// swizzled boxes of 128 rows x 64 bf16 (16 KB).
+// swizzled boxes of 128 rows x 64 bf16 (16 KB).  X rides a ring of three
+// buffers: a block's X lands, is folded, read by P X and the update, and
+// holds its y until the y store has read it, so two blocks in flight do not
+// cover that span (measured: three buffers and one B buffer beat two of
+// each).
+constexpr int kXBufs = 3;
 constexpr uint32_t kBox = 16384;
 constexpr uint32_t kOffC = 0;            // C block: states 0-63 | 64-127
-constexpr uint32_t kOffB = 2 * kBox;     // B double buffer: [2][states 0-63 | 64-127]
-constexpr uint32_t kOffX = 6 * kBox;     // X double buffer: [2][head a | head b]; w . X, then y, in place
+constexpr uint32_t kOffB = 2 * kBox;     // B block: states 0-63 | 64-127
+constexpr uint32_t kOffX = 4 * kBox;     // X ring: [3][head a | head b]; w . X, then y, in place
 constexpr uint32_t kOffT = 10 * kBox;    // bf16 z h for Z (rows = states): head a | head b
 constexpr uint32_t kOffVec = 12 * kBox;  // per X buffer: G[2][128], dt[2][128], misc[8]
 constexpr uint32_t kVecBytes = 2304;
-constexpr uint32_t kOffBar = kOffVec + 2 * kVecBytes;
+constexpr uint32_t kOffBar = kOffVec + kXBufs * kVecBytes;
 // misc: D_a, D_b, G_s of a, b
 constexpr int kMiscD = 0, kMiscGs = 2;
 
@@ -98,15 +104,15 @@ enum : int {
     kBarDrainA,
     kBarDrainB,
     kBarDrainC,
-    kBarZScaled,                       // [2] per head
-    kBarBFull = kBarZScaled + 2,       // [2]
-    kBarBFree = kBarBFull + 2,         // [2] CB and the update have read B
-    kBarXFull = kBarBFree + 2,         // [2] X buffer filled (TMA + gathers)
-    kBarFold1 = kBarXFull + 2,         // [2] mild heads' w . X written
-    kBarFold2 = kBarFold1 + 2,         // [2] every head's fold written
-    kBarXUsed = kBarFold2 + 2,         // [2] P X and the update have read the buffer
-    kBarYReady = kBarXUsed + 2,        // [2] the epilogue has written y over the buffer
-    kNumBars = kBarYReady + 2
+    kBarBFull,
+    kBarBFree,                              // CB and the update have read B
+    kBarZScaled,                            // [2] per head
+    kBarXFull = kBarZScaled + 2,            // [kXBufs] X buffer filled (TMA + gathers)
+    kBarFold1 = kBarXFull + kXBufs,         // [kXBufs] mild heads' w . X written
+    kBarFold2 = kBarFold1 + kXBufs,         // [kXBufs] every head's fold written
+    kBarXUsed = kBarFold2 + kXBufs,         // [kXBufs] P X and the update have read the buffer
+    kBarYReady = kBarXUsed + kXBufs,        // [kXBufs] the epilogue has written y over the buffer
+    kNumBars = kBarYReady + kXBufs
 };
 constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + ctl + alignment slack
 static_assert(kSmemBytes <= (uint32_t)kSmemLimit, "shared-memory plan too large");
@@ -230,10 +236,10 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         tc::mbar_init(&bars[kBarDrainA], 1);
         tc::mbar_init(&bars[kBarDrainB], 1);
         tc::mbar_init(&bars[kBarDrainC], 1);
-        for (int u = 0; u < 2; ++u) {
-            tc::mbar_init(&bars[kBarZScaled + u], 8);
-            tc::mbar_init(&bars[kBarBFull + u], 1);
-            tc::mbar_init(&bars[kBarBFree + u], 2);
+        tc::mbar_init(&bars[kBarBFull], 1);
+        tc::mbar_init(&bars[kBarBFree], 2);
+        for (int u = 0; u < 2; ++u) tc::mbar_init(&bars[kBarZScaled + u], 8);
+        for (int u = 0; u < kXBufs; ++u) {
             tc::mbar_init(&bars[kBarXFull + u], 1 + 32);  // expect-tx + one cp.async arrival per lane
             tc::mbar_init(&bars[kBarFold1 + u], 4);
             tc::mbar_init(&bars[kBarFold2 + u], 4);
@@ -263,18 +269,18 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         tc::griddep_wait();  // G comes from stage 1
         bool ok = true;
-        int fills0 = 0, fills1 = 0;  // fills issued per buffer
+        int fills[kXBufs] = {};  // fills issued per buffer
         for (int k = 0; ok && k < nblk; ++k) {
-            const int u = k & 1, v = k >> 1;
-            if (k >= 2) {
-                // y of block k - 2 sits over this buffer's X: store it, then refill
+            const int u = k % kXBufs, v = k / kXBufs;
+            if (k >= kXBufs) {
+                // y of block k - kXBufs sits over this buffer's X: store it, then refill
                 bool w_ok = true;
                 if (lane == 0) {
                     w_ok = tc::mbar_wait(&bars[kBarYReady + u], (v - 1) & 1, abort_flag);
                     if (w_ok) {
                         for (int hh = 0; hh < 2; ++hh)
                             tc::tma_store_4d(&tm_y, smem + kOffX + u * 2 * kBox + hh * kBox, 0, h0 + hh,
-                                             (k - 2) * kBlk, (int)b);
+                                             (k - kXBufs) * kBlk, (int)b);
                         tc::bulk_commit();
                         tc::bulk_wait_read_all();
                     }
@@ -316,12 +322,12 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc::cp_async4(&vec->misc[kMiscGs + hh], gs, pos ? 4u : 0u);
             }
             tc::cp_async_mbar_arrive_noinc(full);
-            if (u) ++fills1; else ++fills0;
+            ++fills[u];
         }
-        // the last (up to) two blocks' y
-        for (int k = nblk - 2 < 0 ? 0 : nblk - 2; ok && k < nblk; ++k) {
+        // the last (up to) kXBufs blocks' y
+        for (int k = nblk - kXBufs < 0 ? 0 : nblk - kXBufs; ok && k < nblk; ++k) {
             if (lane == 0) {
-                const int u = k & 1, v = k >> 1;
+                const int u = k % kXBufs, v = k / kXBufs;
                 ok = tc::mbar_wait(&bars[kBarYReady + u], v & 1, abort_flag);
                 if (ok) {
                     for (int hh = 0; hh < 2; ++hh)
@@ -335,8 +341,8 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // no copy of this warp may still be landing or reading when the CTA exits
         if (lane == 0) {
             tc::bulk_wait_all();
-            if (fills0 > 0) (void)tc::mbar_wait(&bars[kBarXFull + 0], (fills0 - 1) & 1, never);
-            if (fills1 > 0) (void)tc::mbar_wait(&bars[kBarXFull + 1], (fills1 - 1) & 1, never);
+            for (int u = 0; u < kXBufs; ++u)
+                if (fills[u] > 0) (void)tc::mbar_wait(&bars[kBarXFull + u], (fills[u] - 1) & 1, never);
         }
     } else if (warp == 1) {
         // ============== C and B loads (TMA), issuer of CB = C B^T ==============
@@ -344,14 +350,12 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::tma_prefetch_desc(&tm_b);
             tc::tma_prefetch_desc(&tm_c);
             bool ok = true;
-            int cfills = 0, bfills0 = 0, bfills1 = 0;
+            int cfills = 0, bfills = 0;
             auto load_b = [&](int k) {
-                const int u = k & 1;
-                tc::mbar_arrive_expect_tx(&bars[kBarBFull + u], 2 * kBox);
+                tc::mbar_arrive_expect_tx(&bars[kBarBFull], 2 * kBox);
                 for (int kb = 0; kb < 2; ++kb)
-                    tc::tma_load_4d(smem + kOffB + u * 2 * kBox + kb * kBox, &tm_b, &bars[kBarBFull + u], kb * 64,
-                                    grp, k * kBlk, (int)b);
-                if (u) ++bfills1; else ++bfills0;
+                    tc::tma_load_4d(smem + kOffB + kb * kBox, &tm_b, &bars[kBarBFull], kb * 64, grp, k * kBlk, (int)b);
+                ++bfills;
             };
             auto load_c = [&](int k) {
                 tc::mbar_arrive_expect_tx(&bars[kBarCFull], 2 * kBox);
@@ -361,17 +365,15 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             };
             load_b(0);
             load_c(0);
-            const uint32_t aC = tc::smem_u32(smem + kOffC), aB0 = tc::smem_u32(smem + kOffB);
+            const uint32_t aC = tc::smem_u32(smem + kOffC), aB = tc::smem_u32(smem + kOffB);
             const uint32_t id_cb = tc::idesc_bf16(128, 128, false, false);
             for (int k = 0; ok && k < nblk; ++k) {
-                const int u = k & 1, v = k >> 1;
                 if (!tc::mbar_wait(&bars[kBarCFull], k & 1, abort_flag)) { ok = false; break; }
-                if (!tc::mbar_wait(&bars[kBarBFull + u], v & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarBFull], k & 1, abort_flag)) { ok = false; break; }
                 // CB of block k - 1 has been read by every P warp
                 if (k >= 1 && !tc::mbar_wait(&bars[kBarCbFree], (k - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 // CB = C B^T: both K-major over the state (two boxes of 64)
-                const uint32_t aB = aB0 + u * 2 * kBox;
 #pragma unroll
                 for (int k16 = 0; k16 < kS / 16; ++k16) {
                     const uint32_t off = (k16 >> 2) * kBox + (k16 & 3) * 32;
@@ -380,13 +382,10 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 }
                 tc::mma_commit(&bars[kBarCbDone]);
                 tc::mma_commit(&bars[kBarCFree]);
-                tc::mma_commit(&bars[kBarBFree + u]);
+                tc::mma_commit(&bars[kBarBFree]);
                 if (k + 1 < nblk) {
-                    // B of block k + 1 into the buffer that block k - 1's CB and update read
-                    if (k >= 1 && !tc::mbar_wait(&bars[kBarBFree + (u ^ 1)], ((k - 1) >> 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    // B of block k + 1 once block k's CB and update have read B
+                    if (!tc::mbar_wait(&bars[kBarBFree], k & 1, abort_flag)) { ok = false; break; }
                     load_b(k + 1);
                     // C of block k + 1 once block k's CB and Z products have read it
                     if (!tc::mbar_wait(&bars[kBarCFree], k & 1, abort_flag)) { ok = false; break; }
@@ -398,8 +397,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::mma_commit(&bars[kBarDrainA]);
             (void)tc::mbar_wait(&bars[kBarDrainA], 0, never);
             if (cfills > 0) (void)tc::mbar_wait(&bars[kBarCFull], (cfills - 1) & 1, never);
-            if (bfills0 > 0) (void)tc::mbar_wait(&bars[kBarBFull + 0], (bfills0 - 1) & 1, never);
-            if (bfills1 > 0) (void)tc::mbar_wait(&bars[kBarBFull + 1], (bfills1 - 1) & 1, never);
+            if (bfills > 0) (void)tc::mbar_wait(&bars[kBarBFull], (bfills - 1) & 1, never);
             if (!ok) set_abort(ctl, p.status);
         }
     } else if (warp == 2) {
@@ -414,7 +412,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const uint64_t dT = tc::sdesc_sw128(tc::smem_u32(smem + kOffT), kBox, 1024);
             const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffX), kBox, 1024);
             for (int k = 0; ok && k < nblk; ++k) {
-                const int u = k & 1, v = k >> 1;
+                const int u = k % kXBufs, v = k / kXBufs;
                 if (k >= 1 && !tc::mbar_wait(&bars[kBarYFree], (k - 1) & 1, abort_flag)) { ok = false; break; }
                 if (!tc::mbar_wait(&bars[kBarTileReady], k & 1, abort_flag)) { ok = false; break; }
                 if (!tc::mbar_wait(&bars[kBarCFull], k & 1, abort_flag)) { ok = false; break; }
@@ -466,21 +464,20 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const uint32_t id_u = tc::idesc_bf16(128, 2 * kH, true, true);
             // A = B^T, MN-major: rows = tokens = K, the two 64-state boxes kBox
             // apart; B = the folded X buffer, MN-major as for P X
-            const uint64_t dBt0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffB), kBox, 1024);
+            const uint64_t dBt = tc::sdesc_sw128(tc::smem_u32(smem + kOffB), kBox, 1024);
             const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(smem + kOffX), kBox, 1024);
             for (int k = 0; ok && k < nblk; ++k) {
-                const int u = k & 1, v = k >> 1;
+                const int u = k % kXBufs, v = k / kXBufs;
                 if (!tc::mbar_wait(&bars[kBarTileReady], k & 1, abort_flag)) { ok = false; break; }
                 if (!tc::mbar_wait(&bars[kBarFold2 + u], v & 1, abort_flag)) { ok = false; break; }
-                if (!tc::mbar_wait(&bars[kBarBFull + u], v & 1, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&bars[kBarBFull], k & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
-                const uint64_t dBt = dBt0 + (uint64_t)u * ((2 * kBox) >> 4);
                 const uint64_t dX = dX0 + (uint64_t)u * ((2 * kBox) >> 4);
 #pragma unroll
                 for (int k16 = 0; k16 < kBlk / 16; ++k16)
                     tc::mma_bf16_ss(tmem + kColH, dBt + 128 * k16, dX + 128 * k16, id_u, 1u);
                 tc::mma_commit(&bars[kBarUDone]);
-                tc::mma_commit(&bars[kBarBFree + u]);
+                tc::mma_commit(&bars[kBarBFree]);
                 tc::mma_commit(&bars[kBarXUsed + u]);
             }
             tc::mma_commit(&bars[kBarDrainC]);
@@ -495,7 +492,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         const int i = 32 * (warp - kWarpFold0) + lane;
         bool ok = true;
         for (int k = 0; ok && k < nblk; ++k) {
-            const int u = k & 1, v = k >> 1;
+            const int u = k % kXBufs, v = k / kXBufs;
             if (!(ok = tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag))) break;
             const Vec* vec = vecs + u;
             const bool all_mild = block_split(vec, 0).mild && block_split(vec, 1).mild;
@@ -557,7 +554,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         // forms block kp's P tiles of this warp; false on a timeout
         auto form_p = [&](int kp) -> bool {
-            const int up = kp & 1, vp = kp >> 1;
+            const int up = kp % kXBufs, vp = kp / kXBufs;
             if (!tc::mbar_wait(&bars[kBarCbDone], kp & 1, abort_flag)) return false;
             if (!tc::mbar_wait(&bars[kBarXFull + up], vp & 1, abort_flag)) return false;
             tc::tc_fence_after();
@@ -610,7 +607,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         };
         bool ok = form_p(0);
         for (int k = 0; ok && k < nblk; ++k) {
-            const int u = k & 1, v = k >> 1;
+            const int u = k % kXBufs, v = k / kXBufs;
             const int64_t t = (int64_t)k * kBlk + i;
             // x of this row (32 columns) for D x, from global memory: the X
             // buffer holds w . X by the time y is formed
@@ -720,7 +717,7 @@ k_ssd_fused_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         float dprev0 = 1.f, dprev1 = 1.f;  // per head: h = dprev * (what TMEM holds)
         bool ok = true;
         for (int k = 0; k < nblk; ++k) {
-            const int u = k & 1, v = k >> 1;
+            const int u = k % kXBufs, v = k / kXBufs;
             if (ok && k >= 1) ok = tc::mbar_wait(&bars[kBarUDone], (k - 1) & 1, abort_flag);
             if (ok && k >= 1) ok = tc::mbar_wait(&bars[kBarZDone], (k - 1) & 1, abort_flag);  // tile free
             if (ok) ok = tc::mbar_wait(&bars[kBarXFull + u], v & 1, abort_flag);
