@@ -159,3 +159,32 @@ def test_fused_long_sequence_full_size(monkeypatch):
     for b, h in pairs:
         assert rel_err(np64(y[b, :, h]), ref[(b, h)][0]) <= TOL["bf16"], (b, h)
         assert rel_err(np64(fin[b, h]), ref[(b, h)][1]) <= TOL["bf16"], (b, h)
+
+
+def _fused_sweep():
+    from mamba_chunked_ssd_gb300.synthetic import sweep_workloads
+    return [w for w in sweep_workloads(seeds=(0, 1, 2)) if w.dstate == 128 and w.headdim == 64]
+
+
+FUSED_SWEEP = _fused_sweep()
+
+
+@pytest.mark.parametrize("w", FUSED_SWEEP, ids=[f"{w.name}_seed{w.seed}" for w in FUSED_SWEEP])
+def test_fused_sweep_shape_sampled(w, monkeypatch):
+    """The sweep points the fused kernel covers (state 128, head dim 64; every
+    length, both chunks, seeds 0-2) at full size on the fused path, inputs
+    drawn on the GPU; four (batch, head) pairs per point against the fp64
+    recurrence."""
+    monkeypatch.setenv("MAMBA2_FWD_PATH", "fused")
+    inp = make_inputs(w, device="cuda")
+    y, fin = _fwd(inp, w)
+    pairs = sample_pairs(w.batch, w.nheads, 4, seed=7 * w.seqlen + 1000 * w.seed + w.chunk_size)
+    ref = oracle_pairs(inp, pairs)
+    bi = torch.tensor([b for b, _ in pairs], device="cuda")
+    hi = torch.tensor([h for _, h in pairs], device="cuda")
+    ys = y[bi, :, hi].cpu()
+    fs = fin[bi, hi].cpu()
+    for i, p in enumerate(pairs):
+        assert rel_err(np64(ys[i]), ref[p][0]) <= TOL["bf16"], p
+        assert rel_err(np64(fs[i]), ref[p][1]) <= TOL["bf16"], p
+    assert torch.isfinite(y.float()).all()
