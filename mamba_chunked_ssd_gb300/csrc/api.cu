@@ -127,6 +127,20 @@ cudaError_t ensure_max_dynamic_smem(const void* func, int bytes) {
     return e;
 }
 
+int sm_count() {
+    static std::mutex mu;
+    static std::map<int, int> known;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = known.find(dev);
+    if (it != known.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    known[dev] = n;
+    return n;
+}
+
 unsigned int* device_status_word() {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;

@@ -174,6 +174,10 @@ bool use_fused_forward(const Geom& g, bool bf16);
 // Device address of the current device's status word (api.cu).
 unsigned int* device_status_word();
 
+// Streaming multiprocessors of the current device (queried once per device;
+// 0 if the query fails) (api.cu).
+int sm_count();
+
 // Raises `func`'s dynamic shared-memory limit to at least `bytes` on the
 // current device.  The driver call is made once per (device, kernel) and again
 // only when a launch needs more than was set before, so launches do no

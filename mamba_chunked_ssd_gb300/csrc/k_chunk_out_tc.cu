@@ -54,6 +54,7 @@
 // first, and their quadrant 2 takes the chunk start as its reference.
 // Every wait is bounded; a timeout sets the status word and the CTA unwinds.
 #include <stdlib.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -116,6 +117,7 @@ struct CoTcParams {
     int nhb;          // heads per CTA (all in one group)
     int nstr;         // epilogue head streams (2 for H = 64, 1 for H = 128)
     int head_blocks;  // nheads / nhb
+    int persistent;   // one CTA per SM walks the work items (one row block per chunk)
     uint32_t off_C, off_CB10, smem_bytes;
     CoLayout lay[2];  // by row block I
     const float* dt;
@@ -203,16 +205,31 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const Geom& g = p.g;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // blockIdx.x = hb + head_blocks (I + (T / 128) c): the chunk index rides in
-    // x, whose range (2^31 - 1) covers every chunk count the library accepts
-    const int hb = (int)(blockIdx.x % (unsigned)p.head_blocks);
-    const unsigned rest = blockIdx.x / (unsigned)p.head_blocks;
-    const int I = (int)(rest % (unsigned)(T / 128));  // row block inside the chunk
-    const int64_t c = rest / (unsigned)(T / 128);
-    const int64_t b = blockIdx.y;
-    const int64_t t0 = (int64_t)c * T;
+    // Work items: x index hb + head_blocks (I + (T / 128) c) (the chunk index
+    // rides in x, whose range covers every chunk count the library accepts)
+    // and the batch row.  Without persistence each CTA takes the one item its
+    // blockIdx names.  With it (one row block per chunk, so every item has the
+    // same shared-memory layout) one CTA per SM walks the items blockIdx.x,
+    // blockIdx.x + gridDim.x, ...: every item starts with fresh barriers and
+    // ends with the CTA quiescent, so items are independent, and the CTA keeps
+    // its tensor memory and skips the turnover between CTAs (measured at
+    // about 4.6 us per CTA with one CTA per SM).
+    const int64_t gx = (int64_t)p.head_blocks * (T / 128) * g.nchunks;
+    const int64_t n_items = gx * g.batch;
+    const int64_t it_step = p.persistent ? (int64_t)gridDim.x : n_items;
+    bool tmem_held = false;
+    uint32_t tmem = 0;
+    for (int64_t it = p.persistent ? (int64_t)blockIdx.x : (int64_t)blockIdx.x + gx * blockIdx.y; it < n_items;
+         it += it_step) {
+    const int64_t xi = it % gx;
+    const int hb = (int)(xi % p.head_blocks);
+    const int64_t rest = xi / p.head_blocks;
+    const int I = (int)(rest % (T / 128));  // row block inside the chunk
+    const int64_t c = rest / (T / 128);
+    const int64_t b = it / gx;
+    const int64_t t0 = c * T;
     const int tc = (int)imin64(T, g.seqlen - t0);  // valid tokens of the chunk
-    if (128 * I >= tc) return;                           // ragged tail: no valid row here
+    if (128 * I >= tc) continue;                         // ragged tail: no valid row here
     const int h0 = hb * p.nhb;
     const int nvh = p.nhb * VS;  // virtual heads of this CTA
     const int grp = (int)(h0 / g.heads_per_group);
@@ -251,10 +268,10 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc::mbar_init(&bars[kBarStored + i], 1);
             tc::mbar_init(&bars[kBarYReady + i], wps);
         }
-        ctl->abort = 0;
+        if (!tmem_held) ctl->abort = 0;
         tc::fence_barrier_init();
     }
-    if (PAIR) {
+    if (PAIR && !tmem_held) {
         // zero rows 64..127 of C_top and rows 0..63 of C_bot (the TMA fills
         // the other halves); the MMAs read them through the async proxy
         const int nbox = S / 64;
@@ -265,14 +282,15 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         tc::fence_proxy_async_smem();
     }
-    if (warp == 1) {
+    if (warp == 1 && !tmem_held) {
         tc::tmem_alloc(&ctl->tmem_base, 512);
         tc::tmem_relinquish();
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = ctl->tmem_base;
+    if (!tmem_held) tmem = ctl->tmem_base;
+    tmem_held = true;
     volatile int* abort_flag = &ctl->abort;
     const uint32_t x_bytes = (uint32_t)Tj * H * 2;
     const uint32_t h_bytes = (uint32_t)S * H * 2;
@@ -784,7 +802,12 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    // the item's barriers have completed their last phases: retire them
+    if (threadIdx.x == 0)
+        for (int i = 0; i < kNumBars; ++i) tc::mbar_inval(&bars[i]);
+    if (*abort_flag) break;  // read after the barrier: the same for every thread
+    }
+    if (tmem_held && warp == 1) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 512);
     }
@@ -952,7 +975,15 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
                                : (p.T == 256 ? k_chunk_out_tc<128, 256, 1, false> : k_chunk_out_tc<128, 128, 1, false>));
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((int64_t)p.head_blocks * (p.T / 128) * p.g.nchunks), (unsigned)g.batch);
+    // One row block per chunk: one CTA per SM walks the work items (unless
+    // MAMBA2_CHUNK_OUT_PERSISTENT=0); else one CTA per item.
+    const int64_t gx = (int64_t)p.head_blocks * (p.T / 128) * p.g.nchunks, n_items = gx * g.batch;
+    const char* pe = getenv("MAMBA2_CHUNK_OUT_PERSISTENT");
+    p.persistent = (row_blocks(g) == 1 && !(pe && strcmp(pe, "0") == 0)) ? 1 : 0;
+    const int nsm = sm_count();
+    if (p.persistent && nsm <= 0) return cudaErrorInvalidValue;
+    dim3 grid = p.persistent ? dim3((unsigned)(n_items < nsm ? n_items : nsm))
+                             : dim3((unsigned)gx, (unsigned)g.batch);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
