@@ -205,34 +205,57 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const Geom& g = p.g;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // Work items: x index hb + head_blocks (I + (T / 128) c) (the chunk index
-    // rides in x, whose range covers every chunk count the library accepts)
-    // and the batch row.  Without persistence each CTA takes the one item its
-    // blockIdx names.  With it (one row block per chunk, so every item has the
-    // same shared-memory layout) one CTA per SM walks the items blockIdx.x,
-    // blockIdx.x + gridDim.x, ...: every item starts with fresh barriers and
-    // ends with the CTA quiescent, so items are independent, and the CTA keeps
-    // its tensor memory and skips the turnover between CTAs (measured at
-    // about 4.6 us per CTA with one CTA per SM).
+    // Work items.  Without persistence each CTA takes the one item its
+    // blockIdx names: x index hb + head_blocks (I + (T / 128) c) (the chunk
+    // index rides in x, whose range covers every chunk count the library
+    // accepts) and the batch row, nhb heads from head hb * nhb.  With it (one
+    // row block per chunk, so every item has the same shared-memory layout)
+    // one CTA per SM takes an equal share of the (batch, chunk, virtual head)
+    // triples, in that order, and runs it as items of consecutive heads that
+    // share one chunk and one group: so C, B and their product are formed
+    // once per chunk and group rather than once per 16 heads, and the CTAs'
+    // shares differ by one head at most.  Every item starts with fresh
+    // barriers and ends with the CTA quiescent, so items are independent, and
+    // the CTA keeps its tensor memory and skips the turnover between CTAs.
     const int64_t gx = (int64_t)p.head_blocks * (T / 128) * g.nchunks;
     const int64_t n_items = gx * g.batch;
-    const int64_t it_step = p.persistent ? (int64_t)gridDim.x : n_items;
+    const int64_t vh_all = g.nheads * VS;               // virtual heads per chunk
+    const int64_t vh_grp = g.heads_per_group * VS;      // virtual heads per group
+    const int64_t n_units = g.batch * g.nchunks * vh_all;
+    int64_t f = p.persistent ? n_units * blockIdx.x / gridDim.x : 0;
+    const int64_t f_end = p.persistent ? n_units * (blockIdx.x + 1) / gridDim.x : 0;
+    int64_t it = p.persistent ? n_items : (int64_t)blockIdx.x + gx * blockIdx.y;
     bool tmem_held = false;
     uint32_t tmem = 0;
-    for (int64_t it = p.persistent ? (int64_t)blockIdx.x : (int64_t)blockIdx.x + gx * blockIdx.y; it < n_items;
-         it += it_step) {
-    const int64_t xi = it % gx;
-    const int hb = (int)(xi % p.head_blocks);
-    const int64_t rest = xi / p.head_blocks;
-    const int I = (int)(rest % (T / 128));  // row block inside the chunk
-    const int64_t c = rest / (T / 128);
-    const int64_t b = it / gx;
+    for (;;) {
+    int64_t b, c;
+    int I, vh0, nvh;
+    if (p.persistent) {
+        if (f >= f_end) break;
+        const int64_t bc = f / vh_all;
+        const int vh = (int)(f % vh_all);
+        nvh = (int)imin64(f_end - f, (vh / vh_grp + 1) * vh_grp - vh);
+        vh0 = vh;
+        b = bc / g.nchunks;
+        c = bc % g.nchunks;
+        I = 0;
+        f += nvh;
+    } else {
+        if (it >= n_items) break;
+        const int64_t xi = it % gx;
+        const int hb = (int)(xi % p.head_blocks);
+        const int64_t rest = xi / p.head_blocks;
+        I = (int)(rest % (T / 128));  // row block inside the chunk
+        c = rest / (T / 128);
+        b = it / gx;
+        vh0 = hb * p.nhb * VS;
+        nvh = p.nhb * VS;
+        it = n_items;
+    }
     const int64_t t0 = c * T;
     const int tc = (int)imin64(T, g.seqlen - t0);  // valid tokens of the chunk
     if (128 * I >= tc) continue;                         // ragged tail: no valid row here
-    const int h0 = hb * p.nhb;
-    const int nvh = p.nhb * VS;  // virtual heads of this CTA
-    const int grp = (int)(h0 / g.heads_per_group);
+    const int grp = (int)(vh0 / VS / g.heads_per_group);
     const int Tj = 128 * (I + 1);  // columns j that rows of block I can see
     const int S = (int)g.dstate;
     constexpr int nstr = (H == 64) ? 2 : 1;
@@ -300,7 +323,7 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     auto issue_y_store = [&](int k, int st) {
         const uint8_t* sY = sStage + slot_of(st) * lay.stage_bytes;
         for (int cb = 0; cb < H / 64; ++cb)
-            tc::tma_store_4d(&tm_y, sY + cb * (Tj * 128) + I * 16384, (k % VS) * H + cb * 64, h0 + k / VS,
+            tc::tma_store_4d(&tm_y, sY + cb * (Tj * 128) + I * 16384, ((vh0 + k) % VS) * H + cb * 64, (vh0 + k) / VS,
                              (int)(t0 + 128 * I), (int)b);
         tc::bulk_commit();
     };
@@ -372,8 +395,8 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             float* vG = reinterpret_cast<float*>(sX + lay.off_vec_in_stage);  // G[T], dt[T], D
             float* vDt = vG + T;
             uint64_t* full = &bars[kBarFull + fill];
-            const int h = h0 + k / VS;          // real head
-            const int col0 = (k % VS) * H;      // its first column in this virtual head
+            const int h = (vh0 + k) / VS;          // real head
+            const int col0 = ((vh0 + k) % VS) * H;  // its first column in this virtual head
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(full, x_bytes + (PAIR ? 2 : 1) * h_bytes);
                 // state rows of the chunk (of both chunks of a pair; past the
