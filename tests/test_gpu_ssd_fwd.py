@@ -313,6 +313,38 @@ def test_outputs_stay_inside_their_buffers(w):
     assert rel_err(np64(y2.t), r["y"]) <= TOL[w.dtype]
 
 
+# Stage 3 with one row block per chunk runs one CTA per SM, each taking an
+# equal share of the (batch, chunk, virtual head) triples and running it as
+# items of consecutive heads of one chunk and group.  These shares start and
+# end inside chunks and inside groups; a 128-wide head is two virtual heads,
+# so a share may start at its second half; chunks of 64 run in pairs; the
+# sequences end ragged.
+SHARE_SHAPES = [
+    Workload("share_h128_groups_ragged", 2, 33 * 128 - 37, 24, 128, 128, 3, 128, init_state=True),
+    Workload("share_h64_groups", 3, 20 * 128 + 5, 40, 64, 128, 5, 128, init_state=True),
+    Workload("share_t64_pairs", 3, 41 * 64 - 9, 36, 64, 64, 3, 64, init_state=True),
+]
+
+
+@pytest.mark.parametrize("w", SHARE_SHAPES, ids=[w.name for w in SHARE_SHAPES])
+def test_persistent_shares(w, monkeypatch):
+    """Sampled (batch, head) pairs against the fp64 recurrence, and the same
+    pass with one CTA per work item gives the same y bit for bit (each head's
+    products and epilogue do not depend on which CTA runs them)."""
+    monkeypatch.setenv("MAMBA2_FWD_CHUNK", "given")
+    inp = make_inputs(w, device="cuda")
+    y, fin = _fwd(inp, w)
+    pairs = sample_pairs(w.batch, w.nheads, 12, seed=3)
+    ref = oracle_pairs(inp, pairs)
+    for (b, h) in pairs:
+        ry, rs = ref[(b, h)]
+        assert rel_err(np64(y[b, :, h]), ry) <= TOL[w.dtype], (b, h)
+        assert rel_err(np64(fin[b, h]), rs) <= TOL[w.dtype], (b, h)
+    monkeypatch.setenv("MAMBA2_CHUNK_OUT_PERSISTENT", "0")
+    y0, fin0 = _fwd(inp, w)
+    assert torch.equal(y, y0) and torch.equal(fin, fin0)
+
+
 def test_more_chunks_than_a_grid_y_dimension():
     """65 600 chunks of 128 tokens (8.4 M tokens, ragged end): more chunks than
     a grid's y or z dimension holds.  The carried state forgets a prefix of
