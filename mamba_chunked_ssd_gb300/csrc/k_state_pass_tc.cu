@@ -19,6 +19,9 @@
 //               the state h lives in TMEM next to U; per chunk each thread
 //               (one state row, half of the columns) stores h_c, then sets
 //               h <- exp2(G_last) h + U_c.
+// Heads of 64 columns may run in pairs (HP below): a pair's x rows are
+// adjacent, so the two heads load as one 128-column head and share B's tile
+// and one product per sub-block.
 // The weighted-operand fold applies the blog's "pre-multiplied operand" to X
 // instead of B (same product; X is the smaller per-head tile).  States past
 // dstate (when dstate = 64) are zero-filled by TMA and never stored.
@@ -110,7 +113,12 @@ __device__ __forceinline__ void set_abort(SharedCtl* ctl, unsigned int* status) 
 // group's two fp32 boxes become its hi box and its lo box), U takes three
 // products (B_hi (w x)_hi + B_hi (w x)_lo + B_lo (w x)_hi), and the chunk
 // states leave as fp32, rows [b, nh, nc, S] x H.
-template <int H, int T, int KB, bool SPLIT>
+// HP: a pair of heads 2 h', 2 h' + 1 of 64 columns each, whose x rows are
+// adjacent in memory, runs as one head of 128 columns (H = 128): one B tile
+// and one 128 x 128 x KB product per sub-block serve both heads.  The fold
+// takes each half's own weights, the scan each half's own decay, and the
+// halves' states come from and go to their own heads' rows.
+template <int H, int T, int KB, bool SPLIT, bool HP = false>
 __global__ void __launch_bounds__(kThreads, 2)
 k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_cs, const SpTcParams p) {
@@ -119,11 +127,15 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const Geom& g = p.g;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int mt = blockIdx.x;              // 128-row tile of the state
-    const int h = blockIdx.y;
+    const int h = blockIdx.y;               // head (HP: head pair; x's view has nheads / 2 heads of 128)
     const int64_t b = blockIdx.z / (unsigned)p.seg_grid;
     const int seg = (int)(blockIdx.z % (unsigned)p.seg_grid);
-    const int64_t bh = b * g.nheads + h;
-    const int grp = (int)(h / g.heads_per_group);
+    const int hr = HP ? 2 * h : h;          // the (first) real head
+    const int64_t bh = b * g.nheads + hr;
+    const int grp = (int)(hr / g.heads_per_group);
+    static_assert(!HP || (H == 128 && !SPLIT), "head pairs: two bf16 heads of 64 columns");
+    constexpr int HH = HP ? 64 : H;         // columns of a real head
+    constexpr int NV = HP ? 2 : 1;          // real heads of this CTA
     const int S = (int)g.dstate;
     constexpr int kKb = KB;
     static_assert(KB == 64 || KB == 128, "sub-blocks of 64 or 128 tokens");
@@ -206,14 +218,20 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // straight into the stage; each lane arrives on the stage barrier
             // once its copies have landed.
 #pragma unroll
-            for (int r = 0; r < kKb / 32; ++r) {
-                const int tl = sb * kKb + lane + 32 * r;
-                const int tv = tl < tc ? tl : tc - 1;
-                tc::cp_async4(sV + lane + 32 * r, Gbh + t0 + tv, 4);
-                tc::cp_async4(sV + kKb + lane + 32 * r, p.dt + (b * g.seqlen + t0 + tv) * g.nheads + h,
-                              tl < tc ? 4u : 0u);
+            for (int v = 0; v < NV; ++v) {
+                // head hr + v: its G row follows the previous head's
+                float* sVv = sV + v * (2 * kKb + 1);
+                const float* Gv = Gbh + v * g.seqlen;
+#pragma unroll
+                for (int r = 0; r < kKb / 32; ++r) {
+                    const int tl = sb * kKb + lane + 32 * r;
+                    const int tv = tl < tc ? tl : tc - 1;
+                    tc::cp_async4(sVv + lane + 32 * r, Gv + t0 + tv, 4);
+                    tc::cp_async4(sVv + kKb + lane + 32 * r, p.dt + (b * g.seqlen + t0 + tv) * g.nheads + hr + v,
+                                  tl < tc ? 4u : 0u);
+                }
+                if (lane == 0) tc::cp_async4(sVv + 2 * kKb, Gv + t0 + tc - 1, 4);
             }
-            if (lane == 0) tc::cp_async4(sV + 2 * kKb, Gbh + t0 + tc - 1, 4);
             tc::cp_async_mbar_arrive_noinc(&bars[kBarFull + st]);
         }
         if (!ok && lane == 0) set_abort(ctl, p.status);
@@ -294,6 +312,10 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (!tc::mbar_wait(&bars[kBarFull + st], full_phase, abort_flag)) { ok = false; break; }
                 const float* sV = reinterpret_cast<const float*>(smem + st * p.stage_bytes + p.off_w_in_stage);
                 const float w = sV[kKb + frow] * exp2f(sV[2 * kKb] - sV[frow]);  // w_t = dt_t exp2(G_last - G_t)
+                // HP: the second head's weight, for the row's second 64-column box
+                const float w1 = HP ? sV[(2 * kKb + 1) + kKb + frow] *
+                                          exp2f(sV[(2 * kKb + 1) + 2 * kKb] - sV[(2 * kKb + 1) + frow])
+                                    : w;
                 uint8_t* rowp = smem + st * p.stage_bytes + p.off_x_in_stage + frow * 128;
                 if (SPLIT) {
                     // fp32 x -> w x as a hi/lo pair, one 64-column group at a
@@ -344,11 +366,12 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                     for (int f = 0; f < 2; ++f) {
                         const int flat = fh * per + f0 + f;
+                        const float wf = (HP && (flat >> 3)) ? w1 : w;
                         uint4 a = v[f];
-                        a.x = tc::pack_bf16x2(tc::bf16_lo(a.x) * w, tc::bf16_hi(a.x) * w);
-                        a.y = tc::pack_bf16x2(tc::bf16_lo(a.y) * w, tc::bf16_hi(a.y) * w);
-                        a.z = tc::pack_bf16x2(tc::bf16_lo(a.z) * w, tc::bf16_hi(a.z) * w);
-                        a.w = tc::pack_bf16x2(tc::bf16_lo(a.w) * w, tc::bf16_hi(a.w) * w);
+                        a.x = tc::pack_bf16x2(tc::bf16_lo(a.x) * wf, tc::bf16_hi(a.x) * wf);
+                        a.y = tc::pack_bf16x2(tc::bf16_lo(a.y) * wf, tc::bf16_hi(a.y) * wf);
+                        a.z = tc::pack_bf16x2(tc::bf16_lo(a.z) * wf, tc::bf16_hi(a.z) * wf);
+                        a.w = tc::pack_bf16x2(tc::bf16_lo(a.w) * wf, tc::bf16_hi(a.w) * wf);
                         *reinterpret_cast<uint4*>(rowp + (flat >> 3) * x_box_bytes +
                                                   ((((flat & 7) + frow) & 7) << 4)) = a;
                     }
@@ -364,9 +387,10 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const bool valid = s < S;
             const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
             const float* Gbh = p.G + bh * g.seqlen;
-            auto glast_of = [&](int c) -> float {
+            // G_last of chunk c for real head hr + v
+            auto glast_of = [&](int c, int v) -> float {
                 const int64_t t0 = (int64_t)c * T;
-                return Gbh[t0 + imin64(T, g.seqlen - t0) - 1];
+                return Gbh[v * g.seqlen + t0 + imin64(T, g.seqlen - t0) - 1];
             };
             // h <- initial state (segment 0), the segment's entering state
             // (segment pass), or zeros; 32 columns (eight 16-byte loads) per
@@ -376,10 +400,12 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             auto load_h = [&](const float* h_in) {
 #pragma unroll 1
                 for (int m = 0; m < H / 32; ++m) {
+                    // columns 32 m .. of the CTA's state: real head hr + (32 m) / HH
+                    const float* src = h_in + ((32 * m) / HH) * S * HH + s * HH + (32 * m) % HH;
                     float4 f[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        f[j] = (valid && h_in) ? *reinterpret_cast<const float4*>(h_in + s * H + 32 * m + 4 * j)
+                        f[j] = (valid && h_in) ? *reinterpret_cast<const float4*>(src + 4 * j)
                                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
@@ -397,11 +423,11 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 tc::tmem_wait_st();
             };
             if (seg == 0) {
-                load_h(p.init ? p.init + bh * S * H : nullptr);
+                load_h(p.init ? p.init + bh * S * HH : nullptr);
                 tc::griddep_wait();
             } else {
                 tc::griddep_wait();
-                load_h(p.mode == kSegmentPass ? p.seg_states + (bh * (p.nseg - 1) + seg - 1) * S * H : nullptr);
+                load_h(p.mode == kSegmentPass ? p.seg_states + (bh * (p.nseg - 1) + seg - 1) * S * HH : nullptr);
             }
             // Per chunk: h_{c+1} = exp2(G_last) h_c + U_c into the other h
             // buffer (then U_c's buffer is released to the MMA), then h_c is
@@ -419,14 +445,17 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const int nhalf = (S - mt * 128 >= 128) ? 2 : 1;
             const int npass = p.stg_tiles >= nhalf ? 1 : nhalf;
             constexpr uint32_t tile_bytes = (SPLIT ? H / 32 : H / 64) * 8192;
-            float gl_next = glast_of(c_begin);
+            float gl_next = glast_of(c_begin, 0), gl_next1 = HP ? glast_of(c_begin, 1) : 0.f;
             // Every scan warp runs every iteration and every named barrier below,
             // whatever its own waits return, so no warp is left at a barrier;
             // after a failed wait a warp only skips the work.
             for (int cl = 0; cl < nchl; ++cl) {
                 const int c = c_begin + cl, ub = cl & 1;
-                const float alpha = exp2f(gl_next);
-                if (cl + 1 < nchl) gl_next = glast_of(c + 1);
+                const float alpha = exp2f(gl_next), alpha1 = HP ? exp2f(gl_next1) : alpha;
+                if (cl + 1 < nchl) {
+                    gl_next = glast_of(c + 1, 0);
+                    if (HP) gl_next1 = glast_of(c + 1, 1);
+                }
                 if (ok) ok = tc::mbar_wait(&bars[kBarUDone + ub], (cl >> 1) & 1, abort_flag);
                 tc::tc_fence_after();
                 const int64_t row0 = (bh * g.nchunks + c) * S + mt * 128;  // first state row of the tile
@@ -437,13 +466,14 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll 1
                     for (int m = 0; m < H / 16; ++m) {
                         uint32_t hv[16], uv[16];
+                        const float am = (HP && 16 * m >= HH) ? alpha1 : alpha;  // this column group's head
                         tc::tmem_ld16_nowait(h_cur + lane_base + 16 * m, hv);
                         tc::tmem_ld16_nowait(tm_u0 + ub * H + lane_base + 16 * m, uv);
                         tc::tmem_wait_ld16(hv);
                         tc::tmem_wait_ld16(uv);
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            hv[e] = __float_as_uint(fmaf(alpha, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
+                            hv[e] = __float_as_uint(fmaf(am, __uint_as_float(hv[e]), __uint_as_float(uv[e])));
                         tc::tmem_st16(h_nxt + lane_base + 16 * m, hv);
                     }
                 }
@@ -496,8 +526,10 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         constexpr int scols = SPLIT ? 32 : 64;  // columns per box (fp32 / bf16)
                         for (int hf = (npass == 1 ? 0 : pass); hf < (npass == 1 ? nhalf : pass + 1); ++hf)
                             for (int cb = 0; cb < H / scols; ++cb)
+                                // HP: box cb is head hr + cb's 64 columns, in its own rows
                                 tc::tma_store_2d(&tm_cs, stg + (npass == 1 ? hf : 0) * tile_bytes + cb * 8192,
-                                                 cb * scols, (int)(row0 + 64 * hf));
+                                                 HP ? 0 : cb * scols,
+                                                 (int)(row0 + 64 * hf + (HP ? cb * g.nchunks * S : 0)));
                         tc::bulk_commit();
                     }
                 }
@@ -507,15 +539,15 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // segment's into final_state
             float* h_out = nullptr;
             if (p.mode == kSegmentSummary)
-                h_out = p.seg_states + (bh * (p.nseg - 1) + seg) * S * H;
+                h_out = p.seg_states + (bh * (p.nseg - 1) + seg) * S * HH;
             else if (seg == p.nseg - 1 && p.final_state)
-                h_out = p.final_state + bh * S * H;
+                h_out = p.final_state + bh * S * HH;
             if (ok && h_out && valid) {
 #pragma unroll 1
                 for (int m = 0; m < H / 16; ++m) {
                     uint32_t hv[16];
                     tc::tmem_ld16(tm_h + (nchl & 1) * H + lane_base + 16 * m, hv);  // h after the last chunk
-                    float4* d4 = reinterpret_cast<float4*>(h_out + s * H + 16 * m);
+                    float4* d4 = reinterpret_cast<float4*>(h_out + ((16 * m) / HH) * S * HH + s * HH + (16 * m) % HH);
 #pragma unroll
                     for (int s4 = 0; s4 < 4; ++s4)
                         d4[s4] = make_float4(__uint_as_float(hv[4 * s4]), __uint_as_float(hv[4 * s4 + 1]),
@@ -585,8 +617,8 @@ __global__ void __launch_bounds__(256) k_state_carry(const float* __restrict__ G
 // A split (fp32) problem's stages hold B's hi and lo tiles and fp32 x (the
 // bytes of x's hi/lo pair): one CTA per SM with a ring of 64-token
 // sub-blocks.
-bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2, bool split = false) {
-    const int H = (int)g.headdim;
+bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2, bool split = false, bool hp = false) {
+    const int H = hp ? 128 : (int)g.headdim;  // head pairs run as one head of 128 columns
     p.tmem_cols = (4 * H <= 256) ? 256 : 512;  // U x 2, h x 2
     const bool two = p.tmem_cols == 256 && ctas_per_sm_cap >= 2 && !split;
     const int kKb = (!two && g.chunk >= 128 && !split) ? 128 : 64;
@@ -598,8 +630,8 @@ bool plan(const Geom& g, SpTcParams& p, int ctas_per_sm_cap = 2, bool split = fa
     // split: a 64-column group's lo box follows its hi box
     p.off_xlo_in_stage = p.off_x_in_stage + kKb * 128;
     p.off_w_in_stage = p.off_x_in_stage + planes * (H / 64) * kKb * 128;
-    // G[kKb], dt[kKb], G_last; padded to keep stages 1 KB aligned
-    p.stage_bytes = p.off_w_in_stage + ((2 * kKb + 1) * 4 + 1023) / 1024 * 1024;
+    // G[kKb], dt[kKb], G_last (of each head of a pair); padded to keep stages 1 KB aligned
+    p.stage_bytes = p.off_w_in_stage + ((hp ? 2 : 1) * (2 * kKb + 1) * 4 + 1023) / 1024 * 1024;
     const uint32_t budget = two ? (kSmemLimit / 2 - 2048) : kSmemLimit;
     const uint32_t fixed = kNumBars * 8 + 64 + 1024;
     // Staging tiles of 64 rows x H: bf16 (boxes of 64 columns), or fp32
@@ -665,15 +697,34 @@ bool state_pass_tc_fits(const Geom& g) {
     return plan(g, p);
 }
 
+// Heads of 64 columns run in pairs (two heads of one group per CTA, as one
+// head of 128 columns, one CTA per SM) where the pairs still give at least
+// 128 CTAs and the state has 128 rows or more.  Measured on GB300 (whole
+// forward pass, µs, single heads / pairs, same box): long_seq_carried_state
+// (256 (batch, head) CTAs) 261.9 / 256.3; sweep state 256, L 4096 (2048)
+// 763 / 758; state 128, L 1024 (4096) 528.6 / 530; state 64, L 16384 (256)
+// 433 / 436; 128 (batch, head) CTAs: mamba2_1p3b_layer 50.1 / 60.2, state
+// 128, L 32768 513 / 657.  MAMBA2_STATE_PAIRS=0 or =1 turns the pairs off
+// or on (where they apply), for timing both on one shape.
+bool use_head_pairs(const Geom& g, const StatePassArgs& a) {
+    if (a.split || a.segments > 1 || g.headdim != 64) return false;
+    if (g.nheads % 2 != 0 || g.heads_per_group % 2 != 0) return false;
+    const char* env = getenv("MAMBA2_STATE_PAIRS");
+    if (env && (env[0] == '0' || env[0] == '1') && env[1] == 0) return env[0] == '1';
+    return g.dstate >= 128 && g.batch * g.nheads * ((g.dstate + 127) / 128) >= 2 * 128;
+}
+
 cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStream_t st) {
     SpTcParams p{};
     p.g = g;
+    const bool hp = use_head_pairs(g, a);
     const int mtiles = (int)((g.dstate + 127) / 128);
     const int seg_grid = a.segments > 1 ? (a.summary ? a.segments - 1 : a.segments) : 1;
-    const int64_t ctas = (int64_t)mtiles * g.nheads * g.batch * seg_grid;
+    const int64_t heads = hp ? g.nheads / 2 : g.nheads;  // CTAs along the heads
+    const int64_t ctas = (int64_t)mtiles * heads * g.batch * seg_grid;
     const bool split = a.split;
     if (split && (a.segments > 1 || g.chunk != 128)) return cudaErrorInvalidConfiguration;
-    if (!plan(g, p, ctas <= kTargetSms ? 1 : 2, split)) return cudaErrorInvalidConfiguration;
+    if (!plan(g, p, ctas <= kTargetSms ? 1 : 2, split, hp)) return cudaErrorInvalidConfiguration;
     p.mode = kWholeSequence;
     p.nseg = 1;
     p.cps = (int)g.nchunks;
@@ -699,8 +750,10 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
     const uint32_t xcols = split ? 32 : 64;  // columns of their boxes
     CUtensorMap tm_x, tm_b;
     {
-        const uint64_t dims[4] = {H, nh, L, (uint64_t)g.batch};
-        const uint64_t strides[3] = {H * xe, nh * H * xe, L * nh * H * xe};
+        // head pairs: x viewed as nh / 2 heads of 128 columns (a pair's rows are adjacent)
+        const uint64_t Hx = hp ? 2 * H : H, nhx = hp ? nh / 2 : nh;
+        const uint64_t dims[4] = {Hx, nhx, L, (uint64_t)g.batch};
+        const uint64_t strides[3] = {Hx * xe, nhx * Hx * xe, L * nhx * Hx * xe};
         const uint32_t box[4] = {xcols, 1, (uint32_t)kKb, 1};
         if (!make_tmap(&tm_x, split ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, 4,
                        dims, strides, box))
@@ -723,6 +776,9 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
             return cudaErrorInvalidValue;
     }
     auto kern = split ? (g.headdim == 64 ? k_state_pass_tc<64, 128, 64, true> : k_state_pass_tc<128, 128, 64, true>)
+                : hp ? (g.chunk == 256 ? k_state_pass_tc<128, 256, 128, false, true>
+                        : g.chunk == 128 ? k_state_pass_tc<128, 128, 128, false, true>
+                                         : k_state_pass_tc<128, 64, 64, false, true>)
                 : (g.headdim == 64)
                     ? (g.chunk == 256 ? (kKb == 128 ? k_state_pass_tc<64, 256, 128, false> : k_state_pass_tc<64, 256, 64, false>)
                        : g.chunk == 128 ? (kKb == 128 ? k_state_pass_tc<64, 128, 128, false> : k_state_pass_tc<64, 128, 64, false>)
@@ -731,7 +787,7 @@ cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStre
                        : g.chunk == 128 ? k_state_pass_tc<128, 128, 128, false> : k_state_pass_tc<128, 64, 64, false>);
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)mtiles, (unsigned)g.nheads, (unsigned)(g.batch * p.seg_grid));
+    dim3 grid((unsigned)mtiles, (unsigned)heads, (unsigned)(g.batch * p.seg_grid));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);

@@ -116,6 +116,39 @@ def test_chunk_out_matches_oracle(spec):
     assert rel_err(np64(y), y_ref) <= TOL[w.dtype]
 
 
+# Heads of 64 columns run in pairs in the state pass (two heads of one group
+# per CTA, as one head of 128 columns) where there are enough (batch, head)
+# pairs; MAMBA2_STATE_PAIRS=1 forces the pairs on these small shapes: chunks
+# of 64, 128 and 256, states of 64, 128 and 256, ragged ends, groups of two
+# and four heads, with and without a carried state.
+PAIR_SHAPES = [
+    ("pairs_t128_s128_init", 2, 640, 4, 64, 128, 1, 128, "bf16", True),
+    ("pairs_t256_s64_groups_ragged", 1, 777, 8, 64, 64, 2, 256, "bf16", False),
+    ("pairs_t64_s256_groups_init", 1, 300, 6, 64, 256, 3, 64, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("spec", PAIR_SHAPES, ids=[s[0] for s in PAIR_SHAPES])
+def test_state_pass_head_pairs(spec, monkeypatch):
+    """Chunk states and final state against the oracle, and equal bit for bit
+    to one head per CTA: each element of the pair's product, fold and scan
+    takes the same operations in the same order as for a single head."""
+    w = _w(*spec)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    G32, cs_ref, fin_ref = _oracle_stage_inputs(inp, w)
+    G = torch.from_numpy(G32).cuda()
+    monkeypatch.setenv("MAMBA2_STATE_PAIRS", "1")
+    cs, fin = bd.mamba2_state_pass(d["x"], d["dt"], d["B"], G, w.chunk_size, initial_state=d["initial_state"])
+    bd.mamba2_check_device_status()
+    assert rel_err(np64(cs), cs_ref) <= TOL[w.dtype]
+    assert rel_err(np64(fin), fin_ref) <= TOL[w.dtype]
+    monkeypatch.setenv("MAMBA2_STATE_PAIRS", "0")
+    cs1, fin1 = bd.mamba2_state_pass(d["x"], d["dt"], d["B"], G, w.chunk_size, initial_state=d["initial_state"])
+    bd.mamba2_check_device_status()
+    assert torch.equal(cs, cs1) and torch.equal(fin, fin1)
+
+
 @pytest.mark.parametrize("spec", [s for s in SHAPES if s[-1]], ids=[s[0] for s in SHAPES if s[-1]])
 def test_state_pass_exact_cases(spec):
     """dt = 0 leaves the state untouched (exp2(0) = 1, added terms exactly 0),
