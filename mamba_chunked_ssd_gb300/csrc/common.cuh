@@ -131,6 +131,9 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
 bool state_pass_tc_fits(const Geom& g);
 bool state_pass_split_fits(const Geom& g);
 cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStream_t st);
+// Whether the tensor-core state pass runs heads of 64 columns in pairs
+// (dispatch.cu).
+bool use_head_pairs(const Geom& g, const StatePassArgs& a);
 // Segments the forward pass splits each sequence into for stage 2 (1: one
 // pass over the whole sequence), the bytes of their states, and the carry
 // between the summary and segment passes.

@@ -22,6 +22,27 @@ cudaError_t launch_chunk_out(const Geom& g, bool bf16, const ChunkOutArgs& a, cu
     return launch_chunk_out_simt(g, bf16, a, st);
 }
 
+// Heads of 64 columns run in pairs (two heads of one group per CTA, as one
+// head of 128 columns, one CTA per SM) where the state has 128 rows or more
+// and single heads would give 256 to 2048 CTAs: the pairs then still give
+// 128 CTAs or more, and beyond that many waves of single heads at two CTAs
+// per SM do better.  Measured on GB300 (whole forward pass, µs, single heads
+// / pairs, CTAs of single heads): long_seq_carried_state (256) 261.5 /
+// 256.3; state 128, L 16384 (256) 500.9 / 489.4; state 256, L 32768 (256)
+// 789.4 / 774.0; state 128, L 4096 (1024) 511.5 / 505.5; state 256, L 4096
+// (2048) 762.9 / 756.5; state 128, L 1024 (4096) 528.1 / 529.8; state 256,
+// L 1024 (8192) 843.0 / 848.6; state 64, L 4096 (1024) 442.1 / 452.3;
+// mamba2_1p3b_layer (128) 50.1 / 60.3.  MAMBA2_STATE_PAIRS=0 or =1 turns
+// the pairs off or on (where they apply), for timing both on one shape.
+bool use_head_pairs(const Geom& g, const StatePassArgs& a) {
+    if (a.split || a.segments > 1 || g.headdim != 64) return false;
+    if (g.nheads % 2 != 0 || g.heads_per_group % 2 != 0) return false;
+    const char* env = getenv("MAMBA2_STATE_PAIRS");
+    if (env && (env[0] == '0' || env[0] == '1') && env[1] == 0) return env[0] == '1';
+    const int64_t ctas = g.batch * g.nheads * ((g.dstate + 127) / 128);  // single heads
+    return g.dstate >= 128 && ctas >= 2 * 128 && ctas <= 2048;
+}
+
 // The fused kernel keeps one CTA per pair of heads of a batch row on the chip
 // for the whole sequence.  Measured on GB300 it is still slower than the
 // separate stages (long-sequence workload: 0.42 ms against 0.31 ms per pass),

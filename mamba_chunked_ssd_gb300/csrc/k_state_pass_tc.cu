@@ -697,27 +697,10 @@ bool state_pass_tc_fits(const Geom& g) {
     return plan(g, p);
 }
 
-// Heads of 64 columns run in pairs (two heads of one group per CTA, as one
-// head of 128 columns, one CTA per SM) where the pairs still give at least
-// 128 CTAs and the state has 128 rows or more.  Measured on GB300 (whole
-// forward pass, µs, single heads / pairs, same box): long_seq_carried_state
-// (256 (batch, head) CTAs) 261.9 / 256.3; sweep state 256, L 4096 (2048)
-// 763 / 758; state 128, L 1024 (4096) 528.6 / 530; state 64, L 16384 (256)
-// 433 / 436; 128 (batch, head) CTAs: mamba2_1p3b_layer 50.1 / 60.2, state
-// 128, L 32768 513 / 657.  MAMBA2_STATE_PAIRS=0 or =1 turns the pairs off
-// or on (where they apply), for timing both on one shape.
-bool use_head_pairs(const Geom& g, const StatePassArgs& a) {
-    if (a.split || a.segments > 1 || g.headdim != 64) return false;
-    if (g.nheads % 2 != 0 || g.heads_per_group % 2 != 0) return false;
-    const char* env = getenv("MAMBA2_STATE_PAIRS");
-    if (env && (env[0] == '0' || env[0] == '1') && env[1] == 0) return env[0] == '1';
-    return g.dstate >= 128 && g.batch * g.nheads * ((g.dstate + 127) / 128) >= 2 * 128;
-}
-
 cudaError_t launch_state_pass_tc(const Geom& g, const StatePassArgs& a, cudaStream_t st) {
     SpTcParams p{};
     p.g = g;
-    const bool hp = use_head_pairs(g, a);
+    const bool hp = use_head_pairs(g, a);  // the rule lives with the other per-shape choices
     const int mtiles = (int)((g.dstate + 127) / 128);
     const int seg_grid = a.segments > 1 ? (a.summary ? a.segments - 1 : a.segments) : 1;
     const int64_t heads = hp ? g.nheads / 2 : g.nheads;  // CTAs along the heads

@@ -22,6 +22,12 @@ be checked against measurements:
   MAMBA2_FWD_CHUNK = given | 64 | 128 | 256   the chunk the forward pass
       runs with: the caller's, or a fixed one (the result does not depend on
       it; the default picks one per shape).
+  MAMBA2_STATE_PAIRS = 0 | 1            the state pass with heads of 64
+      columns one per CTA, or two of one group per CTA as one head of 128
+      columns (where the head count and the group size are even).
+  MAMBA2_CHUNK_OUT_PERSISTENT = 0       stage 3 with one CTA per work item
+      instead of one CTA per SM taking an equal share of the work (where
+      every chunk is one 128-row block: chunks of 128, and of 64 in pairs).
 
 Usage (one GPU):  python -m mamba_chunked_ssd_gb300.tune [--steps K] [--json]
 Each line: workload, candidate, mean stage time in microseconds (CUDA events
@@ -51,6 +57,8 @@ FWD_PATH_ENV = "MAMBA2_FWD_PATH"
 SEGMENTS_ENV = "MAMBA2_STATE_SEGMENTS"
 FP32_ENV = "MAMBA2_FP32_PATH"
 FWD_CHUNK_ENV = "MAMBA2_FWD_CHUNK"
+PAIRS_ENV = "MAMBA2_STATE_PAIRS"
+PERSISTENT_ENV = "MAMBA2_CHUNK_OUT_PERSISTENT"
 
 
 def _time(fn, steps, warmup, flush, stream):
@@ -295,6 +303,42 @@ def profile_run(name, steps):
     print(f"{name}: {steps} forward passes")
 
 
+def env_rows(workloads, env, values, steps=10, warmup=3):
+    """Whole-pass time of each workload with the environment variable `env`
+    set to each of `values` in turn, and with it unset (the default)."""
+    import torch
+    from mamba_chunked_ssd_gb300 import binding as bd
+    from mamba_chunked_ssd_gb300.synthetic import make_inputs
+
+    bd.load_library()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    rows = []
+    saved = os.environ.pop(env, None)
+    try:
+        for w in workloads:
+            d = make_inputs(w, device="cuda")
+            shape = bd.shape_of(d["x"], d["B"], w.chunk_size)
+            ws = torch.empty(max(bd.mamba2_ssd_fwd_workspace_size(shape), 1), device="cuda", dtype=torch.uint8)
+            y = torch.empty_like(d["x"])
+            fn = lambda: bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size,  # noqa: E731
+                                           D=d["D"], initial_state=d["initial_state"], y=y, workspace=ws)
+            r = {"workload": w.name}
+            for v in values:
+                os.environ[env] = v
+                r[v] = _time(fn, steps, warmup, flush, stream)
+            os.environ.pop(env, None)
+            r["default"] = _time(fn, steps, warmup, flush, stream)
+            bd.mamba2_check_device_status()
+            rows.append(r)
+            del d, ws, y
+    finally:
+        os.environ.pop(env, None)
+        if saved is not None:
+            os.environ[env] = saved
+    return rows
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--steps", type=int, default=None)
@@ -318,9 +362,13 @@ def main():
     segs = segment_rows(seg_ws, steps=args.steps)
     f32 = fp32_rows([WORKLOADS["long_seq_fp32_t128"],
                      Workload("fp32_h128_s64", 2, 4096, 16, 128, 64, 2, 128, dtype="fp32")])
+    h64 = [w for w in ws if w.dtype == "bf16" and w.headdim == 64 and w.nheads % 2 == 0
+           and (w.nheads // w.ngroups) % 2 == 0]
+    pairs = env_rows(h64, PAIRS_ENV, ("0", "1"), steps=args.steps)
+    persist = env_rows([w for w in ws if w.dtype == "bf16"], PERSISTENT_ENV, ("0",), steps=args.steps)
     if args.json:
         print(json.dumps({"chunk": chunks, "head_split": rows, "fwd_path": paths, "segments": segs,
-                          "fp32": f32}))
+                          "fp32": f32, "state_pairs": pairs, "persistent": persist}))
         return
     print("Whole forward pass at each chunk it can run:")
     print("| workload (caller's chunk) | 64 (µs) | 128 (µs) | 256 (µs) | default |")
@@ -352,6 +400,18 @@ def main():
     print("|---|---|---|")
     for r in f32:
         print(f"| {r['workload']} | {r['tensor_cores_us']:.1f} | {r['cuda_cores_us']:.1f} |")
+    print()
+    print("State pass with heads of 64 columns single or in pairs (whole forward pass):")
+    print("| workload | single (µs) | pairs (µs) | default (µs) |")
+    print("|---|---|---|---|")
+    for r in pairs:
+        print(f"| {r['workload']} | {r['0']:.1f} | {r['1']:.1f} | {r['default']:.1f} |")
+    print()
+    print("Stage 3 with one CTA per work item vs persistent CTAs (whole forward pass):")
+    print("| workload | one CTA per item (µs) | default (µs) |")
+    print("|---|---|---|")
+    for r in persist:
+        print(f"| {r['workload']} | {r['0']:.1f} | {r['default']:.1f} |")
 
 
 if __name__ == "__main__":
