@@ -238,6 +238,28 @@ def test_stages_under_strong_decay(spec):
         assert rel_err(np64(y[:, :, h]), y_ref[:, :, h]) <= TOL[w.dtype], h
 
 
+@pytest.mark.parametrize("spec", [s for s in STRONG if s[4] == 64], ids=[s[0] for s in STRONG if s[4] == 64])
+def test_state_pass_head_pairs_strong_decay(spec, monkeypatch):
+    """Heads in pairs whose two heads decay at very different rates (each
+    pair mixes a mild head with a strong one): each half keeps its own
+    weights and decay.  Against the oracle, and bit for bit against single
+    heads."""
+    w = _w(*spec)
+    inp = strong_decay(make_inputs(w))
+    d = to_dev(inp)
+    G32, cs_ref, fin_ref = _oracle_stage_inputs(inp, w)
+    Gd = torch.from_numpy(G32).cuda()
+    monkeypatch.setenv("MAMBA2_STATE_PAIRS", "1")
+    cs, fin = bd.mamba2_state_pass(d["x"], d["dt"], d["B"], Gd, w.chunk_size, initial_state=d["initial_state"])
+    bd.mamba2_check_device_status()
+    assert rel_err(np64(cs), cs_ref) <= TOL[w.dtype]
+    assert rel_err(np64(fin), fin_ref) <= TOL[w.dtype]
+    monkeypatch.setenv("MAMBA2_STATE_PAIRS", "0")
+    cs1, fin1 = bd.mamba2_state_pass(d["x"], d["dt"], d["B"], Gd, w.chunk_size, initial_state=d["initial_state"])
+    bd.mamba2_check_device_status()
+    assert torch.equal(cs, cs1) and torch.equal(fin, fin1)
+
+
 # Heads of 128 columns in stage 3: whole (one 128-wide MMA per head) or split
 # into two 64-wide virtual heads; the override selects the variant where it
 # fits, and both must match the oracle.  State 256 with chunk 256 fits only
