@@ -32,15 +32,19 @@ cudaError_t launch_chunk_out(const Geom& g, bool bf16, const ChunkOutArgs& a, cu
 // 789.4 / 774.0; state 128, L 4096 (1024) 511.5 / 505.5; state 256, L 4096
 // (2048) 762.9 / 756.5; state 128, L 1024 (4096) 528.1 / 529.8; state 256,
 // L 1024 (8192) 843.0 / 848.6; state 64, L 4096 (1024) 442.1 / 452.3;
-// mamba2_1p3b_layer (128) 50.1 / 60.3.  MAMBA2_STATE_PAIRS=0 or =1 turns
-// the pairs off or on (where they apply), for timing both on one shape.
+// mamba2_1p3b_layer (128) 50.1 / 60.3.  Chunks of 256 (two 128-token
+// sub-blocks per chunk) lose with pairs: long_seq_carried_state run at chunk
+// 256 306.5 / 310.9, state 128, L 4096 596 / 606, state 256, L 4096 1066 /
+// 1086; so the pairs run at chunk 128 only (the forward pass's usual chunk).
+// MAMBA2_STATE_PAIRS=0 or =1 turns the pairs off or on (where they apply),
+// for timing both on one shape.
 bool use_head_pairs(const Geom& g, const StatePassArgs& a) {
     if (a.split || a.segments > 1 || g.headdim != 64) return false;
     if (g.nheads % 2 != 0 || g.heads_per_group % 2 != 0) return false;
     const char* env = getenv("MAMBA2_STATE_PAIRS");
     if (env && (env[0] == '0' || env[0] == '1') && env[1] == 0) return env[0] == '1';
     const int64_t ctas = g.batch * g.nheads * ((g.dstate + 127) / 128);  // single heads
-    return g.dstate >= 128 && ctas >= 2 * 128 && ctas <= 2048;
+    return g.chunk == 128 && g.dstate >= 128 && ctas >= 2 * 128 && ctas <= 2048;
 }
 
 // The fused kernel keeps one CTA per pair of heads of a batch row on the chip
