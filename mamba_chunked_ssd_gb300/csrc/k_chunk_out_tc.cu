@@ -117,7 +117,7 @@ struct CoTcParams {
     int nhb;          // heads per CTA (all in one group)
     int nstr;         // epilogue head streams (2 for H = 64, 1 for H = 128)
     int head_blocks;  // nheads / nhb
-    int persistent;   // one CTA per SM walks the work items (one row block per chunk)
+    int persistent;   // one CTA per SM takes an equal share of the work (one row block per chunk)
     uint32_t off_C, off_CB10, smem_bytes;
     CoLayout lay[2];  // by row block I
     const float* dt;
@@ -998,7 +998,7 @@ cudaError_t launch_chunk_out_tc(const Geom& g, const ChunkOutArgs& a, cudaStream
                                : (p.T == 256 ? k_chunk_out_tc<128, 256, 1, false> : k_chunk_out_tc<128, 128, 1, false>));
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
-    // One row block per chunk: one CTA per SM walks the work items (unless
+    // One row block per chunk: one CTA per SM takes an equal share (unless
     // MAMBA2_CHUNK_OUT_PERSISTENT=0); else one CTA per item.
     const int64_t gx = (int64_t)p.head_blocks * (p.T / 128) * p.g.nchunks, n_items = gx * g.batch;
     const char* pe = getenv("MAMBA2_CHUNK_OUT_PERSISTENT");
