@@ -217,40 +217,44 @@ k_chunk_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     // shares differ by one head at most.  Every item starts with fresh
     // barriers and ends with the CTA quiescent, so items are independent, and
     // the CTA keeps its tensor memory and skips the turnover between CTAs.
-    const int64_t gx = (int64_t)p.head_blocks * (T / 128) * g.nchunks;
-    const int64_t n_items = gx * g.batch;
-    const int64_t vh_all = g.nheads * VS;               // virtual heads per chunk
-    const int64_t vh_grp = g.heads_per_group * VS;      // virtual heads per group
-    const int64_t n_units = g.batch * g.nchunks * vh_all;
-    int64_t f = p.persistent ? n_units * blockIdx.x / gridDim.x : 0;
-    const int64_t f_end = p.persistent ? n_units * (blockIdx.x + 1) / gridDim.x : 0;
-    int64_t it = p.persistent ? n_items : (int64_t)blockIdx.x + gx * blockIdx.y;
+    // (The counts fit in 32 bits: the host caps b nh nc S below 2^31.)
+    const int gx = p.head_blocks * (T / 128) * (int)g.nchunks;
+    const int vh_all = (int)g.nheads * VS;           // virtual heads per chunk
+    const int vh_grp = (int)g.heads_per_group * VS;  // virtual heads per group
+    // persistent: this CTA's triples [f, f_end); else its one item f
+    int f, f_end;
+    if (p.persistent) {
+        const int64_t n_units = g.batch * g.nchunks * vh_all;
+        f = (int)(n_units * blockIdx.x / gridDim.x);
+        f_end = (int)(n_units * (blockIdx.x + 1) / gridDim.x);
+    } else {
+        f = (int)blockIdx.x + gx * (int)blockIdx.y;
+        f_end = f + 1;
+    }
     bool tmem_held = false;
     uint32_t tmem = 0;
-    for (;;) {
+    while (f < f_end) {
     int64_t b, c;
     int I, vh0, nvh;
     if (p.persistent) {
-        if (f >= f_end) break;
-        const int64_t bc = f / vh_all;
-        const int vh = (int)(f % vh_all);
-        nvh = (int)imin64(f_end - f, (vh / vh_grp + 1) * vh_grp - vh);
+        const int bc = f / vh_all;
+        const int vh = f % vh_all;
+        nvh = min(f_end - f, (vh / vh_grp + 1) * vh_grp - vh);
         vh0 = vh;
-        b = bc / g.nchunks;
-        c = bc % g.nchunks;
+        b = bc / (int)g.nchunks;
+        c = bc % (int)g.nchunks;
         I = 0;
         f += nvh;
     } else {
-        if (it >= n_items) break;
-        const int64_t xi = it % gx;
-        const int hb = (int)(xi % p.head_blocks);
-        const int64_t rest = xi / p.head_blocks;
-        I = (int)(rest % (T / 128));  // row block inside the chunk
+        const int xi = f % gx;
+        const int hb = xi % p.head_blocks;
+        const int rest = xi / p.head_blocks;
+        I = rest % (T / 128);  // row block inside the chunk
         c = rest / (T / 128);
-        b = it / gx;
+        b = f / gx;
         vh0 = hb * p.nhb * VS;
         nvh = p.nhb * VS;
-        it = n_items;
+        f = f_end;
     }
     const int64_t t0 = c * T;
     const int tc = (int)imin64(T, g.seqlen - t0);  // valid tokens of the chunk
