@@ -6,6 +6,7 @@ fixed seed, so a failure names a reproducible case."""
 import random
 
 import pytest
+import torch
 
 import oracle
 from gpu_helpers import TOL, np64, rel_err, to_dev
@@ -62,3 +63,14 @@ def test_random_shape_matches_oracle(w, monkeypatch):
         bd.mamba2_check_device_status()
         assert rel_err(np64(y), r["y"]) <= TOL[w.dtype], chunk
         assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype], chunk
+        # the state pass with heads of 64 columns forced into pairs (where the
+        # head count and the group size allow them) and stage 3 with one CTA
+        # per work item both give the same result bit for bit
+        for env in ("MAMBA2_STATE_PAIRS=1", "MAMBA2_CHUNK_OUT_PERSISTENT=0"):
+            k, v = env.split("=")
+            monkeypatch.setenv(k, v)
+            y1, fin1 = bd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk_size, D=d["D"],
+                                         initial_state=d["initial_state"])
+            bd.mamba2_check_device_status()
+            monkeypatch.delenv(k)
+            assert torch.equal(y1, y) and torch.equal(fin1, fin), (chunk, env)
