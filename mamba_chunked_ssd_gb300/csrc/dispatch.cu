@@ -36,13 +36,17 @@ cudaError_t launch_chunk_out(const Geom& g, bool bf16, const ChunkOutArgs& a, cu
 // sub-blocks per chunk) lose with pairs: long_seq_carried_state run at chunk
 // 256 306.5 / 310.9, state 128, L 4096 596 / 606, state 256, L 4096 1066 /
 // 1086; so the pairs run at chunk 128 only (the forward pass's usual chunk).
+// Over sequence segments (few (batch, head) pairs) they are off: the blog's
+// example problem 124.0 / 122.7, but b 1, L 32768, 4 heads 62.0 / 65.0 and
+// chunk 256 57.1 / 66.7, state 256 with 8 heads 102.7 / 103.3.
 // MAMBA2_STATE_PAIRS=0 or =1 turns the pairs off or on (where they apply),
 // for timing both on one shape.
 bool use_head_pairs(const Geom& g, const StatePassArgs& a) {
-    if (a.split || a.segments > 1 || g.headdim != 64) return false;
+    if (a.split || g.headdim != 64) return false;
     if (g.nheads % 2 != 0 || g.heads_per_group % 2 != 0) return false;
     const char* env = getenv("MAMBA2_STATE_PAIRS");
     if (env && (env[0] == '0' || env[0] == '1') && env[1] == 0) return env[0] == '1';
+    if (a.segments > 1) return false;
     const int64_t ctas = g.batch * g.nheads * ((g.dstate + 127) / 128);  // single heads
     return g.chunk == 128 && g.dstate >= 128 && ctas >= 2 * 128 && ctas <= 2048;
 }

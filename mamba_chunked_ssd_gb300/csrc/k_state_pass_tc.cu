@@ -397,11 +397,12 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // round.  The initial state is the caller's input, so its loads
             // start before the wait for the previous kernel; the entering
             // state of a later segment comes from the carry kernel.
-            auto load_h = [&](const float* h_in) {
+            // (hstride: elements from one head's state to the next head's)
+            auto load_h = [&](const float* h_in, int64_t hstride) {
 #pragma unroll 1
                 for (int m = 0; m < H / 32; ++m) {
                     // columns 32 m .. of the CTA's state: real head hr + (32 m) / HH
-                    const float* src = h_in + ((32 * m) / HH) * S * HH + s * HH + (32 * m) % HH;
+                    const float* src = h_in + ((32 * m) / HH) * hstride + s * HH + (32 * m) % HH;
                     float4 f[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
@@ -423,11 +424,12 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 tc::tmem_wait_st();
             };
             if (seg == 0) {
-                load_h(p.init ? p.init + bh * S * HH : nullptr);
+                load_h(p.init ? p.init + bh * S * HH : nullptr, (int64_t)S * HH);
                 tc::griddep_wait();
             } else {
                 tc::griddep_wait();
-                load_h(p.mode == kSegmentPass ? p.seg_states + (bh * (p.nseg - 1) + seg - 1) * S * HH : nullptr);
+                load_h(p.mode == kSegmentPass ? p.seg_states + (bh * (p.nseg - 1) + seg - 1) * S * HH : nullptr,
+                       (int64_t)(p.nseg - 1) * S * HH);
             }
             // Per chunk: h_{c+1} = exp2(G_last) h_c + U_c into the other h
             // buffer (then U_c's buffer is released to the MMA), then h_c is
@@ -538,16 +540,19 @@ k_state_pass_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // the end state: a summary's into its segment slot, the last
             // segment's into final_state
             float* h_out = nullptr;
-            if (p.mode == kSegmentSummary)
+            int64_t out_stride = (int64_t)S * HH;  // from one head's end state to the next head's
+            if (p.mode == kSegmentSummary) {
                 h_out = p.seg_states + (bh * (p.nseg - 1) + seg) * S * HH;
-            else if (seg == p.nseg - 1 && p.final_state)
+                out_stride = (int64_t)(p.nseg - 1) * S * HH;
+            } else if (seg == p.nseg - 1 && p.final_state) {
                 h_out = p.final_state + bh * S * HH;
+            }
             if (ok && h_out && valid) {
 #pragma unroll 1
                 for (int m = 0; m < H / 16; ++m) {
                     uint32_t hv[16];
                     tc::tmem_ld16(tm_h + (nchl & 1) * H + lane_base + 16 * m, hv);  // h after the last chunk
-                    float4* d4 = reinterpret_cast<float4*>(h_out + ((16 * m) / HH) * S * HH + s * HH + (16 * m) % HH);
+                    float4* d4 = reinterpret_cast<float4*>(h_out + ((16 * m) / HH) * out_stride + s * HH + (16 * m) % HH);
 #pragma unroll
                     for (int s4 = 0; s4 < 4; ++s4)
                         d4[s4] = make_float4(__uint_as_float(hv[4 * s4]), __uint_as_float(hv[4 * s4 + 1]),

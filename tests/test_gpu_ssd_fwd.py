@@ -391,6 +391,25 @@ def test_sequence_segments(w):
     assert rel_err(np64(fin), r["final_state"]) <= TOL[w.dtype]
 
 
+@pytest.mark.parametrize("w", [w for w in SEGMENT_SHAPES if w.headdim == 64] +
+                         [Workload("seg_pairs_groups_strong", 1, 3000, 4, 64, 128, 2, 128, init_state=True)],
+                         ids=lambda w: w.name)
+def test_sequence_segments_head_pairs(w, monkeypatch):
+    """The summary and segment passes with heads of 64 columns in pairs (each
+    half's entering and end states in its own head's rows) give the same y and
+    final state as single heads, bit for bit, also under strong decay."""
+    inp = strong_decay(make_inputs(w)) if "strong" in w.name else make_inputs(w)
+    d = to_dev(inp)
+    monkeypatch.setenv("MAMBA2_STATE_PAIRS", "0")
+    y0, fin0 = _fwd(d, w)
+    monkeypatch.setenv("MAMBA2_STATE_PAIRS", "1")
+    y1, fin1 = _fwd(d, w)
+    assert torch.equal(y0, y1) and torch.equal(fin0, fin1)
+    r = oracle.ssd_recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"],
+                              init=inp["initial_state"])
+    assert rel_err(np64(y1), r["y"]) <= TOL[w.dtype]
+
+
 def test_sequence_segments_strong_decay():
     w = Workload("seg_strong", 1, 2048, 6, 64, 128, 1, 128, init_state=True)
     inp = strong_decay(make_inputs(w))
